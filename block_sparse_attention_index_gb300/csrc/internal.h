@@ -1,0 +1,106 @@
+// Host-side interface between the C ABI layer (msa_api.cu) and the kernel
+// translation units.  Not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace msa {
+
+// Per-(sequence, KV head, split) partial softmax state of decode attention:
+// unnormalised output O[16][128], running max m[16] (log2 domain), sum l[16].
+constexpr int kPartialFloats = 16 * 128 + 16 + 16;
+
+struct ScanArgs {
+    int H;
+    const uint16_t* iq;
+    const uint16_t* ik;
+    const int32_t* cu_rows;
+    const int32_t* cache_lens;
+    const int64_t* cache_starts;
+    int num_seqs;
+    int total_rows;
+    int max_cache_len;
+    int64_t cache_tokens;
+    int max_blocks;
+    int64_t unit_bound;   // upper bound of the number of work units
+    float* pooled;        // [B, H, max_blocks]
+    int32_t* clear_words; // zeroed by the scan (tickets of the attention kernel)
+    int n_clear;
+};
+
+struct DecodeAttendArgs {
+    const CUtensorMap* k_map;  // host copies, passed by value to the kernel
+    const CUtensorMap* v_map;
+    const uint16_t* q;
+    const float* pooled;       // fused path: pooled scores (nullptr when sel is given)
+    int max_blocks;
+    const int32_t* sel_in;     // staged path: given selection
+    const int32_t* nsel_in;
+    const int32_t* cu_rows;
+    const int32_t* cache_lens;
+    const int64_t* cache_starts;
+    int num_seqs, H, G, top_k, total_rows, max_cache_len;
+    int64_t cache_tokens;
+    float scale_log2;          // softmax scale * log2(e)
+    void* out;
+    int out_bf16;
+    float* partials;           // [B, H, top_k, kPartialFloats]
+    int32_t* tickets;          // [B, H], zero on entry
+    int32_t* sel_out;          // nullable
+    int32_t* nsel_out;         // nullable
+    uint32_t* err;
+};
+
+struct StagedArgs {
+    int H, G, top_k, num_seqs, total_rows, max_cache_len;
+    int64_t cache_tokens;
+    const int32_t* cu_rows;
+    const int32_t* cache_lens;
+    const int64_t* cache_starts;
+};
+
+struct PrefillIndexArgs {
+    const CUtensorMap* iq_map;  // iq as (Di, H, rows)
+    const CUtensorMap* ik_map;  // ik as (Di, H, tokens)
+    const int32_t* cu_rows;
+    const int32_t* cache_lens;
+    const int64_t* cache_starts;
+    int num_seqs, H, top_k, total_rows, max_rows_per_seq, max_cache_len;
+    int64_t cache_tokens;
+    int32_t* sel;   // [R, H, top_k]
+    int32_t* nsel;  // [R, H]
+    uint32_t* err;
+};
+
+struct PrefillAttendArgs {
+    const CUtensorMap* q_map;  // q as (D, H*G, rows)
+    const CUtensorMap* k_map;  // k as (D, H, tokens)
+    const CUtensorMap* v_map;
+    const int32_t* sel;
+    const int32_t* nsel;
+    const int32_t* cu_rows;
+    const int32_t* cache_lens;
+    const int64_t* cache_starts;
+    int num_seqs, H, G, top_k, total_rows, max_rows_per_seq, max_cache_len;
+    int64_t cache_tokens;
+    float scale_log2;
+    void* out;
+    int out_bf16;
+    int only_multi_row;  // 1: skip sequences with a single row (fused path)
+    uint32_t* err;
+};
+
+cudaError_t run_decode_scan(const ScanArgs& a, cudaStream_t stream);
+cudaError_t run_decode_attend(const DecodeAttendArgs& a, cudaStream_t stream);
+cudaError_t run_index_scores(const StagedArgs& a, const uint16_t* iq, const uint16_t* ik, float* scores,
+                             int64_t ld, cudaStream_t stream);
+cudaError_t run_select_blocks(const StagedArgs& a, const float* scores, int64_t ld, int32_t* sel, int32_t* nsel,
+                              cudaStream_t stream);
+cudaError_t run_prefill_index(const PrefillIndexArgs& a, cudaStream_t stream);
+cudaError_t run_prefill_attend(const PrefillAttendArgs& a, cudaStream_t stream);
+
+int device_sm_count();
+
+}  // namespace msa

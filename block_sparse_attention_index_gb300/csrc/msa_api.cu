@@ -1,0 +1,479 @@
+// C ABI of the MSA hot path: argument checks, workspace layout, TMA tensor
+// maps and the launch sequence.  See include/msa.h for the contract.
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "../../include/msa.h"
+#include "common.cuh"
+#include "internal.h"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+msa_status fail(msa_status s, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return s;
+}
+
+msa_status cuda_fail(cudaError_t e, const char* what) {
+    return fail(MSA_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+constexpr int64_t kMaxCacheLen = int64_t(1) << 21;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Host-side validation shared by every entry point.
+msa_status check_problem(const msa_problem* p) {
+    if (p == nullptr) return fail(MSA_ERR_INVALID_ARG, "problem is null");
+    if (p->num_seqs < 1) return fail(MSA_ERR_INVALID_ARG, "num_seqs must be >= 1 (got %d)", p->num_seqs);
+    if (p->num_seqs > 65535) return fail(MSA_ERR_UNSUPPORTED, "num_seqs > 65535");
+    if (p->head_dim != msa::kHeadDim) return fail(MSA_ERR_UNSUPPORTED, "head_dim must be 128 (got %d)", p->head_dim);
+    if (p->index_dim != msa::kIndexDim)
+        return fail(MSA_ERR_UNSUPPORTED, "index_dim must be 64 (got %d)", p->index_dim);
+    if (p->block_size != msa::kBlock) return fail(MSA_ERR_UNSUPPORTED, "block_size must be 64 (got %d)", p->block_size);
+    if (p->top_k < 1) return fail(MSA_ERR_INVALID_ARG, "top_k must be >= 1 (got %d)", p->top_k);
+    if (p->top_k > msa::kMaxTopK) return fail(MSA_ERR_UNSUPPORTED, "top_k must be <= 16 (got %d)", p->top_k);
+    if (p->group_size < 1) return fail(MSA_ERR_INVALID_ARG, "group_size must be >= 1");
+    if (p->group_size > msa::kMaxGroup) return fail(MSA_ERR_UNSUPPORTED, "group_size must be <= 16");
+    const int H = p->num_kv_heads;
+    if (H < 1) return fail(MSA_ERR_INVALID_ARG, "num_kv_heads must be >= 1");
+    if (!(H == 1 || H == 2 || H == 4 || H == 8)) return fail(MSA_ERR_UNSUPPORTED, "num_kv_heads must be 1, 2, 4 or 8");
+    if (!std::isfinite(p->softmax_scale) || p->softmax_scale < 0.f)
+        return fail(MSA_ERR_INVALID_ARG, "softmax_scale must be finite and >= 0");
+    if (p->out_dtype != MSA_OUT_F32 && p->out_dtype != MSA_OUT_BF16) return fail(MSA_ERR_INVALID_ARG, "bad out_dtype");
+    if (p->total_rows < p->num_seqs) return fail(MSA_ERR_INVALID_ARG, "total_rows < num_seqs");
+    if (p->max_rows_per_seq < 1 || p->max_rows_per_seq > p->total_rows)
+        return fail(MSA_ERR_INVALID_ARG, "max_rows_per_seq out of range");
+    if (p->max_cache_len < p->max_rows_per_seq) return fail(MSA_ERR_INVALID_ARG, "max_cache_len < max_rows_per_seq");
+    if (p->max_cache_len > kMaxCacheLen) return fail(MSA_ERR_UNSUPPORTED, "max_cache_len > 2^21");
+    if (p->cache_tokens < 1 || p->cache_tokens > INT32_MAX) return fail(MSA_ERR_INVALID_ARG, "cache_tokens out of range");
+    if (p->num_decode_seqs < -1 || p->num_decode_seqs > p->num_seqs)
+        return fail(MSA_ERR_INVALID_ARG, "num_decode_seqs out of range");
+    if (p->max_rows_per_seq == 1 && p->num_decode_seqs != -1 && p->num_decode_seqs != p->num_seqs)
+        return fail(MSA_ERR_INVALID_ARG, "max_rows_per_seq == 1 implies num_decode_seqs == num_seqs");
+    if (!p->cu_rows || !p->cache_lens || !p->cache_starts) return fail(MSA_ERR_INVALID_ARG, "device metadata is null");
+    if (!aligned16(p->cu_rows) && (reinterpret_cast<uintptr_t>(p->cu_rows) & 3u))
+        return fail(MSA_ERR_INVALID_ARG, "cu_rows misaligned");
+    if (reinterpret_cast<uintptr_t>(p->cache_starts) & 7u) return fail(MSA_ERR_INVALID_ARG, "cache_starts misaligned");
+    return MSA_OK;
+}
+
+msa_status check_ptr(const void* ptr, const char* name) {
+    if (ptr == nullptr) return fail(MSA_ERR_INVALID_ARG, "%s is null", name);
+    if (!aligned16(ptr)) return fail(MSA_ERR_INVALID_ARG, "%s is not 16-byte aligned", name);
+    return MSA_OK;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+struct Layout {
+    size_t err = 0, tickets = 0, pooled = 0, partials = 0, sel = 0, nsel = 0, total = 0;
+    size_t header_bytes = 0;  // error word + tickets, cleared at the start of a call
+};
+
+Layout layout_of(const msa_problem* p) {
+    Layout l;
+    const size_t B = p->num_seqs, H = p->num_kv_heads, R = p->total_rows, K = p->top_k;
+    const size_t MB = (static_cast<size_t>(p->max_cache_len) + msa::kBlock - 1) / msa::kBlock;
+    size_t off = 0;
+    l.err = off;
+    off += 16;
+    l.tickets = off;
+    off += B * H * sizeof(int32_t);
+    l.header_bytes = off;
+    off = align256(off);
+    l.pooled = off;
+    off = align256(off + B * H * MB * sizeof(float));
+    l.partials = off;
+    off = align256(off + B * H * K * msa::kPartialFloats * sizeof(float));
+    l.sel = off;
+    off = align256(off + R * H * K * sizeof(int32_t));
+    l.nsel = off;
+    off = align256(off + R * H * sizeof(int32_t));
+    l.total = off;
+    return l;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    });
+    return fn;
+}
+
+// 3-D bf16 tensor (d0 innermost, contiguous) with a box of b0 x b1 x b2 and
+// 128-byte swizzle (b0 * 2 bytes must be 128).
+msa_status make_map(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint32_t b0,
+                    uint32_t b1, uint32_t b2, const char* name) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return fail(MSA_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable from the driver");
+    cuuint64_t dims[3] = {d0, d1, d2};
+    cuuint64_t strides[2] = {d0 * 2, d0 * d1 * 2};
+    cuuint32_t box[3] = {b0, b1, b2};
+    cuuint32_t es[3] = {1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(MSA_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed with %d", name, int(r));
+    return MSA_OK;
+}
+
+msa::StagedArgs staged_args(const msa_problem* p) {
+    msa::StagedArgs a;
+    a.H = p->num_kv_heads;
+    a.G = p->group_size;
+    a.top_k = p->top_k;
+    a.num_seqs = p->num_seqs;
+    a.total_rows = p->total_rows;
+    a.max_cache_len = p->max_cache_len;
+    a.cache_tokens = p->cache_tokens;
+    a.cu_rows = p->cu_rows;
+    a.cache_lens = p->cache_lens;
+    a.cache_starts = p->cache_starts;
+    return a;
+}
+
+float scale_log2(const msa_problem* p) { return p->softmax_scale * 1.4426950408889634f; }
+
+struct Marks {
+    void* const* events;
+    int n;
+    cudaStream_t stream;
+    msa_status mark(int i) {
+        if (events && i < n && events[i]) {
+            cudaError_t e = cudaEventRecord(static_cast<cudaEvent_t>(events[i]), stream);
+            if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
+        }
+        return MSA_OK;
+    }
+};
+
+bool decode_family(const msa_problem* p) { return p->num_decode_seqs != 0; }
+bool prefill_family(const msa_problem* p) {
+    return p->max_rows_per_seq > 1 && p->num_decode_seqs != p->num_seqs;
+}
+
+}  // namespace
+
+int msa::device_sm_count() {
+    static int counts[64] = {0};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    int& c = counts[dev & 63];
+    if (c == 0) {
+        int v = 0;
+        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+        c = v > 0 ? v : 1;
+    }
+    return c;
+}
+
+extern "C" {
+
+const char* msa_status_string(msa_status s) {
+    switch (s) {
+        case MSA_OK: return "MSA_OK";
+        case MSA_ERR_INVALID_ARG: return "MSA_ERR_INVALID_ARG";
+        case MSA_ERR_UNSUPPORTED: return "MSA_ERR_UNSUPPORTED";
+        case MSA_ERR_WORKSPACE: return "MSA_ERR_WORKSPACE";
+        case MSA_ERR_CUDA: return "MSA_ERR_CUDA";
+        case MSA_ERR_INTERNAL: return "MSA_ERR_INTERNAL";
+    }
+    return "MSA_ERR_UNKNOWN";
+}
+
+const char* msa_last_error(void) { return g_last_error.c_str(); }
+
+msa_status msa_workspace_size(const msa_problem* p, size_t* bytes) {
+    g_last_error.clear();
+    msa_status s = check_problem(p);
+    if (s != MSA_OK) return s;
+    if (!bytes) return fail(MSA_ERR_INVALID_ARG, "bytes is null");
+    *bytes = layout_of(p).total;
+    return MSA_OK;
+}
+
+msa_status msa_index_scores(const msa_problem* p, const void* iq, const void* ik_cache, float* scores, int64_t ld,
+                            void* stream) {
+    g_last_error.clear();
+    msa_status s;
+    if ((s = check_problem(p)) != MSA_OK) return s;
+    if ((s = check_ptr(iq, "iq")) != MSA_OK || (s = check_ptr(ik_cache, "ik_cache")) != MSA_OK ||
+        (s = check_ptr(scores, "scores")) != MSA_OK)
+        return s;
+    if (ld < p->max_cache_len) return fail(MSA_ERR_INVALID_ARG, "ld < max_cache_len");
+    cudaError_t e = msa::run_index_scores(staged_args(p), static_cast<const uint16_t*>(iq),
+                                          static_cast<const uint16_t*>(ik_cache), scores, ld,
+                                          static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? MSA_OK : cuda_fail(e, "index scores launch");
+}
+
+msa_status msa_select_blocks(const msa_problem* p, const float* scores, int64_t ld, int32_t* sel, int32_t* nsel,
+                             void* stream) {
+    g_last_error.clear();
+    msa_status s;
+    if ((s = check_problem(p)) != MSA_OK) return s;
+    if ((s = check_ptr(scores, "scores")) != MSA_OK || (s = check_ptr(sel, "sel")) != MSA_OK ||
+        (s = check_ptr(nsel, "nsel")) != MSA_OK)
+        return s;
+    if (ld < p->max_cache_len) return fail(MSA_ERR_INVALID_ARG, "ld < max_cache_len");
+    cudaError_t e = msa::run_select_blocks(staged_args(p), scores, ld, sel, nsel, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? MSA_OK : cuda_fail(e, "select blocks launch");
+}
+
+static msa_status check_workspace(const msa_problem* p, const void* ws, size_t ws_bytes, Layout* l) {
+    *l = layout_of(p);
+    if (ws == nullptr) return fail(MSA_ERR_WORKSPACE, "workspace is null");
+    if (reinterpret_cast<uintptr_t>(ws) & 255u) return fail(MSA_ERR_WORKSPACE, "workspace is not 256-byte aligned");
+    if (ws_bytes < l->total) return fail(MSA_ERR_WORKSPACE, "workspace has %zu bytes, needs %zu", ws_bytes, l->total);
+    return MSA_OK;
+}
+
+static msa_status attend_common(const msa_problem* p, const void* q, const void* k_cache, const void* v_cache,
+                                const int32_t* sel, const int32_t* nsel, void* out, void* ws, size_t ws_bytes,
+                                Layout* l) {
+    msa_status s;
+    if ((s = check_problem(p)) != MSA_OK) return s;
+    if ((s = check_ptr(q, "q")) != MSA_OK || (s = check_ptr(k_cache, "k_cache")) != MSA_OK ||
+        (s = check_ptr(v_cache, "v_cache")) != MSA_OK || (s = check_ptr(sel, "sel")) != MSA_OK ||
+        (s = check_ptr(nsel, "nsel")) != MSA_OK || (s = check_ptr(out, "out")) != MSA_OK)
+        return s;
+    return check_workspace(p, ws, ws_bytes, l);
+}
+
+static msa::DecodeAttendArgs decode_args(const msa_problem* p, const CUtensorMap* km, const CUtensorMap* vm,
+                                         const void* q, void* out, uint8_t* ws, const Layout& l) {
+    msa::DecodeAttendArgs a{};
+    a.k_map = km;
+    a.v_map = vm;
+    a.q = static_cast<const uint16_t*>(q);
+    a.max_blocks = static_cast<int>((p->max_cache_len + msa::kBlock - 1) / msa::kBlock);
+    a.cu_rows = p->cu_rows;
+    a.cache_lens = p->cache_lens;
+    a.cache_starts = p->cache_starts;
+    a.num_seqs = p->num_seqs;
+    a.H = p->num_kv_heads;
+    a.G = p->group_size;
+    a.top_k = p->top_k;
+    a.total_rows = p->total_rows;
+    a.max_cache_len = p->max_cache_len;
+    a.cache_tokens = p->cache_tokens;
+    a.scale_log2 = scale_log2(p);
+    a.out = out;
+    a.out_bf16 = p->out_dtype == MSA_OUT_BF16;
+    a.partials = reinterpret_cast<float*>(ws + l.partials);
+    a.tickets = reinterpret_cast<int32_t*>(ws + l.tickets);
+    a.err = reinterpret_cast<uint32_t*>(ws + l.err);
+    return a;
+}
+
+msa_status msa_attend_decode(const msa_problem* p, const void* q, const void* k_cache, const void* v_cache,
+                             const int32_t* sel, const int32_t* nsel, void* out, void* workspace,
+                             size_t workspace_bytes, void* stream) {
+    g_last_error.clear();
+    Layout l;
+    msa_status s = attend_common(p, q, k_cache, v_cache, sel, nsel, out, workspace, workspace_bytes, &l);
+    if (s != MSA_OK) return s;
+    if (p->max_rows_per_seq != 1)
+        return fail(MSA_ERR_INVALID_ARG, "msa_attend_decode needs one row per sequence (max_rows_per_seq == 1)");
+    const uint64_t T = p->cache_tokens, H = p->num_kv_heads;
+    CUtensorMap km, vm;
+    if ((s = make_map(&km, k_cache, 128, H, T, 64, 1, 64, "k_cache")) != MSA_OK) return s;
+    if ((s = make_map(&vm, v_cache, 128, H, T, 64, 1, 64, "v_cache")) != MSA_OK) return s;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    cudaError_t e = cudaMemsetAsync(ws, 0, l.header_bytes, st);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
+    msa::DecodeAttendArgs a = decode_args(p, &km, &vm, q, out, ws, l);
+    a.pooled = nullptr;
+    a.sel_in = sel;
+    a.nsel_in = nsel;
+    e = msa::run_decode_attend(a, st);
+    return e == cudaSuccess ? MSA_OK : cuda_fail(e, "decode attention launch");
+}
+
+static msa::PrefillAttendArgs prefill_attend_args(const msa_problem* p, const CUtensorMap* qm, const CUtensorMap* km,
+                                                  const CUtensorMap* vm, const int32_t* sel, const int32_t* nsel,
+                                                  void* out, uint8_t* ws, const Layout& l) {
+    msa::PrefillAttendArgs a{};
+    a.q_map = qm;
+    a.k_map = km;
+    a.v_map = vm;
+    a.sel = sel;
+    a.nsel = nsel;
+    a.cu_rows = p->cu_rows;
+    a.cache_lens = p->cache_lens;
+    a.cache_starts = p->cache_starts;
+    a.num_seqs = p->num_seqs;
+    a.H = p->num_kv_heads;
+    a.G = p->group_size;
+    a.top_k = p->top_k;
+    a.total_rows = p->total_rows;
+    a.max_rows_per_seq = p->max_rows_per_seq;
+    a.max_cache_len = p->max_cache_len;
+    a.cache_tokens = p->cache_tokens;
+    a.scale_log2 = scale_log2(p);
+    a.out = out;
+    a.out_bf16 = p->out_dtype == MSA_OUT_BF16;
+    a.err = reinterpret_cast<uint32_t*>(ws + l.err);
+    return a;
+}
+
+static msa_status attention_maps(const msa_problem* p, const void* q, const void* k, const void* v, CUtensorMap* qm,
+                                 CUtensorMap* km, CUtensorMap* vm) {
+    const uint64_t T = p->cache_tokens, H = p->num_kv_heads, R = p->total_rows;
+    const uint64_t HQ = static_cast<uint64_t>(p->num_kv_heads) * p->group_size;
+    msa_status s;
+    if (qm && (s = make_map(qm, q, 128, HQ, R, 64, 16, 1, "q")) != MSA_OK) return s;
+    if ((s = make_map(km, k, 128, H, T, 64, 1, 64, "k_cache")) != MSA_OK) return s;
+    return make_map(vm, v, 128, H, T, 64, 1, 64, "v_cache");
+}
+
+msa_status msa_attend_prefill(const msa_problem* p, const void* q, const void* k_cache, const void* v_cache,
+                              const int32_t* sel, const int32_t* nsel, void* out, void* workspace,
+                              size_t workspace_bytes, void* stream) {
+    g_last_error.clear();
+    Layout l;
+    msa_status s = attend_common(p, q, k_cache, v_cache, sel, nsel, out, workspace, workspace_bytes, &l);
+    if (s != MSA_OK) return s;
+    CUtensorMap qm, km, vm;
+    if ((s = attention_maps(p, q, k_cache, v_cache, &qm, &km, &vm)) != MSA_OK) return s;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    cudaError_t e = cudaMemsetAsync(ws, 0, l.header_bytes, st);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
+    msa::PrefillAttendArgs a = prefill_attend_args(p, &qm, &km, &vm, sel, nsel, out, ws, l);
+    a.only_multi_row = 0;
+    e = msa::run_prefill_attend(a, st);
+    return e == cudaSuccess ? MSA_OK : cuda_fail(e, "prefill attention launch");
+}
+
+int32_t msa_forward_launches(const msa_problem* p) {
+    if (check_problem(p) != MSA_OK) return -1;
+    return (decode_family(p) ? 2 : 0) + (prefill_family(p) ? 2 : 0);
+}
+
+msa_status msa_forward_marked(const msa_problem* p, const void* q, const void* iq, const void* k_cache,
+                              const void* v_cache, const void* ik_cache, void* out, int32_t* sel_out,
+                              int32_t* nsel_out, void* workspace, size_t workspace_bytes, void* stream,
+                              void* const* events, int32_t n_events) {
+    g_last_error.clear();
+    msa_status s;
+    if ((s = check_problem(p)) != MSA_OK) return s;
+    if ((s = check_ptr(q, "q")) != MSA_OK || (s = check_ptr(iq, "iq")) != MSA_OK ||
+        (s = check_ptr(k_cache, "k_cache")) != MSA_OK || (s = check_ptr(v_cache, "v_cache")) != MSA_OK ||
+        (s = check_ptr(ik_cache, "ik_cache")) != MSA_OK || (s = check_ptr(out, "out")) != MSA_OK)
+        return s;
+    if ((sel_out == nullptr) != (nsel_out == nullptr))
+        return fail(MSA_ERR_INVALID_ARG, "sel_out and nsel_out must both be given or both be null");
+    if (sel_out && ((s = check_ptr(sel_out, "sel_out")) != MSA_OK || (s = check_ptr(nsel_out, "nsel_out")) != MSA_OK))
+        return s;
+    if (n_events < 0 || n_events > 5) return fail(MSA_ERR_INVALID_ARG, "n_events must be in [0, 5]");
+    Layout l;
+    if ((s = check_workspace(p, workspace, workspace_bytes, &l)) != MSA_OK) return s;
+
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    Marks marks{events, n_events, st};
+    const bool dec = decode_family(p), pre = prefill_family(p);
+    int32_t* sel = sel_out ? sel_out : reinterpret_cast<int32_t*>(ws + l.sel);
+    int32_t* nsel = nsel_out ? nsel_out : reinterpret_cast<int32_t*>(ws + l.nsel);
+    const uint64_t T = p->cache_tokens, H = p->num_kv_heads;
+    const int max_blocks = static_cast<int>((p->max_cache_len + msa::kBlock - 1) / msa::kBlock);
+
+    CUtensorMap km, vm, qm, iqm, ikm;
+    if ((s = attention_maps(p, q, k_cache, v_cache, pre ? &qm : nullptr, &km, &vm)) != MSA_OK) return s;
+    if (pre) {
+        if ((s = make_map(&iqm, iq, 64, H, p->total_rows, 64, 1, 128, "iq")) != MSA_OK) return s;
+        if ((s = make_map(&ikm, ik_cache, 64, H, T, 64, 1, 256, "ik_cache")) != MSA_OK) return s;
+    }
+    if ((s = marks.mark(0)) != MSA_OK) return s;
+    cudaError_t e;
+    if (dec) {
+        msa::ScanArgs sa{};
+        sa.H = p->num_kv_heads;
+        sa.iq = static_cast<const uint16_t*>(iq);
+        sa.ik = static_cast<const uint16_t*>(ik_cache);
+        sa.cu_rows = p->cu_rows;
+        sa.cache_lens = p->cache_lens;
+        sa.cache_starts = p->cache_starts;
+        sa.num_seqs = p->num_seqs;
+        sa.total_rows = p->total_rows;
+        sa.max_cache_len = p->max_cache_len;
+        sa.cache_tokens = p->cache_tokens;
+        sa.max_blocks = max_blocks;
+        const int64_t nd = p->num_decode_seqs >= 0 ? p->num_decode_seqs : p->num_seqs;
+        sa.unit_bound = nd * max_blocks;
+        sa.pooled = reinterpret_cast<float*>(ws + l.pooled);
+        sa.clear_words = reinterpret_cast<int32_t*>(ws + l.err);
+        sa.n_clear = static_cast<int>(l.header_bytes / sizeof(int32_t));
+        if ((e = msa::run_decode_scan(sa, st)) != cudaSuccess) return cuda_fail(e, "decode scan launch");
+        if ((s = marks.mark(1)) != MSA_OK) return s;
+        msa::DecodeAttendArgs da = decode_args(p, &km, &vm, q, out, ws, l);
+        da.pooled = sa.pooled;
+        da.max_blocks = max_blocks;
+        da.sel_out = sel;
+        da.nsel_out = nsel;
+        if ((e = msa::run_decode_attend(da, st)) != cudaSuccess) return cuda_fail(e, "decode attention launch");
+        if ((s = marks.mark(2)) != MSA_OK) return s;
+    } else {
+        if ((e = cudaMemsetAsync(ws, 0, l.header_bytes, st)) != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
+        if ((s = marks.mark(1)) != MSA_OK || (s = marks.mark(2)) != MSA_OK) return s;
+    }
+    if (pre) {
+        msa::PrefillIndexArgs ia{};
+        ia.iq_map = &iqm;
+        ia.ik_map = &ikm;
+        ia.cu_rows = p->cu_rows;
+        ia.cache_lens = p->cache_lens;
+        ia.cache_starts = p->cache_starts;
+        ia.num_seqs = p->num_seqs;
+        ia.H = p->num_kv_heads;
+        ia.top_k = p->top_k;
+        ia.total_rows = p->total_rows;
+        ia.max_rows_per_seq = p->max_rows_per_seq;
+        ia.max_cache_len = p->max_cache_len;
+        ia.cache_tokens = p->cache_tokens;
+        ia.sel = sel;
+        ia.nsel = nsel;
+        ia.err = reinterpret_cast<uint32_t*>(ws + l.err);
+        if ((e = msa::run_prefill_index(ia, st)) != cudaSuccess) return cuda_fail(e, "prefill indexer launch");
+        if ((s = marks.mark(3)) != MSA_OK) return s;
+        msa::PrefillAttendArgs pa = prefill_attend_args(p, &qm, &km, &vm, sel, nsel, out, ws, l);
+        pa.only_multi_row = 1;
+        if ((e = msa::run_prefill_attend(pa, st)) != cudaSuccess) return cuda_fail(e, "prefill attention launch");
+        if ((s = marks.mark(4)) != MSA_OK) return s;
+    } else {
+        if ((s = marks.mark(3)) != MSA_OK || (s = marks.mark(4)) != MSA_OK) return s;
+    }
+    return MSA_OK;
+}
+
+msa_status msa_forward(const msa_problem* p, const void* q, const void* iq, const void* k_cache,
+                       const void* v_cache, const void* ik_cache, void* out, int32_t* sel_out, int32_t* nsel_out,
+                       void* workspace, size_t workspace_bytes, void* stream) {
+    return msa_forward_marked(p, q, iq, k_cache, v_cache, ik_cache, out, sel_out, nsel_out, workspace,
+                              workspace_bytes, stream, nullptr, 0);
+}
+
+}  // extern "C"

@@ -1,0 +1,129 @@
+// CTA-wide top-k block selection with the forced local block.
+//
+// Rule ("MiniMax-M3 on 4x RTX PRO 6000 Blackwell (SM120)", "What this fixes":
+// per-GQA-group top-16 block selection, max-pool scoring, forced local
+// block; PR #1388 "minimax_m3: a CUDA backend ...": top-16 selection per row
+// and key head): keep the local block J plus the (top_k - 1) best blocks
+// j < J under (pooled score descending, block index ascending); keep every
+// block 0..J when J < top_k; list the kept blocks ascending.
+//
+// Each candidate j is a distinct 64-bit key (ordered score, ~j), so the
+// result does not depend on thread order:
+//   1. every thread takes the largest key among its strided candidates;
+//   2. tau = the (k)-th largest of those per-thread maxima (rank counting) --
+//      tau is a lower bound of the k-th largest key overall, because the
+//      per-thread maxima are k distinct candidates;
+//   3. candidates >= tau are gathered (a handful for typical data) and
+//      ranked exactly by counting; the k best are placed by rank;
+//   4. if more than kCandCap candidates pass the threshold (adversarial
+//      inputs), k rounds of CTA-wide arg-max give the same answer.
+#pragma once
+
+#include "common.cuh"
+
+namespace msa {
+
+constexpr int kCandCap = 512;
+
+template <int NT>
+struct SelectSmem {
+    uint64_t thread_max[NT];
+    uint64_t cand[kCandCap];
+    uint64_t red[NT / 32];
+    uint64_t tau;
+    int32_t picked[kMaxTopK];
+    int32_t count;
+};
+
+// Largest key among candidates j < J with key < below (0 if none).
+template <int NT>
+__device__ __forceinline__ uint64_t cta_argmax_below(const float* pooled, int J, uint64_t below, SelectSmem<NT>& sm) {
+    uint64_t best = 0;
+    for (int j = threadIdx.x; j < J; j += NT) {
+        uint64_t key = block_key(pooled[j], j);
+        if (key < below && key > best) best = key;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        uint64_t other = __shfl_xor_sync(0xffffffffu, best, o);
+        best = other > best ? other : best;
+    }
+    if ((threadIdx.x & 31) == 0) sm.red[threadIdx.x >> 5] = best;
+    __syncthreads();
+    uint64_t r = 0;
+#pragma unroll
+    for (int w = 0; w < NT / 32; ++w) r = sm.red[w] > r ? sm.red[w] : r;
+    __syncthreads();
+    return r;
+}
+
+// Selects from pooled[0..J) (+ the local block J).  All NT threads call it.
+// Writes the kept blocks ascending to sel[0..top_k) (-1 padded; sel may be
+// shared or global memory, written by threads < top_k) and returns nsel.
+template <int NT>
+__device__ int cta_select(const float* pooled, int J, int top_k, int* sel, SelectSmem<NT>& sm) {
+    const int tid = threadIdx.x;
+    const int others = min(top_k - 1, J);
+    if (others == J) {  // every causal block is kept
+        if (tid < top_k) sel[tid] = tid <= J ? tid : -1;
+        __syncthreads();
+        return J + 1;
+    }
+    // 1. per-thread maxima
+    uint64_t mine = 0;
+    for (int j = tid; j < J; j += NT) {
+        uint64_t key = block_key(pooled[j], j);
+        mine = key > mine ? key : mine;
+    }
+    sm.thread_max[tid] = mine;
+    if (tid == 0) sm.count = 0;
+    __syncthreads();
+    // 2. tau = the others-th largest per-thread maximum (others >= 1 here)
+    if (mine != 0) {
+        int rank = 0;
+        for (int u = 0; u < NT; ++u) rank += sm.thread_max[u] > mine;
+        if (rank == others - 1) sm.tau = mine;
+    }
+    __syncthreads();
+    const uint64_t tau = sm.tau;
+    // 3. gather candidates >= tau
+    for (int j = tid; j < J; j += NT) {
+        uint64_t key = block_key(pooled[j], j);
+        if (key >= tau) {
+            int slot = atomicAdd(&sm.count, 1);
+            if (slot < kCandCap) sm.cand[slot] = key;
+        }
+    }
+    __syncthreads();
+    const int n = sm.count;
+    if (n <= kCandCap) {
+        for (int c = tid; c < n; c += NT) {
+            uint64_t key = sm.cand[c];
+            int rank = 0;
+            for (int u = 0; u < n; ++u) rank += sm.cand[u] > key;
+            if (rank < others) sm.picked[rank] = key_block(key);
+        }
+        __syncthreads();
+    } else {
+        uint64_t below = ~0ull;
+        for (int i = 0; i < others; ++i) {
+            below = cta_argmax_below<NT>(pooled, J, below, sm);
+            if (tid == 0) sm.picked[i] = key_block(below);
+        }
+        __syncthreads();
+    }
+    // 4. picked[0..others) + J, ascending (J is the largest)
+    if (tid <= others) {
+        int v = tid < others ? sm.picked[tid] : J;
+        int pos = 0;
+        for (int u = 0; u < others; ++u) pos += sm.picked[u] < v;
+        if (tid == others) pos = others;
+        sel[pos] = v;
+    } else if (tid < top_k) {
+        sel[tid] = -1;
+    }
+    __syncthreads();
+    return others + 1;
+}
+
+}  // namespace msa

@@ -1,0 +1,187 @@
+/*
+ * msa.h -- C ABI of the GB300 (sm_103a) block-sparse attention (MSA) hot path.
+ *
+ * The method (MiniMax-M3 sparse attention, as the pages describe it):
+ *   "MiniMax-M3 on 4x RTX PRO 6000 Blackwell (SM120)", section "What this
+ *   fixes": the MSA model does per-GQA-group top-16 block selection with
+ *   max-pool scoring and a forced local block.
+ *   "minimax_m3: a CUDA backend for MiniMax-M3.1-Flash at TP over GB10s"
+ *   (PR #1388), commit text of the native Metal family: lightning-indexer
+ *   index scores and top-16 block selection per row and key head; decode
+ *   attention over the kept blocks in partials; prompt chunks on the tensor
+ *   units over each tile's kept blocks.  Same PR, prompt-tile commit: a tile
+ *   holds the 16 query heads of one key head, which share their rows'
+ *   selection, so each key/value block is read once for all of them.  Same
+ *   PR, cache commit: keys, values and index keys are cached as bf16.
+ *
+ * For every query row r (absolute position p) and KV head h:
+ *   s_t  = iq[r,h,:] . ik[t,h,:]                     t = 0..p        (indexer)
+ *   m_j  = max { s_t : t in block j, t <= p }        j = 0..J, J = p / S
+ *   K    = {J} + the (top_k-1) best j < J by (m_j desc, j asc); all j <= J
+ *          when J < top_k; listed ascending
+ *   out[r, h*G+g] = softmax_t(scale * q[r,h*G+g] . k[t,h]) . v[t,h]
+ *          over t in the blocks of K with t <= p
+ *
+ * Conventions for every entry point
+ *   - All tensors are device pointers (cudaMalloc'd or equivalent) owned by
+ *     the caller.  The library allocates no device or pinned memory; scratch
+ *     space comes from the caller's workspace (msa_workspace_size).
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
+ *     default stream) and launch only the library's own kernels.  No call
+ *     synchronises the device or reads device memory on the host, so every
+ *     call can be enqueued back to back.
+ *   - bf16 is IEEE-754 binary16 "brain float" bits (uint16_t); fp32 is float.
+ *   - Layouts are contiguous, row-major:
+ *       q    [total_rows, H*G, D]   bf16   q head g of KV head h is h*G+g
+ *       iq   [total_rows, H, Di]    bf16
+ *       k, v [cache_tokens, H, D]   bf16   token t of sequence b is row
+ *       ik   [cache_tokens, H, Di]  bf16   cache_starts[b] + t
+ *       out  [total_rows, H*G, D]   fp32 or bf16 (msa_problem.out_dtype)
+ *       sel  [total_rows, H, top_k] int32, kept blocks ascending, -1 padded
+ *       nsel [total_rows, H]        int32, number of kept blocks
+ *     Every pointer must be 16-byte aligned.
+ *   - Rows of sequence b are cu_rows[b] .. cu_rows[b+1]-1.  With n rows and
+ *     cache length L (the rows' own tokens included), row i is at p = L-n+i.
+ *   - Errors: invalid or unsupported arguments are rejected on the host
+ *     before anything is enqueued (MSA_ERR_INVALID_ARG, MSA_ERR_UNSUPPORTED,
+ *     MSA_ERR_WORKSPACE).  A failed launch returns MSA_ERR_CUDA.  Device
+ *     metadata (cu_rows, cache_lens, cache_starts) is read only by kernels:
+ *     values inconsistent with the host-side bounds in msa_problem are the
+ *     caller's error; kernels clamp them so that they never read or write
+ *     out of the stated extents, and the affected outputs are unspecified.
+ *     msa_last_error() returns a message for the calling thread's last
+ *     failure.  Nothing traps on the device.
+ *   - Supported set: D = 128, Di = 64, S = 64, 1 <= top_k <= 16,
+ *     1 <= G <= 16, H in {1, 2, 4, 8}, max_cache_len <= 2^21,
+ *     num_seqs <= 65535; other values return MSA_ERR_UNSUPPORTED.
+ *   - Thread safety: calls from several host threads are safe; the only
+ *     library state is a per-device set-up flag and the thread-local error
+ *     message.  Two calls sharing one workspace must be ordered on the GPU.
+ */
+#ifndef MSA_H_
+#define MSA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum msa_status {
+    MSA_OK = 0,
+    MSA_ERR_INVALID_ARG = 1, /* null pointer, bad size, bad alignment        */
+    MSA_ERR_UNSUPPORTED = 2, /* valid, but outside the supported set         */
+    MSA_ERR_WORKSPACE = 3,   /* workspace null or smaller than required      */
+    MSA_ERR_CUDA = 4,        /* a CUDA runtime/driver call or launch failed  */
+    MSA_ERR_INTERNAL = 5     /* a library invariant failed                   */
+} msa_status;
+
+enum { MSA_OUT_F32 = 0, MSA_OUT_BF16 = 1 };
+
+/* One batch: B sequences, each with n_b >= 1 query rows and a cache of L_b
+ * tokens (n_b <= L_b).  Host fields size grids and workspaces; device
+ * fields are read by the kernels. */
+typedef struct msa_problem {
+    int32_t num_seqs;         /* B >= 1                                        */
+    int32_t num_kv_heads;     /* H                                             */
+    int32_t group_size;       /* G, query heads per KV head                    */
+    int32_t head_dim;         /* D = 128                                       */
+    int32_t index_dim;        /* Di = 64                                       */
+    int32_t block_size;       /* S = 64                                        */
+    int32_t top_k;            /* kept blocks per row and KV head, local incl.  */
+    float softmax_scale;      /* finite, >= 0; typically 1/sqrt(D)             */
+    int32_t out_dtype;        /* MSA_OUT_F32 or MSA_OUT_BF16                   */
+    int32_t total_rows;       /* R = cu_rows[B] (host copy)                    */
+    int32_t max_rows_per_seq; /* >= every n_b (host bound); 1 = pure decode    */
+    int32_t max_cache_len;    /* >= every L_b (host bound)                     */
+    int64_t cache_tokens;     /* rows in each of k, v, ik (host), < 2^31       */
+    int32_t num_decode_seqs;  /* host count of sequences with exactly one row,
+                                 or -1 if unknown (then both kernel families
+                                 run and each skips the other's sequences)   */
+    const int32_t* cu_rows;      /* device [B+1], cu_rows[0] = 0, ascending    */
+    const int32_t* cache_lens;   /* device [B], 1 <= L_b <= max_cache_len      */
+    const int64_t* cache_starts; /* device [B], start + L_b <= cache_tokens    */
+} msa_problem;
+
+/* Human-readable name of a status code (static string). */
+const char* msa_status_string(msa_status status);
+
+/* Message describing the calling thread's most recent failure ("" if none). */
+const char* msa_last_error(void);
+
+/* Bytes of scratch that msa_forward, msa_attend_decode and msa_attend_prefill
+ * need for problem p (host only; enqueues nothing).  The workspace must be
+ * 256-byte aligned; its contents need no initialisation and are clobbered.
+ * Its first 4 bytes are the device error word of the last call that used
+ * it: 0, or a bitwise OR of 1 (a bounded wait gave up), 2 (device metadata
+ * outside the host-side bounds), 4 (tensor memory could not be allocated);
+ * valid once that call has completed on the stream. */
+msa_status msa_workspace_size(const msa_problem* p, size_t* bytes);
+
+/* Stage 1 alone: the lightning-indexer scores
+ *   scores[r, h, t] = iq[r,h,:] . ik[t,h,:]   (fp32)   for t <= p,
+ *   scores[r, h, t] = -inf                             for p < t < ld.
+ * scores is [total_rows, H, ld] fp32 with ld >= max_cache_len.  fp32
+ * accumulation: exact when the products and partial sums are integers below
+ * 2^24 in magnitude (index values in [-8, 8] give |s| <= 4096).  This staged
+ * path materialises every score and exists for stage-by-stage checking; the
+ * fused path (msa_forward) never writes them. */
+msa_status msa_index_scores(const msa_problem* p, const void* iq, const void* ik_cache,
+                            float* scores, int64_t ld, void* stream);
+
+/* Stage 2 alone: block max-pool of `scores` (as written by msa_index_scores,
+ * entries past p ignored) and top-k selection with the forced local block,
+ * ties to the lower block index.  Writes sel and nsel. */
+msa_status msa_select_blocks(const msa_problem* p, const float* scores, int64_t ld,
+                             int32_t* sel, int32_t* nsel, void* stream);
+
+/* Stage 3, decode form: every sequence has exactly one row
+ * (max_rows_per_seq == 1).  Each kept block is one split whose partial
+ * softmax state (running max, sum, unnormalised output) is combined by
+ * log-sum-exp in the last split to finish.  sel/nsel as msa_select_blocks
+ * writes them (entries must be causal blocks <= J, ascending, distinct).
+ * Needs msa_workspace_size bytes of workspace. */
+msa_status msa_attend_decode(const msa_problem* p, const void* q, const void* k_cache,
+                             const void* v_cache, const int32_t* sel, const int32_t* nsel,
+                             void* out, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Stage 3, prompt-chunk form (any rows per sequence): tcgen05 tensor-core
+ * tiles in which the G query heads of one KV head share each key/value block
+ * read; accumulators live in tensor memory.  Same arguments as the decode
+ * form. */
+msa_status msa_attend_prefill(const msa_problem* p, const void* q, const void* k_cache,
+                              const void* v_cache, const int32_t* sel, const int32_t* nsel,
+                              void* out, void* workspace, size_t workspace_bytes, void* stream);
+
+/* The fused hot path: all three stages for every row of the batch.
+ * Sequences with one row take the decode kernels (index-key scan with the
+ * block max-pool fused in, then selection + split attention + combine);
+ * sequences with more rows take the prompt-chunk kernels (tcgen05 indexer
+ * with the pool and a running top-k in its epilogue, then tcgen05
+ * attention).  No scores are materialised.  sel_out/nsel_out (nullable)
+ * receive the selection. */
+msa_status msa_forward(const msa_problem* p, const void* q, const void* iq, const void* k_cache,
+                       const void* v_cache, const void* ik_cache, void* out, int32_t* sel_out,
+                       int32_t* nsel_out, void* workspace, size_t workspace_bytes, void* stream);
+
+/* msa_forward with timing marks: events[i] (cudaEvent_t, created by the
+ * caller, may be NULL) is recorded on `stream` at mark i:
+ *   0 before the first kernel, 1 after the decode index scan, 2 after decode
+ *   attention, 3 after the prompt-chunk indexer, 4 after prompt-chunk
+ *   attention.  Marks of a path with no rows are recorded back to back.
+ * n_events <= 5. */
+msa_status msa_forward_marked(const msa_problem* p, const void* q, const void* iq,
+                              const void* k_cache, const void* v_cache, const void* ik_cache,
+                              void* out, int32_t* sel_out, int32_t* nsel_out, void* workspace,
+                              size_t workspace_bytes, void* stream, void* const* events,
+                              int32_t n_events);
+
+/* Number of kernels msa_forward launches for p (host only). */
+int32_t msa_forward_launches(const msa_problem* p);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MSA_H_ */
