@@ -1,0 +1,390 @@
+"""Benchmark of the MSA hot path on GB300: one JSON line on stdout.
+
+A step is one msa_forward over one batch of the seeded synthetic workload:
+the index-key scan with the block max-pool, the top-16 selection and the
+attention over the kept blocks.  Default workload: decode batch 4 x 65,536
+cached tokens, 4 KV x 16 query heads (value = decode rows/s); a secondary
+measurement runs the 4,096-row prompt chunk at an 8,192-token prefix
+(prefill rows/s).  Inputs sit in HBM before the timed region; L2 is flushed
+(a 512 MiB write) before every timed step and the flush is not timed.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   (the CPU oracle, timed on the host)
+Under torchrun each rank runs its own copy of the workload on its own GPU
+(decode batches are independent problems: weak scaling, no collective on
+the data path); time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+PROFILES = os.path.join(ROOT, "profiles")
+FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS = 6800.0, 1900.0
+
+
+def _peaks():
+    try:
+        with open(PEAKS_FILE) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), float(p.get("bf16_tflops_sustained", p["bf16_tflops"])), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
+
+
+# ---------------------------------------------------------------- work counts
+
+def _kept_keys(p, top_k=16, S=64):
+    J = p // S
+    if J + 1 <= top_k:
+        return p + 1
+    return (top_k - 1) * S + (p % S) + 1
+
+
+def work_counts(w: synth.Workload):
+    """Algorithmic bytes and FLOPs of one step, by stage."""
+    H, G, D, Di = w.H, w.G, w.D, w.Di
+    dec = [(n, L) for n, L in w.seqs if n == 1]
+    pre = [(n, L) for n, L in w.seqs if n > 1]
+    # decode scan: every cached index key once, the index query, the pooled scores out
+    scan_bytes = sum(L * H * Di * 2 + H * Di * 2 + ((L + 63) // 64) * H * 4 for _, L in dec)
+    # decode attention: kept K/V blocks, q in, out (fp32) out
+    att_bytes = sum(H * (_kept_keys(L - 1, w.top_k) * D * 2 * 2) + H * G * D * (2 + 4) for _, L in dec)
+    # prompt chunks: causal index-score FLOPs and kept-block attention FLOPs
+    idx_flops = 0
+    att_flops = 0
+    for n, L in pre:
+        for i in range(n):
+            p = L - n + i
+            idx_flops += 2 * Di * (p + 1) * H
+            att_flops += 4 * D * _kept_keys(p, w.top_k) * H * G
+    return dict(scan_bytes=scan_bytes, dec_att_bytes=att_bytes, idx_flops=idx_flops, att_flops=att_flops,
+                dec_rows=len(dec), pre_rows=sum(n for n, _ in pre))
+
+
+# ---------------------------------------------------------------- ncu traffic
+
+def _kernel_source_hash(files):
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, "block_sparse_attention_index_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(summary_name, kernel_files):
+    """dram bytes per launch from a committed ncu summary, or None when the
+    summary is missing or the kernel source changed since it was taken."""
+    path = os.path.join(PROFILES, summary_name)
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    m = re.search(r"dram_bytes_per_launch:\s*([0-9]+)", text)
+    s = re.search(r"source_sha256_16:\s*([0-9a-f]+)", text)
+    if not m or not s or s.group(1) != _kernel_source_hash(kernel_files):
+        return None
+    return int(m.group(1))
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "200", "-i", str(self.index)], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        if not getattr(self, "lines", None):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in self.lines:
+            c = [x.strip() for x in l.split(",")]
+            try:
+                sm.append(float(c[1]))
+                mx = float(c[2])
+            except (ValueError, IndexError):
+                continue
+            for nm, v in zip(names, c[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- the GPU arm
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def _to_dev(a, dev):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+
+
+def _pinned(a):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).pin_memory()
+
+
+def measure_gpu(w, steps, warmup, dev, dist_on, flush_bytes=512 << 20, e2e_steps=3, with_e2e=True):
+    import torch
+    import torch.distributed as td
+
+    import block_sparse_attention_index_gb300 as msa
+
+    x = synth.make_inputs(w)
+    dx = {k: _to_dev(x[k], dev) for k in ("q", "iq", "k", "v", "ik")}
+    pb = msa.Problem(w.H, w.G, w.seqs, dev, top_k=w.top_k, scale=w.softmax_scale)
+    ws = pb.workspace()
+    out = pb.new_out()
+    sel, nsel = pb.new_sel()
+    flush = torch.empty(flush_bytes // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(events=None):
+        msa.forward(pb, dx["q"], dx["iq"], dx["k"], dx["v"], dx["ik"], out=out, sel=sel, nsel=nsel, workspace=ws,
+                    events=events)
+
+    for _ in range(warmup):
+        flush.fill_(1.0)
+        step()
+    torch.cuda.synchronize(dev)
+    assert msa.error_word(ws) == 0
+    marks = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    for ev in [e for m in marks for e in m]:
+        ev.record(stream)  # torch creates the CUDA event on its first record
+    if dist_on:
+        td.barrier()
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    with ClockSampler(dev.index) as clk:
+        for i in range(steps):
+            flush.fill_(float(i))
+            step(marks[i])
+            ends[i].record(stream)
+        torch.cuda.synchronize(dev)
+    wall = time.perf_counter() - t0
+    if dist_on:
+        td.barrier()
+    step_ms = [marks[i][0].elapsed_time(ends[i]) for i in range(steps)]
+    stage_ms = [[marks[i][j].elapsed_time(marks[i][j + 1]) for j in range(4)] for i in range(steps)]
+    total_ms = float(sum(step_ms))
+    if dist_on:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        td.all_reduce(t, op=td.ReduceOp.MAX)
+        total_ms = float(t.item())
+    res = dict(ms_per_step=total_ms / steps, stage_ms=np.mean(np.array(stage_ms), axis=0).tolist(),
+               wall_s=wall, clocks=clk.summary(), launches=pb.forward_launches() * steps)
+
+    if with_e2e:
+        # end to end through the public API from pinned host buffers: every step copies
+        # all inputs (q, iq, k, v, ik caches) host->device and reads the output back
+        hx = {k: _pinned(x[k]) for k in ("q", "iq", "k", "v", "ik")}
+        h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in hx.values())
+        d2h = h_out.numel() * h_out.element_size()
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        ev0.record(stream)
+        for _ in range(e2e_steps):
+            for k in hx:
+                dx[k].copy_(hx[k], non_blocking=True)
+            step()
+            h_out.copy_(out, non_blocking=True)
+        ev1.record(stream)
+        torch.cuda.synchronize(dev)
+        res["e2e_ms"] = ev0.elapsed_time(ev1) / e2e_steps
+        res["h2d"], res["d2h"] = h2d, d2h
+    return res
+
+
+def cpu_baseline(w, rows_sample, reps=1):
+    import oracle
+    x = synth.make_inputs(w)
+    pr = oracle.Problem.from_workload(w, x)
+    threads = oracle.num_threads()
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        oracle.forward(pr, x, rows=rows_sample, threads=threads)
+    dt = time.perf_counter() - t0
+    return dict(value=len(rows_sample) * reps / dt, unit="rows/s", cores=threads, kind="oracle",
+                sample=f"{len(rows_sample)} of {w.total_rows} rows of {w.name}, {reps} rep(s), fp64 C oracle, "
+                       f"{threads} OpenMP threads", seconds=dt)
+
+
+def _sample_rows(w, max_rows):
+    R = w.total_rows
+    if R <= max_rows:
+        return list(range(R))
+    step = R / max_rows
+    return sorted({int(i * step) for i in range(max_rows)})
+
+
+def _metric_for(w):
+    dec = all(n == 1 for n, _ in w.seqs)
+    pre = all(n > 1 for n, _ in w.seqs)
+    return "MSA decode rows/s" if dec else ("MSA prefill rows/s" if pre else "MSA rows/s (mixed decode + prefill)")
+
+
+def roofline_for(w, res, hbm, bf16, bf16_sus, peak_kind):
+    wc = work_counts(w)
+    stage = res["stage_ms"]  # [decode scan, decode attention, prefill index, prefill attention]
+    if wc["dec_rows"] and stage[0] > 0:
+        achieved = wc["scan_bytes"] / (stage[0] * 1e-3) / 1e9
+        traffic = ncu_traffic("decode_scan_4x65536.md", ["decode_scan.cu", "common.cuh"]) if w.name == "decode_4x65536" else None
+        return {"kernel": "decode_scan_kernel", "bound": "hbm", "achieved": round(achieved, 1), "peak": hbm,
+                "unit": "GB/s", "frac": round(achieved / hbm, 4), "traffic": traffic,
+                "algorithmic_bytes": wc["scan_bytes"], "kernel_us": round(stage[0] * 1e3, 2),
+                "peak_source": f"{peak_kind} hbm_gbs (copy)"}
+    if stage[3] > 0:
+        achieved = wc["att_flops"] / (stage[3] * 1e-3) / 1e12
+        return {"kernel": "prefill_attend_kernel", "bound": "tensor", "achieved": round(achieved, 1), "peak": bf16,
+                "unit": "TFLOP/s", "frac": round(achieved / bf16, 4), "traffic": None,
+                "algorithmic_flops": wc["att_flops"], "kernel_us": round(stage[3] * 1e3, 2),
+                "peak_source": f"{peak_kind} bf16_tflops (burst)"}
+    return None
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="decode_4x65536", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--secondary", default="prefill_4096_at_8192",
+                    help="second workload measured in the same run ('none' to skip)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    ws, rank, local = _dist()
+    w = synth.workload(args.workload)
+    hbm, bf16, bf16_sus, peak_kind = _peaks()
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        steps_done, t_total = 0, 0.0
+        rows = _sample_rows(w, 4 if all(n == 1 for n, _ in w.seqs) else 64)
+        for i in range(args.warmup + args.steps):
+            r = cpu_baseline(w, rows)
+            if i >= args.warmup:
+                steps_done += 1
+                t_total += r["seconds"]
+        value = len(rows) * steps_done / t_total
+        line = {"impl": "reference", "metric": _metric_for(w), "value": value, "unit": "rows/s",
+                "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": 1e3 * t_total / steps_done, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                "config": {"workload": w.name, "note": w.note, "H": w.H, "G": w.G, "rows": w.total_rows,
+                           "sample_rows": len(rows)},
+                "cpu_baseline": {"kind": "oracle", "cores": r["cores"], "sample": r["sample"], "value": value,
+                                 "unit": "rows/s"},
+                "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    import torch
+    import torch.distributed as td
+    dist_on = ws > 1
+    if dist_on:
+        td.init_process_group("nccl")
+    dev = torch.device("cuda", local if dist_on else 0)
+    torch.cuda.set_device(dev)
+
+    res = measure_gpu(w, args.steps, args.warmup, dev, dist_on, with_e2e=not args.no_e2e)
+    rows = w.total_rows
+    value = rows * ws / (res["ms_per_step"] * 1e-3)
+    line = {"metric": _metric_for(w), "value": round(value, 1), "unit": "rows/s", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(res["ms_per_step"], 5), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": w.name, "note": w.note, "H": w.H, "G": w.G, "head_dim": w.D, "index_dim": w.Di,
+                       "block": w.S, "top_k": w.top_k, "rows_per_gpu": rows,
+                       "cache_tokens_per_gpu": w.cache_tokens, "l2": "flushed before every step (512 MiB write)",
+                       "parallelism": f"replicas x{ws}"},
+            "stage_us": {"decode_scan": round(res["stage_ms"][0] * 1e3, 2),
+                         "decode_attend": round(res["stage_ms"][1] * 1e3, 2),
+                         "prefill_index": round(res["stage_ms"][2] * 1e3, 2),
+                         "prefill_attend": round(res["stage_ms"][3] * 1e3, 2)},
+            "roofline": roofline_for(w, res, hbm, bf16, bf16_sus, peak_kind),
+            "clocks": res["clocks"], "gpu_launches": res["launches"]}
+    wc = work_counts(w)
+    step_bytes = wc["scan_bytes"] + wc["dec_att_bytes"]
+    if step_bytes and wc["pre_rows"] == 0:
+        line["step_hbm_frac"] = round(step_bytes / (res["ms_per_step"] * 1e-3) / 1e9 / hbm, 4)
+    if "e2e_ms" in res:
+        line["e2e"] = {"value": round(rows * ws / (res["e2e_ms"] * 1e-3), 1), "unit": "rows/s",
+                       "h2d_bytes_per_step": res["h2d"], "d2h_bytes_per_step": res["d2h"],
+                       "note": "every step copies q, iq and the k, v, ik caches from pinned host memory and reads "
+                               "the output back"}
+    if args.secondary != "none" and args.secondary != args.workload:
+        w2 = synth.workload(args.secondary)
+        res2 = measure_gpu(w2, max(3, args.steps // 2), args.warmup, dev, dist_on, with_e2e=False)
+        line["secondary"] = {"metric": _metric_for(w2), "workload": w2.name,
+                             "value": round(w2.total_rows * ws / (res2["ms_per_step"] * 1e-3), 1), "unit": "rows/s",
+                             "ms_per_step": round(res2["ms_per_step"], 5),
+                             "stage_us": {"prefill_index": round(res2["stage_ms"][2] * 1e3, 2),
+                                          "prefill_attend": round(res2["stage_ms"][3] * 1e3, 2)},
+                             "roofline": roofline_for(w2, res2, hbm, bf16, bf16_sus, peak_kind),
+                             "gpu_launches": res2["launches"]}
+        line["gpu_launches"] += res2["launches"]
+    if rank == 0 and not args.no_cpu_baseline:
+        cb = cpu_baseline(w, _sample_rows(w, 4 if wc["pre_rows"] == 0 else 64), reps=3 if wc["pre_rows"] == 0 else 1)
+        cb.pop("seconds")
+        line["cpu_baseline"] = cb
+    if dist_on:
+        td.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    main()

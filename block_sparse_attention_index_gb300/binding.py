@@ -247,6 +247,8 @@ def forward(pb: Problem, q, iq, k, v, ik, out=None, sel=None, nsel=None, workspa
     args = (C.byref(pb.c), _ptr(q), _ptr(iq), _ptr(k), _ptr(v), _ptr(ik), _ptr(out), _ptr(sel), _ptr(nsel),
             _ptr(ws), ws.numel(), _stream(pb.device))
     if events:
+        if any(e is not None and not e.cuda_event for e in events):
+            raise ValueError("record each torch.cuda.Event once before passing it (torch creates events lazily)")
         arr = (C.c_void_p * len(events))(*[C.c_void_p(e.cuda_event) if e is not None else None for e in events])
         _check(_lib.msa_forward_marked(*args, arr, len(events)))
     else:

@@ -1,0 +1,245 @@
+// Prompt-chunk stages 1+2 on tcgen05: lightning-indexer scores as a tensor-
+// core GEMM with the block max-pool and a running top-k in its epilogue.
+//
+// PR #1388 "minimax_m3: a CUDA backend for MiniMax-M3.1-Flash ...": index
+// scores and top-16 block selection per row and key head; "MiniMax-M3 on 4x
+// RTX PRO 6000 Blackwell (SM120)", "What this fixes": max-pool scoring and a
+// forced local block.
+//
+// One CTA = one tile of 128 query rows of one sequence and one KV head.  It
+// streams the sequence's index keys in tiles of 256 positions:
+//     D[128 rows, 256 positions] = iq[128, 64] . ik[256, 64]^T   (fp32, TMEM)
+// one tcgen05.mma (M=128, N=256, K=16) per 16 index dims.  The accumulator is
+// double-buffered in tensor memory (2 x 256 columns) so the MMA of tile n+1
+// overlaps the epilogue of tile n.  Epilogue: thread i owns row i (TMEM lane
+// i), max-pools each 64-column block over positions <= p, and inserts blocks
+// j < J into a sorted register list of the 15 best (pooled score desc, j asc).
+// Scores are never written to memory.
+//
+// Warp roles: warps 0-3 epilogue, warp 4 TMA producer, warp 5 MMA issuer and
+// tensor-memory owner.
+#include "common.cuh"
+#include "internal.h"
+
+namespace msa {
+
+constexpr int kIdxThreads = 192;
+constexpr int kIdxRows = 128;     // M
+constexpr int kIdxCols = 256;     // N, positions per tile
+constexpr int kIdxStages = 4;     // index-key tile ring
+constexpr int kIdxTileBytes = kIdxCols * kIndexDim * 2;  // 32 KB
+constexpr int kIdxABytes = kIdxRows * kIndexDim * 2;     // 16 KB
+
+struct __align__(1024) IndexSmem {
+    uint8_t b[kIdxStages][kIdxTileBytes];
+    uint8_t a[kIdxABytes];
+    uint64_t full[kIdxStages];
+    uint64_t empty[kIdxStages];
+    uint64_t a_full;
+    uint64_t acc_full[2];
+    uint64_t acc_empty[2];
+    uint32_t tmem_base;
+    int32_t seq, row0, nrows, ntiles, p0, L;
+    int64_t start;
+};
+
+// Which (sequence, row tile) CTA `tile` handles; false when beyond the end.
+// Tiles of a sequence with n rows (n > 1, or any n when !only_multi):
+// ceil(n / 128).  Walks the sequences (num_seqs is small).
+__device__ bool find_tile(const PrefillIndexArgs& a, int tile, int& b, int& i0, int& n) {
+    int acc = 0;
+    for (int s = 0; s < a.num_seqs; ++s) {
+        const int rows = a.cu_rows[s + 1] - a.cu_rows[s];
+        if (rows <= 1) continue;
+        const int t = (rows + kIdxRows - 1) / kIdxRows;
+        if (tile < acc + t) {
+            b = s;
+            i0 = (tile - acc) * kIdxRows;
+            n = rows;
+            return true;
+        }
+        acc += t;
+    }
+    return false;
+}
+
+__device__ __forceinline__ void insert_top15(uint64_t (&best)[15], uint64_t key) {
+    if (key <= best[14]) return;
+    best[14] = key;
+#pragma unroll
+    for (int i = 14; i > 0; --i) {
+        if (best[i] > best[i - 1]) {
+            const uint64_t t = best[i];
+            best[i] = best[i - 1];
+            best[i - 1] = t;
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kIdxThreads, 1) prefill_index_kernel(const __grid_constant__ CUtensorMap iq_map,
+                                                                       const __grid_constant__ CUtensorMap ik_map,
+                                                                       const PrefillIndexArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    IndexSmem& sm = *reinterpret_cast<IndexSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int h = blockIdx.y;
+
+    if (tid == 0) {
+        int b = 0, i0 = 0, n = 0;
+        sm.seq = -1;
+        if (find_tile(a, blockIdx.x, b, i0, n)) {
+            const int L = a.cache_lens[b];
+            const int64_t start = a.cache_starts[b];
+            const int r0 = a.cu_rows[b] + i0;
+            const int nr = min(kIdxRows, n - i0);
+            const bool ok = L >= n && L <= a.max_cache_len && start >= 0 && start + L <= a.cache_tokens &&
+                            r0 >= 0 && r0 + nr <= a.total_rows;
+            if (ok) {
+                sm.seq = b;
+                sm.row0 = r0;
+                sm.nrows = nr;
+                sm.L = L;
+                sm.start = start;
+                sm.p0 = L - n + i0;                              // position of the tile's first row
+                const int pmax = sm.p0 + nr - 1;
+                sm.ntiles = (pmax + kIdxCols) / kIdxCols;        // tiles covering positions 0..pmax
+            } else {
+                atomicOr(a.err, kErrBadMetadata);
+            }
+        }
+        for (int s = 0; s < kIdxStages; ++s) {
+            mbar_init(&sm.full[s], 1);
+            mbar_init(&sm.empty[s], 1);
+        }
+        mbar_init(&sm.a_full, 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&sm.acc_full[s], 1);
+            mbar_init(&sm.acc_empty[s], 128);
+        }
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (sm.seq < 0) return;
+    if (warp == 5) tmem_alloc(&sm.tmem_base, 512);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = sm.tmem_base;
+    const int ntiles = sm.ntiles;
+
+    if (warp == 4) {
+        // ---------------- TMA producer
+        if (lane == 0) {
+            prefetch_tmap(&iq_map);
+            prefetch_tmap(&ik_map);
+            mbar_arrive_expect_tx(&sm.a_full, kIdxABytes);
+            tma_load_3d(sm.a, &iq_map, &sm.a_full, 0, h, sm.row0);
+            const int tok0 = static_cast<int>(sm.start);
+            for (int n = 0; n < ntiles; ++n) {
+                const int s = n % kIdxStages;
+                if (n >= kIdxStages && !mbar_wait(&sm.empty[s], ((n / kIdxStages) - 1) & 1, a.err)) break;
+                mbar_arrive_expect_tx(&sm.full[s], kIdxTileBytes);
+                tma_load_3d(sm.b[s], &ik_map, &sm.full[s], 0, h, tok0 + n * kIdxCols);
+            }
+        }
+    } else if (warp == 5) {
+        // ---------------- MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_bf16_f32(kIdxRows, kIdxCols, 0, 0);
+            bool ok = mbar_wait(&sm.a_full, 0, a.err);
+            const uint32_t a_addr = smem_u32(sm.a);
+            for (int n = 0; ok && n < ntiles; ++n) {
+                const int s = n % kIdxStages, acc = n & 1;
+                if (!mbar_wait(&sm.full[s], (n / kIdxStages) & 1, a.err)) break;
+                if (n >= 2 && !mbar_wait(&sm.acc_empty[acc], ((n >> 1) - 1) & 1, a.err)) break;
+                tc_fence_after();
+                const uint32_t b_addr = smem_u32(sm.b[s]);
+#pragma unroll
+                for (int k = 0; k < kIndexDim / 16; ++k) {
+                    const uint64_t ad = smem_desc_sw128(a_addr + k * 32, 16, 1024);
+                    const uint64_t bd = smem_desc_sw128(b_addr + k * 32, 16, 1024);
+                    tc_mma_ss(tmem + acc * kIdxCols, ad, bd, idesc, k > 0);
+                }
+                tc_commit(&sm.empty[s]);
+                tc_commit(&sm.acc_full[acc]);
+            }
+        }
+    } else {
+        // ---------------- epilogue: one row per thread
+        const int row = tid;  // TMEM lane
+        const bool live = row < sm.nrows;
+        const int p = sm.p0 + row;
+        const int J = p / kBlock;
+        uint64_t best[15];
+#pragma unroll
+        for (int i = 0; i < 15; ++i) best[i] = 0;
+        const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+        for (int n = 0; n < ntiles; ++n) {
+            const int acc = n & 1;
+            if (!mbar_wait(&sm.acc_full[acc], (n >> 1) & 1, a.err)) break;
+            tc_fence_after();
+#pragma unroll 1
+            for (int jb = 0; jb < kIdxCols / kBlock; ++jb) {
+                const int j = n * (kIdxCols / kBlock) + jb;
+                uint32_t v[4][16];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) tmem_ld16(lane_addr + acc * kIdxCols + jb * kBlock + c * 16, v[c]);
+                tmem_ld_wait();
+                if (!live || j >= J) continue;  // the local block is forced; later blocks are in the future
+                float m = __uint_as_float(v[0][0]);
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) m = fmaxf(m, __uint_as_float(v[c][e]));
+                insert_top15(best, block_key(m, j));
+            }
+            tc_fence_before();
+            mbar_arrive(&sm.acc_empty[acc]);
+        }
+        if (live) {
+            // kept blocks: the best min(top_k-1, J) plus J, ascending, -1 padded
+            const int others = min(a.top_k - 1, J);
+            int v[16];
+#pragma unroll
+            for (int i = 0; i < 15; ++i) v[i] = i < others ? key_block(best[i]) : 0x7fffffff;
+            v[15] = 0x7fffffff;
+            if (others < 16) {
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    if (i == others) v[i] = J;
+            }
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+#pragma unroll
+                for (int k = 0; k < 15 - i; ++k)
+                    if (v[k] > v[k + 1]) {
+                        const int t = v[k];
+                        v[k] = v[k + 1];
+                        v[k + 1] = t;
+                    }
+            const int r = sm.row0 + row;
+            int32_t* out = a.sel + (static_cast<int64_t>(r) * a.H + h) * a.top_k;
+            for (int i = 0; i < a.top_k; ++i) out[i] = v[i] == 0x7fffffff ? -1 : v[i];
+            a.nsel[static_cast<int64_t>(r) * a.H + h] = others + 1;
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 5) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+cudaError_t run_prefill_index(const PrefillIndexArgs& a, cudaStream_t stream) {
+    const size_t smem = sizeof(IndexSmem) + 1024;
+    cudaError_t e = cudaFuncSetAttribute(prefill_index_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    const int tiles = (a.total_rows + kIdxRows - 1) / kIdxRows + a.num_seqs;  // upper bound
+    dim3 grid(tiles, a.H);
+    prefill_index_kernel<<<grid, kIdxThreads, smem, stream>>>(*a.iq_map, *a.ik_map, a);
+    return cudaGetLastError();
+}
+
+}  // namespace msa
