@@ -6,6 +6,7 @@ binding over it.  Importing the package does not need a GPU, but it needs
 the built library: there is no CPU fallback.
 """
 from .binding import (  # noqa: F401
-    EXPORTED, LIB_PATH, MsaError, MsaProblem, Problem, attend_decode, attend_prefill, error_word, forward,
+    EXPORTED, LIB_PATH, MsaError, MsaProblem, Problem, attend_decode, attend_decode_noalloc, attend_prefill,
+    error_word, forward,
     index_scores, lib, select_blocks,
 )

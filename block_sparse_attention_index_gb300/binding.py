@@ -23,6 +23,7 @@ ERR_WAIT_TIMEOUT, ERR_BAD_METADATA, ERR_TMEM_ALLOC = 1, 2, 4
 EXPORTED = [
     "msa_status_string", "msa_last_error", "msa_workspace_size", "msa_index_scores", "msa_select_blocks",
     "msa_attend_decode", "msa_attend_prefill", "msa_forward", "msa_forward_marked", "msa_forward_launches",
+    "msa_attend_decode_noalloc",
 ]
 
 
@@ -60,12 +61,14 @@ def _load():
     lib.msa_select_blocks.argtypes = [P, vp, i64, vp, vp, vp]
     lib.msa_attend_decode.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, C.c_size_t, vp]
     lib.msa_attend_prefill.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, C.c_size_t, vp]
+    lib.msa_attend_decode_noalloc.argtypes = [P, vp, vp, vp, vp, vp, vp, vp]
     lib.msa_forward.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, C.c_size_t, vp]
     lib.msa_forward_marked.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, C.c_size_t, vp,
                                        C.POINTER(vp), i32]
     lib.msa_forward_launches.argtypes = [P]
     lib.msa_forward_launches.restype = i32
     for name in ["msa_workspace_size", "msa_index_scores", "msa_select_blocks", "msa_attend_decode",
+                 "msa_attend_decode_noalloc",
                  "msa_attend_prefill", "msa_forward", "msa_forward_marked"]:
         getattr(lib, name).restype = C.c_int
     return lib
@@ -229,6 +232,21 @@ def attend_prefill(pb: Problem, q, k, v, sel, nsel, out=None, workspace=None):
     return _attend(_lib.msa_attend_prefill, pb, q, k, v, sel, nsel, out, workspace)
 
 
+def attend_decode_noalloc(pb: Problem, q, k, v, sel, nsel, out=None):
+    """msa_attend_decode_noalloc: decode attention for callers that cannot
+    allocate device memory; the library's fixed scratch replaces the
+    workspace (at most 32 sequence x KV-head pairs per call)."""
+    pb._check_q(q)
+    pb._check_cache(k, "k", pb.D)
+    pb._check_cache(v, "v", pb.D)
+    pb._check_sel(sel, nsel)
+    out = pb.new_out() if out is None else out
+    _need(out, "out", pb.out_dtype, pb.device, (pb.total_rows, pb.H * pb.G, pb.D))
+    _check(_lib.msa_attend_decode_noalloc(C.byref(pb.c), _ptr(q), _ptr(k), _ptr(v), _ptr(sel), _ptr(nsel),
+                                          _ptr(out), _stream(pb.device)))
+    return out
+
+
 def forward(pb: Problem, q, iq, k, v, ik, out=None, sel=None, nsel=None, workspace=None, events=None):
     """msa_forward (msa_forward_marked when events are given).
 
@@ -262,4 +280,5 @@ def error_word(workspace) -> int:
 
 
 __all__ = ["Problem", "MsaProblem", "MsaError", "index_scores", "select_blocks", "attend_decode", "attend_prefill",
+           "attend_decode_noalloc",
            "forward", "error_word", "lib", "LIB_PATH", "EXPORTED"]

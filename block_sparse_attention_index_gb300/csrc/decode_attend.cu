@@ -16,6 +16,8 @@
 //   - it writes (m, l, O) for its block; the last split to finish (atomic
 //     ticket) combines the partials:  M = max_s m_s,  L = sum_s l_s 2^(m_s-M),
 //     out = sum_s O_s 2^(m_s-M) / L.
+#include <mutex>
+
 #include "common.cuh"
 #include "internal.h"
 #include "select.cuh"
@@ -303,6 +305,67 @@ cudaError_t run_decode_attend(const DecodeAttendArgs& a, cudaStream_t stream) {
         decode_attend_kernel<true><<<grid, kAttThreads, smem, stream>>>(*a.k_map, *a.v_map, a);
     }
     return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Allocation-free launch of decode attention (msa_attend_decode_noalloc).
+//
+// Some callers cannot allocate device memory at all: code enqueued while a
+// framework captures a CUDA graph and forbids allocation inside the capture,
+// hosts whose device memory is carved out once at start-up (real-time or
+// embedded serving), and plug-ins loaded into a process whose allocator they
+// do not own.  For them the split partials, the per-(sequence, head) tickets
+// and the error word live in the file-scope device array below instead of a
+// caller workspace.  Every GPU that loads the library keeps this array
+// (about 4 MiB) until the process exits.  All calls share it: calls that
+// overlap on the GPU (other streams, other host threads) race and give
+// wrong results; order them on one stream.
+namespace {
+
+constexpr size_t kNoAllocHeader = 256;  // error word + tickets
+constexpr size_t kNoAllocBytes =
+    kNoAllocHeader + static_cast<size_t>(kNoAllocMaxPairs) * kMaxTopK * kPartialFloats * sizeof(float);
+static_assert(kNoAllocMaxPairs * sizeof(int32_t) + 16 <= kNoAllocHeader, "tickets must fit the header");
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocBytes];
+
+std::mutex g_noalloc_mutex;
+void* g_noalloc_base[64] = {nullptr};  // device address of the array, per device
+
+// Device address of the array on the current device.  Looked up once per
+// device (host code may not use the symbol itself as a device pointer).
+cudaError_t noalloc_base(void** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    if (g_noalloc_base[dev] == nullptr) {
+        void* ptr = nullptr;
+        e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+        if (e != cudaSuccess) return e;
+        g_noalloc_base[dev] = ptr;
+    }
+    *out = g_noalloc_base[dev];
+    return cudaSuccess;
+}
+
+}  // namespace
+
+cudaError_t run_decode_attend_noalloc(DecodeAttendArgs a, cudaStream_t stream) {
+    if (static_cast<int64_t>(a.num_seqs) * a.H > kNoAllocMaxPairs) return cudaErrorInvalidValue;
+    void* base = nullptr;
+    cudaError_t e = noalloc_base(&base);
+    if (e != cudaSuccess) return e;
+    uint8_t* s = static_cast<uint8_t*>(base);
+    a.err = reinterpret_cast<uint32_t*>(s);
+    a.tickets = reinterpret_cast<int32_t*>(s + 16);
+    a.partials = reinterpret_cast<float*>(s + kNoAllocHeader);
+    // the error word and the tickets must start at zero; the partials are
+    // fully written before they are read
+    e = cudaMemsetAsync(s, 0, 16 + static_cast<size_t>(a.num_seqs) * a.H * sizeof(int32_t), stream);
+    if (e != cudaSuccess) return e;
+    return run_decode_attend(a, stream);
 }
 
 }  // namespace msa

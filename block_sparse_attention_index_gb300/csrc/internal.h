@@ -92,6 +92,11 @@ struct PrefillAttendArgs {
     uint32_t* err;
 };
 
+// Allocation-free decode attention: scratch in a file-scope device array
+// sized for at most kNoAllocMaxPairs (sequence, KV head) pairs per call.
+constexpr int kNoAllocMaxPairs = 32;
+cudaError_t run_decode_attend_noalloc(DecodeAttendArgs a, cudaStream_t stream);
+
 cudaError_t run_decode_scan(const ScanArgs& a, cudaStream_t stream);
 cudaError_t run_decode_attend(const DecodeAttendArgs& a, cudaStream_t stream);
 cudaError_t run_index_scores(const StagedArgs& a, const uint16_t* iq, const uint16_t* ik, float* scores,

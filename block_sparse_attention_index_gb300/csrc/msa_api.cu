@@ -368,6 +368,36 @@ msa_status msa_attend_prefill(const msa_problem* p, const void* q, const void* k
     return e == cudaSuccess ? MSA_OK : cuda_fail(e, "prefill attention launch");
 }
 
+msa_status msa_attend_decode_noalloc(const msa_problem* p, const void* q, const void* k_cache, const void* v_cache,
+                                     const int32_t* sel, const int32_t* nsel, void* out, void* stream) {
+    g_last_error.clear();
+    msa_status s;
+    if ((s = check_problem(p)) != MSA_OK) return s;
+    if ((s = check_ptr(q, "q")) != MSA_OK || (s = check_ptr(k_cache, "k_cache")) != MSA_OK ||
+        (s = check_ptr(v_cache, "v_cache")) != MSA_OK || (s = check_ptr(sel, "sel")) != MSA_OK ||
+        (s = check_ptr(nsel, "nsel")) != MSA_OK || (s = check_ptr(out, "out")) != MSA_OK)
+        return s;
+    if (p->max_rows_per_seq != 1)
+        return fail(MSA_ERR_INVALID_ARG, "msa_attend_decode_noalloc needs one row per sequence (max_rows_per_seq == 1)");
+    const int64_t pairs = static_cast<int64_t>(p->num_seqs) * p->num_kv_heads;
+    if (pairs > msa::kNoAllocMaxPairs)
+        return fail(MSA_ERR_UNSUPPORTED,
+                    "msa_attend_decode_noalloc: num_seqs * num_kv_heads = %lld exceeds its fixed scratch of %d "
+                    "(sequence, KV head) pairs; use msa_attend_decode with a workspace",
+                    static_cast<long long>(pairs), msa::kNoAllocMaxPairs);
+    const uint64_t T = p->cache_tokens, H = p->num_kv_heads;
+    CUtensorMap km, vm;
+    if ((s = make_map(&km, k_cache, 128, H, T, 64, 1, 64, "k_cache")) != MSA_OK) return s;
+    if ((s = make_map(&vm, v_cache, 128, H, T, 64, 1, 64, "v_cache")) != MSA_OK) return s;
+    Layout unused;
+    msa::DecodeAttendArgs a = decode_args(p, &km, &vm, q, out, nullptr, unused);
+    a.pooled = nullptr;
+    a.sel_in = sel;
+    a.nsel_in = nsel;
+    cudaError_t e = msa::run_decode_attend_noalloc(a, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? MSA_OK : cuda_fail(e, "allocation-free decode attention");
+}
+
 int32_t msa_forward_launches(const msa_problem* p) {
     if (check_problem(p) != MSA_OK) return -1;
     return (decode_family(p) ? 2 : 0) + (prefill_family(p) ? 2 : 0);

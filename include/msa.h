@@ -146,6 +146,28 @@ msa_status msa_attend_decode(const msa_problem* p, const void* q, const void* k_
                              const void* v_cache, const int32_t* sel, const int32_t* nsel,
                              void* out, void* workspace, size_t workspace_bytes, void* stream);
 
+/* Stage 3, decode form, for callers that cannot allocate device memory.
+ * The paper has no counterpart: this is a deployment variant of
+ * msa_attend_decode.  Some callers cannot call cudaMalloc at all -- code
+ * enqueued while a framework captures a CUDA graph and forbids allocation
+ * inside the capture, hosts whose device memory is carved out once at
+ * start-up, plug-ins that do not own the process's allocator -- so this
+ * entry point takes no workspace and allocates nothing: its scratch (split
+ * partials, tickets, error word) is a fixed device array inside the library,
+ * about 4 MiB, which every GPU that loads the library holds until the
+ * process exits.  Limit: num_seqs * num_kv_heads <= 32; larger problems are
+ * rejected with MSA_ERR_UNSUPPORTED.  Arguments and results are those of
+ * msa_attend_decode.  The first call on each device looks up the array's
+ * device address (a host-side query, made with that device current); make
+ * that first call before any stream capture.  Every call shares the one
+ * array: calls that overlap on the GPU (several streams or host threads)
+ * race and give wrong results, so order them on one stream.  Device-side
+ * errors are recorded only in the library's own scratch and are not
+ * reported by this entry point. */
+msa_status msa_attend_decode_noalloc(const msa_problem* p, const void* q, const void* k_cache,
+                                     const void* v_cache, const int32_t* sel, const int32_t* nsel,
+                                     void* out, void* stream);
+
 /* Stage 3, prompt-chunk form (any rows per sequence): tcgen05 tensor-core
  * tiles in which the G query heads of one KV head share each key/value block
  * read; accumulators live in tensor memory.  Same arguments as the decode
