@@ -6,7 +6,8 @@ attention over the kept blocks.  Default workload: decode batch 4 x 65,536
 cached tokens, 4 KV x 16 query heads (value = decode rows/s); a secondary
 measurement runs the 4,096-row prompt chunk at an 8,192-token prefix
 (prefill rows/s).  Inputs sit in HBM before the timed region; L2 is flushed
-(a 512 MiB write) before every timed step and the flush is not timed.
+(a 512 MiB write, then a 256 MiB read so no dirty line is left) before every
+timed step; the flush is not timed.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
   python bench.py --impl reference ...   (the CPU oracle, timed on the host)
@@ -171,7 +172,8 @@ def _pinned(a):
     return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).pin_memory()
 
 
-def measure_gpu(w, steps, warmup, dev, dist_on, flush_bytes=512 << 20, e2e_steps=3, with_e2e=True):
+def measure_gpu(w, steps, warmup, dev, dist_on, flush_bytes=512 << 20, e2e_steps=3, with_e2e=True,
+                use_graph=True):
     import torch
     import torch.distributed as td
 
@@ -184,43 +186,73 @@ def measure_gpu(w, steps, warmup, dev, dist_on, flush_bytes=512 << 20, e2e_steps
     out = pb.new_out()
     sel, nsel = pb.new_sel()
     flush = torch.empty(flush_bytes // 4, dtype=torch.float32, device=dev)
+    clean = torch.ones(flush_bytes // 8, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
+
+    def flush_l2(i):
+        # write a buffer 4x the L2, then read another 2x the L2 so the lines the
+        # write left dirty are written back before the timed step, not during it
+        flush.fill_(float(i))
+        clean.sum()
 
     def step(events=None):
         msa.forward(pb, dx["q"], dx["iq"], dx["k"], dx["v"], dx["ik"], out=out, sel=sel, nsel=nsel, workspace=ws,
                     events=events)
 
-    for _ in range(warmup):
-        flush.fill_(1.0)
+    for i in range(warmup):
+        flush_l2(i)
         step()
     torch.cuda.synchronize(dev)
     assert msa.error_word(ws) == 0
-    marks = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
-    for ev in [e for m in marks for e in m]:
+    marks = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+    for ev in marks:
         ev.record(stream)  # torch creates the CUDA event on its first record
+    torch.cuda.synchronize(dev)
+    graph = None
+    if use_graph:
+        # one step captured once (the library enqueues only its own kernels and event
+        # records, never allocates or synchronises) and replayed: no host gaps between
+        # the step's kernels
+        graph = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream(dev)
+        cap.wait_stream(stream)
+        with torch.cuda.stream(cap):
+            with torch.cuda.graph(graph, stream=cap):
+                step(marks)
+        stream.wait_stream(cap)
+        torch.cuda.synchronize(dev)
+    begin = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    step_ms, stage_ms = [], []
     if dist_on:
         td.barrier()
     torch.cuda.synchronize(dev)
     t0 = time.perf_counter()
     with ClockSampler(dev.index) as clk:
         for i in range(steps):
-            flush.fill_(float(i))
-            step(marks[i])
+            flush_l2(i)
+            begin[i].record(stream)
+            if graph is not None:
+                graph.replay()
+            else:
+                step(marks)
             ends[i].record(stream)
+            ends[i].synchronize()
+            step_ms.append(begin[i].elapsed_time(ends[i]))
+            stage_ms.append([marks[j].elapsed_time(marks[j + 1]) for j in range(4)])
         torch.cuda.synchronize(dev)
     wall = time.perf_counter() - t0
     if dist_on:
         td.barrier()
-    step_ms = [marks[i][0].elapsed_time(ends[i]) for i in range(steps)]
-    stage_ms = [[marks[i][j].elapsed_time(marks[i][j + 1]) for j in range(4)] for i in range(steps)]
+    assert msa.error_word(ws) == 0
     total_ms = float(sum(step_ms))
     if dist_on:
         t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
         td.all_reduce(t, op=td.ReduceOp.MAX)
         total_ms = float(t.item())
     res = dict(ms_per_step=total_ms / steps, stage_ms=np.mean(np.array(stage_ms), axis=0).tolist(),
-               wall_s=wall, clocks=clk.summary(), launches=pb.forward_launches() * steps)
+               wall_s=wall, clocks=clk.summary(), launches=pb.forward_launches() * steps,
+               graph=graph is not None)
 
     if with_e2e:
         # end to end through the public API from pinned host buffers: every step copies
@@ -302,6 +334,7 @@ def main():
                     help="second workload measured in the same run ('none' to skip)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-graph", action="store_true", help="launch each step directly instead of replaying a CUDA graph")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -340,7 +373,8 @@ def main():
     dev = torch.device("cuda", local if dist_on else 0)
     torch.cuda.set_device(dev)
 
-    res = measure_gpu(w, args.steps, args.warmup, dev, dist_on, with_e2e=not args.no_e2e)
+    res = measure_gpu(w, args.steps, args.warmup, dev, dist_on, with_e2e=not args.no_e2e,
+                      use_graph=not args.no_graph)
     rows = w.total_rows
     value = rows * ws / (res["ms_per_step"] * 1e-3)
     line = {"metric": _metric_for(w), "value": round(value, 1), "unit": "rows/s", "n_gpus": ws, "steps": args.steps,
@@ -348,7 +382,8 @@ def main():
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": w.name, "note": w.note, "H": w.H, "G": w.G, "head_dim": w.D, "index_dim": w.Di,
                        "block": w.S, "top_k": w.top_k, "rows_per_gpu": rows,
-                       "cache_tokens_per_gpu": w.cache_tokens, "l2": "flushed before every step (512 MiB write)",
+                       "cache_tokens_per_gpu": w.cache_tokens, "l2": "flushed before every step (512 MiB write, then 256 MiB read)",
+                       "launch": "CUDA graph replay of one msa_forward" if res["graph"] else "direct msa_forward calls",
                        "parallelism": f"replicas x{ws}"},
             "stage_us": {"decode_scan": round(res["stage_ms"][0] * 1e3, 2),
                          "decode_attend": round(res["stage_ms"][1] * 1e3, 2),
@@ -367,7 +402,8 @@ def main():
                                "the output back"}
     if args.secondary != "none" and args.secondary != args.workload:
         w2 = synth.workload(args.secondary)
-        res2 = measure_gpu(w2, max(3, args.steps // 2), args.warmup, dev, dist_on, with_e2e=False)
+        res2 = measure_gpu(w2, max(3, args.steps // 2), args.warmup, dev, dist_on, with_e2e=False,
+                           use_graph=not args.no_graph)
         line["secondary"] = {"metric": _metric_for(w2), "workload": w2.name,
                              "value": round(w2.total_rows * ws / (res2["ms_per_step"] * 1e-3), 1), "unit": "rows/s",
                              "ms_per_step": round(res2["ms_per_step"], 5),

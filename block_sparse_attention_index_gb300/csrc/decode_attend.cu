@@ -34,6 +34,7 @@ struct __align__(1024) DecodeSmem {
     float wmax[4][16];
     float wsum[4][16];
     float weight[kMaxTopK][16];
+    float ml[kMaxTopK][32];  // per split: m[16] then l[16]
     uint64_t bar;
     int32_t sel[kMaxTopK];
     int32_t nsel;
@@ -264,28 +265,50 @@ __global__ void __launch_bounds__(kAttThreads) decode_attend_kernel(const __grid
     // ---- last split: log-sum-exp combine of the nsel partials
     __threadfence();
     const float* parts = a.partials + (static_cast<int64_t>(b) * H + h) * a.top_k * kPartialFloats;
-    for (int i = tid; i < 16; i += kAttThreads) {
+    // every split's (m, l) for the 16 head rows, fetched in one round of loads
+    for (int t = tid; t < nsel * 32; t += kAttThreads)
+        sm.ml[t >> 5][t & 31] = __ldcg(parts + (t >> 5) * kPartialFloats + 16 * 128 + (t & 31));
+    __syncthreads();
+    if (tid < 16) {
         float M = -INFINITY;
-        for (int sp = 0; sp < nsel; ++sp) M = fmaxf(M, __ldcg(parts + sp * kPartialFloats + 16 * 128 + i));
+        for (int sp = 0; sp < nsel; ++sp) M = fmaxf(M, sm.ml[sp][tid]);
         float Ls = 0.f;
         for (int sp = 0; sp < nsel; ++sp) {
-            const float w = exp2f(__ldcg(parts + sp * kPartialFloats + 16 * 128 + i) - M);
-            sm.weight[sp][i] = w;
-            Ls += w * __ldcg(parts + sp * kPartialFloats + 16 * 128 + 16 + i);
+            const float w = exp2f(sm.ml[sp][tid] - M);
+            sm.weight[sp][tid] = w;
+            Ls += w * sm.ml[sp][16 + tid];
         }
         const float inv = 1.f / Ls;
-        for (int sp = 0; sp < nsel; ++sp) sm.weight[sp][i] *= inv;
+        for (int sp = 0; sp < nsel; ++sp) sm.weight[sp][tid] *= inv;
     }
     __syncthreads();
-    const int d = tid;  // one output dim per thread
-    for (int g = 0; g < G; ++g) {
-        float acc = 0.f;
-        for (int sp = 0; sp < nsel; ++sp) acc += sm.weight[sp][g] * __ldcg(parts + sp * kPartialFloats + g * 128 + d);
-        const int64_t oi = (static_cast<int64_t>(r) * H * G + static_cast<int64_t>(h) * G + g) * kHeadDim + d;
-        if (a.out_bf16)
-            reinterpret_cast<__nv_bfloat16*>(a.out)[oi] = __float2bfloat16_rn(acc);
-        else
-            reinterpret_cast<float*>(a.out)[oi] = acc;
+    // thread = 4 consecutive dims of heads g0, g0+4, g0+8, g0+12; all splits'
+    // loads of one head are issued together
+    const int d4 = (tid & 31) * 4, g0 = tid >> 5;
+    for (int g = g0; g < G; g += 4) {
+        float4 v[kMaxTopK];
+#pragma unroll
+        for (int sp = 0; sp < kMaxTopK; ++sp)
+            if (sp < nsel) v[sp] = __ldcg(reinterpret_cast<const float4*>(parts + sp * kPartialFloats + g * 128 + d4));
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int sp = 0; sp < kMaxTopK; ++sp)
+            if (sp < nsel) {
+                const float w = sm.weight[sp][g];
+                acc.x = fmaf(w, v[sp].x, acc.x);
+                acc.y = fmaf(w, v[sp].y, acc.y);
+                acc.z = fmaf(w, v[sp].z, acc.z);
+                acc.w = fmaf(w, v[sp].w, acc.w);
+            }
+        const int64_t oi = (static_cast<int64_t>(r) * H * G + static_cast<int64_t>(h) * G + g) * kHeadDim + d4;
+        if (a.out_bf16) {
+            uint2 pk;
+            pk.x = pack_bf16x2(acc.x, acc.y);
+            pk.y = pack_bf16x2(acc.z, acc.w);
+            *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(a.out) + oi) = pk;
+        } else {
+            *reinterpret_cast<float4*>(reinterpret_cast<float*>(a.out) + oi) = acc;
+        }
     }
     if (tid == 0) a.tickets[static_cast<int64_t>(b) * H + h] = 0;  // ready for the next call
 }
@@ -294,13 +317,11 @@ cudaError_t run_decode_attend(const DecodeAttendArgs& a, cudaStream_t stream) {
     const size_t smem = sizeof(DecodeSmem) + 1024;
     dim3 grid(a.top_k, a.H, a.num_seqs);
     if (a.pooled != nullptr) {
-        cudaError_t e = cudaFuncSetAttribute(decode_attend_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(smem));
+        cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(decode_attend_kernel<false>), smem);
         if (e != cudaSuccess) return e;
         decode_attend_kernel<false><<<grid, kAttThreads, smem, stream>>>(*a.k_map, *a.v_map, a);
     } else {
-        cudaError_t e = cudaFuncSetAttribute(decode_attend_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(smem));
+        cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(decode_attend_kernel<true>), smem);
         if (e != cudaSuccess) return e;
         decode_attend_kernel<true><<<grid, kAttThreads, smem, stream>>>(*a.k_map, *a.v_map, a);
     }

@@ -10,159 +10,234 @@
 //
 // The scan is HBM-bound: each cached position carries H x 64 bf16 index-key
 // values (128 B per head) that are read exactly once.  Work unit = one
-// 64-position block of one sequence with all H heads, which is H x 8 KB of
-// contiguous memory.  The grid is a multiple of the SM count; CTA c takes an
-// even share of all units of all decode sequences (the split is computed on
-// the device from the per-sequence lengths, so ragged batches balance).
-// Every thread owns one 16-byte slice (8 dims) of one head and issues all of
-// its 16-byte loads of a unit before using them; eight lanes complete a dot
-// product with three shuffles.
+// 64-position block of one sequence with all H heads: H x 8 KB of contiguous
+// memory (token-major cache).  One CTA per SM takes an even share of all
+// units of all decode sequences (the split is computed on the device from
+// the per-sequence lengths, so ragged batches balance).  A producer lane
+// streams units into a ring of shared-memory stages with TMA tile loads (one
+// 64-position x 64-dim box per head, 128-byte swizzle, mbarrier completion),
+// keeping up to kStages units (192 KB) in flight per SM; consumer warp w
+// owns stage w and reduces whole units on its own, so the loop has no
+// CTA-wide barrier.  The dot products run on the tensor cores (mma.sync
+// m16n8k16: A = 16 positions x 16 index dims from ldmatrix, B = the index
+// query in column 0), about 50 instructions per head and block instead of
+// ~500 on the FP32 pipes; fp32 accumulation keeps integer scores exact.
 #include "common.cuh"
 #include "internal.h"
 
 namespace msa {
 
-constexpr int kScanThreads = 256;
+template <int H>
+struct ScanCfg {
+    static constexpr int kHeadBytes = kBlock * kIndexDim * 2;                 // 8 KB: [64 pos][64 dims]
+    static constexpr int kUnitBytes = H * kHeadBytes;
+    static constexpr int kStages = (H == 8) ? 3 : 6;                          // <= 192 KB of ring
+    static constexpr int kConsumers = kStages;                                // one warp per stage
+    static constexpr int kThreads = 32 * (kConsumers + 1);                    // + producer warp
+};
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ void mma_bf16_16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                               uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+struct ScanSeqState {
+    int b = -1, L = 0, r = 0;
+    int64_t start = 0;
+};
+
+// Advance to the sequence holding unit u and refresh its metadata.
+__device__ __forceinline__ bool scan_locate(const ScanArgs& a, const int32_t* prefix, int64_t u, int& b,
+                                            ScanSeqState& st) {
+    while (u >= prefix[b + 1]) ++b;
+    if (b != st.b) {
+        st.b = b;
+        const int r = a.cu_rows[b];
+        int L = min(max(a.cache_lens[b], 0), a.max_cache_len);
+        const int64_t start = a.cache_starts[b];
+        if (r < 0 || r >= a.total_rows || start < 0 || start + L > a.cache_tokens) L = 0;  // inconsistent: skip
+        st.L = L;
+        st.r = r < 0 ? 0 : (r >= a.total_rows ? a.total_rows - 1 : r);
+        st.start = start;
+        return true;
+    }
+    return false;
+}
 
 template <int H>
-__global__ void __launch_bounds__(kScanThreads) decode_scan_kernel(
-    const uint16_t* __restrict__ iq, const uint16_t* __restrict__ ik, const int32_t* __restrict__ cu_rows,
-    const int32_t* __restrict__ cache_lens, const int64_t* __restrict__ cache_starts, int num_seqs,
-    int total_rows, int max_cache_len, int64_t cache_tokens, int max_blocks, float* __restrict__ pooled,
-    int32_t* __restrict__ clear_words, int n_clear) {
-    static_assert(32 % H == 0, "H must divide 32");
-    constexpr int kLoads = 2 * H;              // 16-byte loads per thread per unit
-    constexpr int kPosPerIter = 32 / H;        // positions covered by one load round
-    extern __shared__ int32_t prefix[];        // [num_seqs + 1] units before sequence b
-    __shared__ float red[kScanThreads / 8];    // one slot per 8-lane group
-    __shared__ int warp_tot[kScanThreads / 32];
+__global__ void __launch_bounds__(ScanCfg<H>::kThreads, 1) decode_scan_kernel(const __grid_constant__ CUtensorMap ik_map,
+                                                                             const ScanArgs a) {
+    using Cfg = ScanCfg<H>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* full = reinterpret_cast<uint64_t*>(ring + Cfg::kStages * Cfg::kUnitBytes);
+    uint64_t* empty = full + Cfg::kStages;
+    int32_t* prefix = reinterpret_cast<int32_t*>(empty + Cfg::kStages);  // [num_seqs + 1]
+    __shared__ int warp_tot[Cfg::kThreads / 32];
 
-    const int tid = threadIdx.x;
-    // The attention kernel that follows uses these counters; clear them here.
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    // The attention kernel that follows uses these words; clear them here.
     if (blockIdx.x == 0)
-        for (int i = tid; i < n_clear; i += kScanThreads) clear_words[i] = 0;
-
-    // Units per sequence: ceil(L/64) for decode sequences, 0 otherwise.
-    // Block-wide exclusive scan in chunks of kScanThreads.
+        for (int i = tid; i < a.n_clear; i += Cfg::kThreads) a.clear_words[i] = 0;
+    if (tid == 0) {
+        for (int s = 0; s < Cfg::kStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        fence_mbar_init();
+    }
+    // Units per sequence: ceil(L/64) for decode sequences, 0 otherwise
+    // (block-wide exclusive scan in chunks of kThreads).
     int carry = 0;
-    for (int base = 0; base < num_seqs; base += kScanThreads) {
+    for (int base = 0; base < a.num_seqs; base += Cfg::kThreads) {
         const int b = base + tid;
         int units = 0;
-        if (b < num_seqs && cu_rows[b + 1] - cu_rows[b] == 1) {
-            const int L = min(max(cache_lens[b], 0), max_cache_len);
+        if (b < a.num_seqs && a.cu_rows[b + 1] - a.cu_rows[b] == 1) {
+            const int L = min(max(a.cache_lens[b], 0), a.max_cache_len);
             units = (L + kBlock - 1) / kBlock;
         }
-        int incl = units;  // inclusive warp scan
+        int incl = units;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            int v = __shfl_up_sync(0xffffffffu, incl, o);
-            if ((tid & 31) >= o) incl += v;
+            const int v = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += v;
         }
-        if ((tid & 31) == 31) warp_tot[tid >> 5] = incl;
+        if (lane == 31) warp_tot[warp] = incl;
         __syncthreads();
-        int before = 0;
-        for (int w = 0; w < (tid >> 5); ++w) before += warp_tot[w];
-        if (b < num_seqs) prefix[b] = carry + before + incl - units;
-        int chunk_total = 0;
-        for (int w = 0; w < kScanThreads / 32; ++w) chunk_total += warp_tot[w];
+        int before = 0, chunk_total = 0;
+        for (int w = 0; w < Cfg::kThreads / 32; ++w) {
+            if (w < warp) before += warp_tot[w];
+            chunk_total += warp_tot[w];
+        }
+        if (b < a.num_seqs) prefix[b] = carry + before + incl - units;
         __syncthreads();
         carry += chunk_total;
     }
-    if (tid == 0) prefix[num_seqs] = carry;
+    if (tid == 0) prefix[a.num_seqs] = carry;
     __syncthreads();
 
     const int64_t total = carry;
     const int64_t u0 = total * blockIdx.x / gridDim.x;
     const int64_t u1 = total * (blockIdx.x + 1) / gridDim.x;
-    if (u0 >= u1) return;
-
-    const int part = tid & 7;                  // which 8 dims of the head
-    const int h = (tid >> 3) % H;              // head of this thread
-    const int pos_off = tid / (8 * H);         // position offset within a round
-
-    // first sequence of this CTA's range
-    int b = 0;
+    const int n = static_cast<int>(u1 - u0);
+    if (n <= 0) return;
+    int b0 = 0;
     {
-        int lo = 0, hi = num_seqs;  // largest b with prefix[b] <= u0
+        int lo = 0, hi = a.num_seqs;  // largest b with prefix[b] <= u0
         while (hi - lo > 1) {
-            int mid = (lo + hi) >> 1;
+            const int mid = (lo + hi) >> 1;
             if (prefix[mid] <= u0) lo = mid; else hi = mid;
         }
-        b = lo;
+        b0 = lo;
     }
-    int cur_b = -1;
-    float qv[8];
-    int L = 0;
-    int64_t start = 0;
 
-    for (int64_t u = u0; u < u1; ++u) {
-        while (u >= prefix[b + 1]) ++b;
-        if (b != cur_b) {
-            cur_b = b;
-            const int r = min(max(cu_rows[b], 0), total_rows - 1);
-            const uint4 w = *reinterpret_cast<const uint4*>(iq + (static_cast<int64_t>(r) * H + h) * kIndexDim + part * 8);
-            qv[0] = bf16_lo(w.x); qv[1] = bf16_hi(w.x); qv[2] = bf16_lo(w.y); qv[3] = bf16_hi(w.y);
-            qv[4] = bf16_lo(w.z); qv[5] = bf16_hi(w.z); qv[6] = bf16_lo(w.w); qv[7] = bf16_hi(w.w);
-            L = min(max(cache_lens[b], 0), max_cache_len);
-            start = cache_starts[b];
-            if (start < 0 || start + L > cache_tokens || cu_rows[b] != r) L = 0;  // inconsistent metadata: pool nothing
+    if (warp == Cfg::kConsumers) {
+        // ---------------- producer: one lane streams units into the ring
+        if (lane == 0) {
+            prefetch_tmap(&ik_map);
+            int b = b0;
+            ScanSeqState st;
+            for (int i = 0; i < n; ++i) {
+                const int64_t u = u0 + i;
+                scan_locate(a, prefix, u, b, st);
+                const int j = static_cast<int>(u - prefix[b]);
+                const int npos = max(0, min(kBlock, st.L - j * kBlock));
+                const int s = i % Cfg::kStages;
+                if (i >= Cfg::kStages && !mbar_wait(&empty[s], ((i / Cfg::kStages) - 1) & 1, a.err)) break;
+                if (npos > 0) {
+                    // whole 64-position boxes; rows past the sequence are masked by the consumer
+                    // and rows past the cache are zero-filled by the copy engine
+                    mbar_arrive_expect_tx(&full[s], Cfg::kUnitBytes);
+                    const int tok = static_cast<int>(st.start + static_cast<int64_t>(j) * kBlock);
+#pragma unroll
+                    for (int h = 0; h < H; ++h)
+                        tma_load_3d(ring + s * Cfg::kUnitBytes + h * Cfg::kHeadBytes, &ik_map, &full[s], 0, h, tok);
+                } else {
+                    mbar_arrive_expect_tx(&full[s], 0);
+                }
+            }
         }
+        return;
+    }
+
+    // ---------------- consumer warp `warp` owns stage `warp`
+    // B fragment of mma.m16n8k16 (col-major 16 x 8): lane (grp = lane/4,
+    // tig = lane%4) holds B[2tig, 2tig+1][grp] and B[2tig+8, 2tig+9][grp].
+    // Column 0 is the index query, the other columns are zero, so the scores
+    // land in column 0 of the accumulator (lanes with tig == 0).
+    const int grp = lane >> 2, tig = lane & 3;
+    int b = b0;
+    ScanSeqState st;
+    const uint32_t stage = smem_u32(ring + warp * Cfg::kUnitBytes);
+    for (int i = warp; i < n; i += Cfg::kStages) {
+        const int64_t u = u0 + i;
+        scan_locate(a, prefix, u, b, st);
+        const uint32_t* q32 = reinterpret_cast<const uint32_t*>(a.iq + static_cast<int64_t>(st.r) * H * kIndexDim);
         const int j = static_cast<int>(u - prefix[b]);
-        const int npos = min(kBlock, L - j * kBlock);
-        const uint16_t* blk = ik + (start + static_cast<int64_t>(j) * kBlock) * (H * kIndexDim);
-
-        uint4 v[kLoads];
+        const int npos = max(0, min(kBlock, st.L - j * kBlock));
+        if (!mbar_wait(&full[warp], (i / Cfg::kStages) & 1, a.err)) break;
+        float mine = -INFINITY;  // lane h < H keeps head h's block maximum
+#pragma unroll 1
+        for (int h = 0; h < H; ++h) {
+            uint32_t bq[4][2];  // this head's index query as B fragments (L1-resident row)
 #pragma unroll
-        for (int i = 0; i < kLoads; ++i) {
-            const int pos = i * kPosPerIter + pos_off;
-            if (pos < npos)
-                v[i] = ld_stream_v4(blk + (static_cast<int64_t>(pos) * H + h) * kIndexDim + part * 8);
-            else
-                v[i] = make_uint4(0, 0, 0, 0);
-        }
-        float mx = -INFINITY;
+            for (int kk = 0; kk < 4; ++kk) {
+                bq[kk][0] = grp == 0 ? __ldg(q32 + h * 32 + kk * 8 + tig) : 0u;
+                bq[kk][1] = grp == 0 ? __ldg(q32 + h * 32 + kk * 8 + 4 + tig) : 0u;
+            }
+            float c[4][4];
 #pragma unroll
-        for (int i = 0; i < kLoads; ++i) {
-            float s = qv[0] * bf16_lo(v[i].x);
-            s = fmaf(qv[1], bf16_hi(v[i].x), s);
-            s = fmaf(qv[2], bf16_lo(v[i].y), s);
-            s = fmaf(qv[3], bf16_hi(v[i].y), s);
-            s = fmaf(qv[4], bf16_lo(v[i].z), s);
-            s = fmaf(qv[5], bf16_hi(v[i].z), s);
-            s = fmaf(qv[6], bf16_lo(v[i].w), s);
-            s = fmaf(qv[7], bf16_hi(v[i].w), s);
-            s += __shfl_xor_sync(0xffffffffu, s, 1);
-            s += __shfl_xor_sync(0xffffffffu, s, 2);
-            s += __shfl_xor_sync(0xffffffffu, s, 4);
-            const int pos = i * kPosPerIter + pos_off;
-            if (pos < npos) mx = fmaxf(mx, s);
-        }
-        if (part == 0) red[tid >> 3] = mx;
-        __syncthreads();
-        if (tid < H) {
+            for (int mt = 0; mt < 4; ++mt) c[mt][0] = c[mt][1] = c[mt][2] = c[mt][3] = 0.f;
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+#pragma unroll
+                for (int mt = 0; mt < 4; ++mt) {
+                    const int mi = lane >> 3;
+                    const int row = mt * 16 + (mi & 1) * 8 + (lane & 7);
+                    const int chunk = kk * 2 + (mi >> 1);
+                    uint32_t a0, a1, a2, a3;
+                    ldsm_x4(stage + h * Cfg::kHeadBytes + row * 128 + ((chunk ^ (row & 7)) << 4), a0, a1, a2, a3);
+                    mma_bf16_16816(c[mt], a0, a1, a2, a3, bq[kk][0], bq[kk][1]);
+                }
+            // column 0: c[mt][0] is position 16mt + grp, c[mt][2] is 16mt + grp + 8
             float m = -INFINITY;
-            for (int g = tid; g < kScanThreads / 8; g += H) m = fmaxf(m, red[g]);
-            if (npos > 0) pooled[(static_cast<int64_t>(b) * H + tid) * max_blocks + j] = m;
+#pragma unroll
+            for (int mt = 0; mt < 4; ++mt) {
+                if (mt * 16 + grp < npos) m = fmaxf(m, c[mt][0]);
+                if (mt * 16 + grp + 8 < npos) m = fmaxf(m, c[mt][2]);
+            }
+            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
+            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
+            m = __shfl_sync(0xffffffffu, m, 0);
+            if (lane == h) mine = m;
         }
-        __syncthreads();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[warp]);  // stage reusable
+        if (npos > 0 && lane < H) a.pooled[(static_cast<int64_t>(b) * H + lane) * a.max_blocks + j] = mine;
     }
 }
 
 template <int H>
 static cudaError_t launch_scan(const ScanArgs& a, cudaStream_t stream) {
-    const size_t smem = static_cast<size_t>(a.num_seqs + 1) * sizeof(int32_t);
-    int occ = 0;
-    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, decode_scan_kernel<H>, kScanThreads, smem);
+    using Cfg = ScanCfg<H>;
+    const size_t smem = 1024 + static_cast<size_t>(Cfg::kStages) * Cfg::kUnitBytes + 2 * Cfg::kStages * sizeof(uint64_t) +
+                        static_cast<size_t>(a.num_seqs + 1) * sizeof(int32_t);
+    cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(decode_scan_kernel<H>), smem);
     if (e != cudaSuccess) return e;
-    if (smem > 48 * 1024) {
-        e = cudaFuncSetAttribute(decode_scan_kernel<H>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-        if (e != cudaSuccess) return e;
-    }
-    int64_t grid = static_cast<int64_t>(device_sm_count()) * (occ > 0 ? occ : 1);
+    int64_t grid = device_sm_count();
     if (a.unit_bound < grid) grid = a.unit_bound > 0 ? a.unit_bound : 1;
-    decode_scan_kernel<H><<<static_cast<unsigned>(grid), kScanThreads, smem, stream>>>(
-        a.iq, a.ik, a.cu_rows, a.cache_lens, a.cache_starts, a.num_seqs, a.total_rows, a.max_cache_len, a.cache_tokens,
-        a.max_blocks, a.pooled, a.clear_words, a.n_clear);
+    decode_scan_kernel<H><<<static_cast<unsigned>(grid), Cfg::kThreads, smem, stream>>>(*a.ik_map, a);
     return cudaGetLastError();
 }
 

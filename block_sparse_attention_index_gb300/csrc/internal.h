@@ -13,6 +13,7 @@ namespace msa {
 constexpr int kPartialFloats = 16 * 128 + 16 + 16;
 
 struct ScanArgs {
+    const CUtensorMap* ik_map;  // ik as (Di, H, tokens), box 64 x 1 x 64, host copy
     int H;
     const uint16_t* iq;
     const uint16_t* ik;
@@ -28,6 +29,7 @@ struct ScanArgs {
     float* pooled;        // [B, H, max_blocks]
     int32_t* clear_words; // zeroed by the scan (tickets of the attention kernel)
     int n_clear;
+    uint32_t* err;
 };
 
 struct DecodeAttendArgs {
@@ -107,5 +109,9 @@ cudaError_t run_prefill_index(const PrefillIndexArgs& a, cudaStream_t stream);
 cudaError_t run_prefill_attend(const PrefillAttendArgs& a, cudaStream_t stream);
 
 int device_sm_count();
+
+// Raise a kernel's dynamic shared-memory limit to at least `bytes` on the
+// current device; the driver call is made only when the limit grows.
+cudaError_t ensure_smem_limit(const void* kernel, size_t bytes);
 
 }  // namespace msa

@@ -39,7 +39,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 msa_status check_problem(const msa_problem* p) {
     if (p == nullptr) return fail(MSA_ERR_INVALID_ARG, "problem is null");
     if (p->num_seqs < 1) return fail(MSA_ERR_INVALID_ARG, "num_seqs must be >= 1 (got %d)", p->num_seqs);
-    if (p->num_seqs > 65535) return fail(MSA_ERR_UNSUPPORTED, "num_seqs > 65535");
+    if (p->num_seqs > 4096) return fail(MSA_ERR_UNSUPPORTED, "num_seqs > 4096");
     if (p->head_dim != msa::kHeadDim) return fail(MSA_ERR_UNSUPPORTED, "head_dim must be 128 (got %d)", p->head_dim);
     if (p->index_dim != msa::kIndexDim)
         return fail(MSA_ERR_UNSUPPORTED, "index_dim must be 64 (got %d)", p->index_dim);
@@ -161,7 +161,14 @@ struct Marks {
     cudaStream_t stream;
     msa_status mark(int i) {
         if (events && i < n && events[i]) {
-            cudaError_t e = cudaEventRecord(static_cast<cudaEvent_t>(events[i]), stream);
+            // inside a stream capture, record an event node of the graph so the
+            // mark is taken at every replay
+            cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+            cudaError_t e = cudaStreamIsCapturing(stream, &cs);
+            if (e != cudaSuccess) return cuda_fail(e, "cudaStreamIsCapturing");
+            e = cudaEventRecordWithFlags(static_cast<cudaEvent_t>(events[i]), stream,
+                                         cs == cudaStreamCaptureStatusActive ? cudaEventRecordExternal
+                                                                             : cudaEventRecordDefault);
             if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
         }
         return MSA_OK;
@@ -186,6 +193,31 @@ int msa::device_sm_count() {
         c = v > 0 ? v : 1;
     }
     return c;
+}
+
+cudaError_t msa::ensure_smem_limit(const void* kernel, size_t bytes) {
+    struct Entry {
+        const void* kernel;
+        int device;
+        size_t bytes;
+    };
+    static std::mutex mu;
+    static Entry table[256];
+    static int used = 0;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < used; ++i)
+        if (table[i].kernel == kernel && table[i].device == dev) {
+            if (table[i].bytes >= bytes) return cudaSuccess;
+            e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+            if (e == cudaSuccess) table[i].bytes = bytes;
+            return e;
+        }
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+    if (e == cudaSuccess && used < 256) table[used++] = Entry{kernel, dev, bytes};
+    return e;
 }
 
 extern "C" {
@@ -437,10 +469,13 @@ msa_status msa_forward_marked(const msa_problem* p, const void* q, const void* i
         if ((s = make_map(&iqm, iq, 64, H, p->total_rows, 64, 1, 128, "iq")) != MSA_OK) return s;
         if ((s = make_map(&ikm, ik_cache, 64, H, T, 64, 1, 256, "ik_cache")) != MSA_OK) return s;
     }
+    CUtensorMap ik_scan;
+    if (dec && (s = make_map(&ik_scan, ik_cache, 64, H, T, 64, 1, 64, "ik_cache")) != MSA_OK) return s;
     if ((s = marks.mark(0)) != MSA_OK) return s;
     cudaError_t e;
     if (dec) {
         msa::ScanArgs sa{};
+        sa.ik_map = &ik_scan;
         sa.H = p->num_kv_heads;
         sa.iq = static_cast<const uint16_t*>(iq);
         sa.ik = static_cast<const uint16_t*>(ik_cache);
@@ -457,6 +492,7 @@ msa_status msa_forward_marked(const msa_problem* p, const void* q, const void* i
         sa.pooled = reinterpret_cast<float*>(ws + l.pooled);
         sa.clear_words = reinterpret_cast<int32_t*>(ws + l.err);
         sa.n_clear = static_cast<int>(l.header_bytes / sizeof(int32_t));
+        sa.err = reinterpret_cast<uint32_t*>(ws + l.err);
         if ((e = msa::run_decode_scan(sa, st)) != cudaSuccess) return cuda_fail(e, "decode scan launch");
         if ((s = marks.mark(1)) != MSA_OK) return s;
         msa::DecodeAttendArgs da = decode_args(p, &km, &vm, q, out, ws, l);

@@ -344,8 +344,7 @@ __global__ void __launch_bounds__(kPaThreads, 1) prefill_attend_kernel(const __g
 
 cudaError_t run_prefill_attend(const PrefillAttendArgs& a, cudaStream_t stream) {
     const size_t smem = sizeof(AttendSmem) + 1024;
-    cudaError_t e = cudaFuncSetAttribute(prefill_attend_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
+    cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(prefill_attend_kernel), smem);
     if (e != cudaSuccess) return e;
     const int64_t items = static_cast<int64_t>(a.total_rows) * a.H;
     const int grid = static_cast<int>(items < device_sm_count() ? items : device_sm_count());

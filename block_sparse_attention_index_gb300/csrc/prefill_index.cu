@@ -233,8 +233,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1) prefill_index_kernel(const __g
 
 cudaError_t run_prefill_index(const PrefillIndexArgs& a, cudaStream_t stream) {
     const size_t smem = sizeof(IndexSmem) + 1024;
-    cudaError_t e = cudaFuncSetAttribute(prefill_index_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
+    cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(prefill_index_kernel), smem);
     if (e != cudaSuccess) return e;
     const int tiles = (a.total_rows + kIdxRows - 1) / kIdxRows + a.num_seqs;  // upper bound
     dim3 grid(tiles, a.H);

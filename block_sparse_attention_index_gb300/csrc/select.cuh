@@ -71,6 +71,7 @@ __device__ int cta_select(const float* pooled, int J, int top_k, int* sel, Selec
     }
     // 1. per-thread maxima
     uint64_t mine = 0;
+#pragma unroll 8
     for (int j = tid; j < J; j += NT) {
         uint64_t key = block_key(pooled[j], j);
         mine = key > mine ? key : mine;
@@ -87,6 +88,7 @@ __device__ int cta_select(const float* pooled, int J, int top_k, int* sel, Selec
     __syncthreads();
     const uint64_t tau = sm.tau;
     // 3. gather candidates >= tau
+#pragma unroll 8
     for (int j = tid; j < J; j += NT) {
         uint64_t key = block_key(pooled[j], j);
         if (key >= tau) {

@@ -104,8 +104,7 @@ cudaError_t run_select_blocks(const StagedArgs& a, const float* scores, int64_t 
                               cudaStream_t stream) {
     const int max_blocks = (a.max_cache_len + kBlock - 1) / kBlock;
     const size_t smem = static_cast<size_t>(max_blocks) * sizeof(float);
-    cudaError_t e = cudaFuncSetAttribute(select_blocks_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
+    cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(select_blocks_kernel), smem);
     if (e != cudaSuccess) return e;
     dim3 grid(a.total_rows, a.H);
     select_blocks_kernel<<<grid, kStagedThreads, smem, stream>>>(a, scores, ld, sel, nsel);

@@ -53,7 +53,7 @@
  *     failure.  Nothing traps on the device.
  *   - Supported set: D = 128, Di = 64, S = 64, 1 <= top_k <= 16,
  *     1 <= G <= 16, H in {1, 2, 4, 8}, max_cache_len <= 2^21,
- *     num_seqs <= 65535; other values return MSA_ERR_UNSUPPORTED.
+ *     num_seqs <= 4096; other values return MSA_ERR_UNSUPPORTED.
  *   - Thread safety: calls from several host threads are safe; the only
  *     library state is a per-device set-up flag and the thread-local error
  *     message.  Two calls sharing one workspace must be ordered on the GPU.
