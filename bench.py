@@ -208,18 +208,24 @@ def measure_gpu(w, steps, warmup, dev, dist_on, flush_bytes=512 << 20, e2e_steps
     for ev in marks:
         ev.record(stream)  # torch creates the CUDA event on its first record
     torch.cuda.synchronize(dev)
-    graph = None
+    graph = graph_marked = None
     if use_graph:
         # one step captured once (the library enqueues only its own kernels and event
         # records, never allocates or synchronises) and replayed: no host gaps between
-        # the step's kernels
-        graph = torch.cuda.CUDAGraph()
+        # the step's kernels.  The timed graph has no marks (a mark between two kernels
+        # would break their programmatic-launch overlap); a second graph with marks
+        # gives the per-stage times.
         cap = torch.cuda.Stream(dev)
-        cap.wait_stream(stream)
-        with torch.cuda.stream(cap):
-            with torch.cuda.graph(graph, stream=cap):
-                step(marks)
-        stream.wait_stream(cap)
+        graphs = []
+        for ev in (None, marks):
+            g = torch.cuda.CUDAGraph()
+            cap.wait_stream(stream)
+            with torch.cuda.stream(cap):
+                with torch.cuda.graph(g, stream=cap):
+                    step(ev)
+            stream.wait_stream(cap)
+            graphs.append(g)
+        graph, graph_marked = graphs
         torch.cuda.synchronize(dev)
     begin = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
@@ -235,16 +241,23 @@ def measure_gpu(w, steps, warmup, dev, dist_on, flush_bytes=512 << 20, e2e_steps
             if graph is not None:
                 graph.replay()
             else:
-                step(marks)
+                step()
             ends[i].record(stream)
             ends[i].synchronize()
             step_ms.append(begin[i].elapsed_time(ends[i]))
-            stage_ms.append([marks[j].elapsed_time(marks[j + 1]) for j in range(4)])
         torch.cuda.synchronize(dev)
     wall = time.perf_counter() - t0
     if dist_on:
         td.barrier()
     assert msa.error_word(ws) == 0
+    for i in range(steps):  # per-stage times, outside the timed region
+        flush_l2(i)
+        if graph_marked is not None:
+            graph_marked.replay()
+        else:
+            step(marks)
+        marks[4].synchronize()
+        stage_ms.append([marks[j].elapsed_time(marks[j + 1]) for j in range(4)])
     total_ms = float(sum(step_ms))
     if dist_on:
         t = torch.tensor([total_ms], dtype=torch.float64, device=dev)

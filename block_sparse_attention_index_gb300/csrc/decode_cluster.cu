@@ -1,0 +1,360 @@
+// Decode stage 2b+3 as one thread-block cluster per (sequence, KV head).
+//
+// PR #1388 "minimax_m3: a CUDA backend for MiniMax-M3.1-Flash ...", commit
+// text of the native Metal family: decode attention runs over the kept
+// blocks in partials.  Here the partials never leave the chip:
+//   - the 8 CTAs of a cluster each take two of the (up to 16) kept blocks,
+//     stage their K and V by TMA (128-byte swizzle) and compute S = Q K^T
+//     and O = P V for the group's 16 query heads on mma.sync (P split into
+//     bf16 hi + lo parts so the weights keep ~16 significant bits);
+//   - each CTA stores the (m, l, O) rows of heads 2c and 2c+1 straight into
+//     the shared memory of CTA c of the cluster (distributed shared memory,
+//     remote stores: no round trip); after one cluster barrier CTA c
+//     combines its two heads from its own shared memory:
+//         M = max m_c,  L = sum l_c 2^(m_c - M),  out = sum O_c 2^(m_c - M) / L
+//   - the kept blocks come from the pooled index scores (every CTA runs the
+//     same deterministic selection) or from a given list.
+// Launched after the index scan as a programmatic dependent launch: q and
+// the sequence metadata are read before waiting for the scan to finish.
+#include "common.cuh"
+#include "internal.h"
+#include "select.cuh"
+
+namespace msa {
+
+constexpr int kClThreads = 128;
+constexpr int kCluster = 8;  // CTAs per (sequence, KV head); 2 kept blocks each
+
+struct __align__(1024) ClusterSmem {
+    uint16_t k[2][2][64 * 64];  // [block][dim half][key][64 dims], 128B-swizzled by TMA
+    uint16_t v[2][2][64 * 64];
+    uint16_t q[16 * 128];       // [head][dim], 16-byte chunks XOR-swizzled by row
+    uint16_t p[2][16 * 128];    // [hi/lo][head][128 keys], same swizzle
+    float recv_o[kCluster][2][128];  // partial outputs of my two heads, one row per source CTA
+    float recv_ml[kCluster][2][2];   // their (max in the log2 domain, sum)
+    float wmax[4][16];
+    float wsum[4][16];
+    uint64_t bar;
+    int32_t sel[kMaxTopK];
+    int32_t nsel;
+    int32_t meta_ok;
+    SelectSmem<kClThreads> select;
+};
+
+__device__ __forceinline__ uint32_t cl_swz(int row, int chunk, int row_bytes) {
+    return row * row_bytes + ((chunk ^ (row & 7)) << 4);
+}
+
+__device__ __forceinline__ void cl_ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+__device__ __forceinline__ void cl_ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                             uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+__device__ __forceinline__ void cl_mma(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                                       uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+// All threads of all CTAs of the cluster; release/acquire orders shared-memory
+// writes before the barrier with reads after it.
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Address of `p` (this CTA's shared memory) in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t map_to_rank(const void* p, uint32_t rank) {
+    uint32_t out;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(out) : "r"(smem_u32(p)), "r"(rank));
+    return out;
+}
+__device__ __forceinline__ void st_cluster_f32x2(uint32_t addr, float x, float y) {
+    asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(x), "f"(y) : "memory");
+}
+// Split cluster barrier: arrive early, wait just before the first remote
+// shared-memory access (every peer has then started).
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.aligned;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// grid (kCluster, H, B), cluster (kCluster, 1, 1): CTA `rank` of the cluster of
+// (sequence b, KV head h) takes kept blocks rank and rank + kCluster.
+template <bool kSelGiven>
+__global__ void __launch_bounds__(kClThreads) decode_cluster_kernel(const __grid_constant__ CUtensorMap k_map,
+                                                                    const __grid_constant__ CUtensorMap v_map,
+                                                                    const DecodeAttendArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    ClusterSmem& sm = *reinterpret_cast<ClusterSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int rank = static_cast<int>(cluster_rank());
+    const int h = blockIdx.y, b = blockIdx.z;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int H = a.H, G = a.G;
+
+    // ---- prologue: only inputs that no earlier kernel of the step writes
+    const int r = a.cu_rows[b];
+    if (a.cu_rows[b + 1] - r != 1) return;  // not a decode sequence (the whole cluster returns)
+    const int L = a.cache_lens[b];
+    const int64_t start = a.cache_starts[b];
+    const bool meta_ok = !(r < 0 || r >= a.total_rows || L < 1 || L > a.max_cache_len || start < 0 ||
+                           start + L > a.cache_tokens);
+    if (tid == 0) {
+        mbar_init(&sm.bar, 1);
+        fence_mbar_init();
+    }
+    if (meta_ok) {
+        const uint16_t* qrow = a.q + (static_cast<int64_t>(r) * H * G + static_cast<int64_t>(h) * G) * kHeadDim;
+        for (int c = tid; c < 16 * 16; c += kClThreads) {  // 16 heads x 16 chunks of 8 dims
+            const int g = c >> 4, ch = c & 15;
+            uint4 val = make_uint4(0, 0, 0, 0);
+            if (g < G) val = *reinterpret_cast<const uint4*>(qrow + g * kHeadDim + ch * 8);
+            *reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(sm.q) + cl_swz(g, ch, 256)) = val;
+        }
+        if constexpr (kSelGiven) {
+            if (tid < kMaxTopK)
+                sm.sel[tid] = tid < a.top_k ? a.sel_in[(static_cast<int64_t>(r) * H + h) * a.top_k + tid] : -1;
+            if (tid == 0) sm.nsel = min(max(a.nsel_in[static_cast<int64_t>(r) * H + h], 0), a.top_k);
+        }
+    }
+    pdl_wait();  // the index scan (pooled scores, error word) is complete and visible
+    if (!meta_ok) {
+        if (tid == 0 && rank == 0) atomicOr(a.err, kErrBadMetadata);
+        return;  // the whole cluster returns: before any cluster barrier
+    }
+    cluster_arrive_relaxed();  // matched by cluster_wait() before the first remote store
+    const int p = L - 1;
+    const int J = p / kBlock;
+    if constexpr (!kSelGiven) {
+        const float* pooled = a.pooled + (static_cast<int64_t>(b) * H + h) * a.max_blocks;
+        const int n = cta_select<kClThreads>(pooled, J, a.top_k, sm.sel, sm.select);
+        if (tid == 0) sm.nsel = n;
+    }
+    __syncthreads();
+    const int nsel = sm.nsel;
+    if constexpr (!kSelGiven) {
+        if (rank == 0 && a.sel_out != nullptr && tid < a.top_k) {
+            a.sel_out[(static_cast<int64_t>(r) * H + h) * a.top_k + tid] = sm.sel[tid];
+            if (tid == 0) a.nsel_out[static_cast<int64_t>(r) * H + h] = nsel;
+        }
+    }
+    // ---- this CTA's blocks: kept blocks rank and rank + kCluster
+    int nmy = (rank < nsel) + (rank + kCluster < nsel);
+    int blk[2] = {J, J};
+    for (int i = 0; i < nmy; ++i) {
+        blk[i] = sm.sel[rank + i * kCluster];
+        if (blk[i] < 0 || blk[i] > J) {  // a given selection outside the causal range
+            if (tid == 0) atomicOr(a.err, kErrBadMetadata);
+            blk[i] = J;
+        }
+    }
+    if (tid == 0 && nmy > 0) {
+        mbar_arrive_expect_tx(&sm.bar, nmy * 4 * 64 * 64 * 2);
+        for (int i = 0; i < nmy; ++i) {
+            const int tok = static_cast<int>(start + static_cast<int64_t>(blk[i]) * kBlock);
+            tma_load_3d(sm.k[i][0], &k_map, &sm.bar, 0, h, tok);
+            tma_load_3d(sm.k[i][1], &k_map, &sm.bar, 64, h, tok);
+            tma_load_3d(sm.v[i][0], &v_map, &sm.bar, 0, h, tok);
+            tma_load_3d(sm.v[i][1], &v_map, &sm.bar, 64, h, tok);
+        }
+    }
+    __syncthreads();  // q visible to every warp
+    if (nmy > 0 && !__syncthreads_and(mbar_wait(&sm.bar, 0, a.err))) nmy = 0;  // copy never landed: no keys
+
+
+    // ---- S = Q K^T: warp w owns keys [32w, 32w+32) of this CTA's 128 (block w/2)
+    const int grp = lane >> 2, tig = lane & 3;
+    const int my_blk = warp >> 1, key0 = (warp & 1) * 32;  // key0: first key of the warp inside its block
+    const bool warp_live = my_blk < nmy;
+    const int wblk = my_blk == 0 ? blk[0] : blk[1];
+    float s[4][4];
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+    if (warp_live) {
+        const uint32_t q_base = smem_u32(sm.q);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {  // 16 dims per step
+            const int mi = lane >> 3;
+            uint32_t a0, a1, a2, a3;
+            cl_ldsm_x4(q_base + cl_swz((mi & 1) * 8 + (lane & 7), kk * 2 + (mi >> 1), 256), a0, a1, a2, a3);
+            const int dim = kk * 16 + (mi & 1) * 8;
+            const uint32_t kb = smem_u32(sm.k[my_blk][dim >> 6]);
+#pragma unroll
+            for (int pp = 0; pp < 2; ++pp) {  // two 8-key tiles per ldmatrix
+                const int key = key0 + pp * 16 + (mi >> 1) * 8 + (lane & 7);
+                uint32_t b0, b1, b2, b3;
+                cl_ldsm_x4(kb + cl_swz(key, (dim & 63) >> 3, 128), b0, b1, b2, b3);
+                cl_mma(s[pp * 2 + 0], a0, a1, a2, a3, b0, b1);
+                cl_mma(s[pp * 2 + 1], a0, a1, a2, a3, b2, b3);
+            }
+        }
+    }
+    // scale (log2 domain), causal mask inside the local block, row maxima
+    float rmax[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int key = key0 + nt * 8 + tig * 2 + (e & 1);
+            const bool valid = warp_live && wblk * kBlock + key <= p;
+            s[nt][e] = valid ? s[nt][e] * a.scale_log2 : -INFINITY;
+            rmax[e >> 1] = fmaxf(rmax[e >> 1], s[nt][e]);
+        }
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        rmax[i] = fmaxf(rmax[i], __shfl_xor_sync(0xffffffffu, rmax[i], 1));
+        rmax[i] = fmaxf(rmax[i], __shfl_xor_sync(0xffffffffu, rmax[i], 2));
+    }
+    if (tig == 0) {
+        sm.wmax[warp][grp] = rmax[0];
+        sm.wmax[warp][grp + 8] = rmax[1];
+    }
+    __syncthreads();
+    float m[2], lsum[2] = {0.f, 0.f};
+    m[0] = fmaxf(fmaxf(sm.wmax[0][grp], sm.wmax[1][grp]), fmaxf(sm.wmax[2][grp], sm.wmax[3][grp]));
+    m[1] = fmaxf(fmaxf(sm.wmax[0][grp + 8], sm.wmax[1][grp + 8]), fmaxf(sm.wmax[2][grp + 8], sm.wmax[3][grp + 8]));
+    // a row with no valid key in this CTA (nmy == 0) gets P = 0
+    const float msafe[2] = {m[0] == -INFINITY ? 0.f : m[0], m[1] == -INFINITY ? 0.f : m[1]};
+    uint8_t* phi = reinterpret_cast<uint8_t*>(sm.p[0]);
+    uint8_t* plo = reinterpret_cast<uint8_t*>(sm.p[1]);
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt) {
+        const float p0 = exp2f(s[nt][0] - msafe[0]), p1 = exp2f(s[nt][1] - msafe[0]);
+        const float p2 = exp2f(s[nt][2] - msafe[1]), p3 = exp2f(s[nt][3] - msafe[1]);
+        lsum[0] += p0 + p1;
+        lsum[1] += p2 + p3;
+        const int key = warp * 32 + nt * 8 + tig * 2;  // key index among this CTA's 128
+        const int chunk = key >> 3, within = (key & 7) * 2;
+        const uint32_t h01 = pack_bf16x2(p0, p1), h23 = pack_bf16x2(p2, p3);
+        *reinterpret_cast<uint32_t*>(phi + cl_swz(grp, chunk, 256) + within) = h01;
+        *reinterpret_cast<uint32_t*>(phi + cl_swz(grp + 8, chunk, 256) + within) = h23;
+        *reinterpret_cast<uint32_t*>(plo + cl_swz(grp, chunk, 256) + within) =
+            pack_bf16x2(p0 - bf16_lo(h01), p1 - bf16_hi(h01));
+        *reinterpret_cast<uint32_t*>(plo + cl_swz(grp + 8, chunk, 256) + within) =
+            pack_bf16x2(p2 - bf16_lo(h23), p3 - bf16_hi(h23));
+    }
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        lsum[i] += __shfl_xor_sync(0xffffffffu, lsum[i], 1);
+        lsum[i] += __shfl_xor_sync(0xffffffffu, lsum[i], 2);
+    }
+    if (tig == 0) {
+        sm.wsum[warp][grp] = lsum[0];
+        sm.wsum[warp][grp + 8] = lsum[1];
+    }
+    __syncthreads();
+
+    // ---- O[:, 32w .. 32w+32) = P V over this CTA's 64 * nmy keys
+    float o[4][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+    for (int kk = 0; kk < 4 * nmy; ++kk) {  // 16 keys per step
+        const int mi = lane >> 3;
+        const int row = (mi & 1) * 8 + (lane & 7);
+        uint32_t a0, a1, a2, a3, l0, l1, l2, l3;
+        cl_ldsm_x4(smem_u32(sm.p[0]) + cl_swz(row, kk * 2 + (mi >> 1), 256), a0, a1, a2, a3);
+        cl_ldsm_x4(smem_u32(sm.p[1]) + cl_swz(row, kk * 2 + (mi >> 1), 256), l0, l1, l2, l3);
+        const int vb = kk >> 2;  // block of these keys
+#pragma unroll
+        for (int np = 0; np < 2; ++np) {  // pairs of 8-dim tiles
+            const int key = (kk & 3) * 16 + (mi & 1) * 8 + (lane & 7);
+            const int dim = warp * 32 + np * 16 + (mi >> 1) * 8;
+            uint32_t b0, b1, b2, b3;
+            cl_ldsm_x4_t(smem_u32(sm.v[vb][dim >> 6]) + cl_swz(key, (dim & 63) >> 3, 128), b0, b1, b2, b3);
+            cl_mma(o[np * 2 + 0], a0, a1, a2, a3, b0, b1);
+            cl_mma(o[np * 2 + 1], a0, a1, a2, a3, b2, b3);
+            cl_mma(o[np * 2 + 0], l0, l1, l2, l3, b0, b1);
+            cl_mma(o[np * 2 + 1], l0, l1, l2, l3, b2, b3);
+        }
+    }
+    // ---- push my partial rows to their owners: head g is finished by CTA g / 2
+    cluster_wait();
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+        const int g = grp + 8 * half;
+        if (g < G) {
+            const int owner = g >> 1, slot = g & 1;
+#pragma unroll
+            for (int nt = 0; nt < 4; ++nt) {
+                const int dim = warp * 32 + nt * 8 + tig * 2;
+                st_cluster_f32x2(map_to_rank(&sm.recv_o[rank][slot][dim], owner), o[nt][2 * half], o[nt][2 * half + 1]);
+            }
+        }
+    }
+    if (tid < G) {
+        const float mg = fmaxf(fmaxf(sm.wmax[0][tid], sm.wmax[1][tid]), fmaxf(sm.wmax[2][tid], sm.wmax[3][tid]));
+        const float lg = sm.wsum[0][tid] + sm.wsum[1][tid] + sm.wsum[2][tid] + sm.wsum[3][tid];
+        st_cluster_f32x2(map_to_rank(&sm.recv_ml[rank][tid & 1][0], tid >> 1), mg, lg);
+    }
+    cluster_sync();  // all pushes have landed; no remote access follows
+
+    // ---- combine my heads 2*rank and 2*rank + 1; thread t owns two dims of one
+    const int slot = tid >> 6;
+    const int g = 2 * rank + slot;
+    const int d = (tid & 63) * 2;
+    if (g < G) {
+        float M = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < kCluster; ++c) M = fmaxf(M, sm.recv_ml[c][slot][0]);
+        float Ls = 0.f, ox = 0.f, oy = 0.f;
+#pragma unroll
+        for (int c = 0; c < kCluster; ++c) {
+            const float mc = sm.recv_ml[c][slot][0];
+            const float w = mc == -INFINITY ? 0.f : exp2f(mc - M);
+            const float2 oc = *reinterpret_cast<const float2*>(&sm.recv_o[c][slot][d]);
+            Ls = fmaf(w, sm.recv_ml[c][slot][1], Ls);
+            ox = fmaf(w, oc.x, ox);
+            oy = fmaf(w, oc.y, oy);
+        }
+        const float inv = 1.f / Ls;
+        const int64_t oi = (static_cast<int64_t>(r) * H * G + static_cast<int64_t>(h) * G + g) * kHeadDim + d;
+        if (a.out_bf16)
+            *reinterpret_cast<uint32_t*>(reinterpret_cast<__nv_bfloat16*>(a.out) + oi) = pack_bf16x2(ox * inv, oy * inv);
+        else
+            *reinterpret_cast<float2*>(reinterpret_cast<float*>(a.out) + oi) = make_float2(ox * inv, oy * inv);
+    }
+}
+
+cudaError_t run_decode_cluster(const DecodeAttendArgs& a, bool after_scan, cudaStream_t stream) {
+    const size_t smem = sizeof(ClusterSmem) + 1024;
+    const bool given = a.pooled == nullptr;
+    const void* fn = given ? reinterpret_cast<const void*>(decode_cluster_kernel<true>)
+                           : reinterpret_cast<const void*>(decode_cluster_kernel<false>);
+    cudaError_t e = ensure_smem_limit(fn, smem);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(kCluster, a.H, a.num_seqs);
+    cfg.blockDim = dim3(kClThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kCluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = after_scan ? 2 : 1;  // overlap the prologue with the index scan's tail
+    if (given)
+        e = cudaLaunchKernelEx(&cfg, decode_cluster_kernel<true>, *a.k_map, *a.v_map, a);
+    else
+        e = cudaLaunchKernelEx(&cfg, decode_cluster_kernel<false>, *a.k_map, *a.v_map, a);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
+}  // namespace msa

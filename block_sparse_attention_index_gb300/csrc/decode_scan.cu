@@ -125,6 +125,9 @@ __global__ void __launch_bounds__(ScanCfg<H>::kThreads, 1) decode_scan_kernel(co
     }
     if (tid == 0) prefix[a.num_seqs] = carry;
     __syncthreads();
+    // the attention kernel may be scheduled now; it waits for this grid to
+    // finish before it reads the pooled scores
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     const int64_t total = carry;
     const int64_t u0 = total * blockIdx.x / gridDim.x;

@@ -100,7 +100,10 @@ constexpr int kNoAllocMaxPairs = 32;
 cudaError_t run_decode_attend_noalloc(DecodeAttendArgs a, cudaStream_t stream);
 
 cudaError_t run_decode_scan(const ScanArgs& a, cudaStream_t stream);
-cudaError_t run_decode_attend(const DecodeAttendArgs& a, cudaStream_t stream);
+cudaError_t run_decode_attend(const DecodeAttendArgs& a, cudaStream_t stream);  // ticket combine through global memory
+// Cluster form (combine through distributed shared memory); after_scan: launch
+// as a programmatic dependent of the index scan that precedes it.
+cudaError_t run_decode_cluster(const DecodeAttendArgs& a, bool after_scan, cudaStream_t stream);
 cudaError_t run_index_scores(const StagedArgs& a, const uint16_t* iq, const uint16_t* ik, float* scores,
                              int64_t ld, cudaStream_t stream);
 cudaError_t run_select_blocks(const StagedArgs& a, const float* scores, int64_t ld, int32_t* sel, int32_t* nsel,

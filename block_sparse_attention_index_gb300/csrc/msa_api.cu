@@ -340,7 +340,7 @@ msa_status msa_attend_decode(const msa_problem* p, const void* q, const void* k_
     a.pooled = nullptr;
     a.sel_in = sel;
     a.nsel_in = nsel;
-    e = msa::run_decode_attend(a, st);
+    e = msa::run_decode_cluster(a, false, st);
     return e == cudaSuccess ? MSA_OK : cuda_fail(e, "decode attention launch");
 }
 
@@ -500,7 +500,8 @@ msa_status msa_forward_marked(const msa_problem* p, const void* q, const void* i
         da.max_blocks = max_blocks;
         da.sel_out = sel;
         da.nsel_out = nsel;
-        if ((e = msa::run_decode_attend(da, st)) != cudaSuccess) return cuda_fail(e, "decode attention launch");
+        const bool pdl = events == nullptr || n_events < 2 || events[1] == nullptr;  // a mark in between breaks it
+        if ((e = msa::run_decode_cluster(da, pdl, st)) != cudaSuccess) return cuda_fail(e, "decode attention launch");
         if ((s = marks.mark(2)) != MSA_OK) return s;
     } else {
         if ((e = cudaMemsetAsync(ws, 0, l.header_bytes, st)) != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");

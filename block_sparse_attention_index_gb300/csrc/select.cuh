@@ -9,10 +9,11 @@
 //
 // Each candidate j is a distinct 64-bit key (ordered score, ~j), so the
 // result does not depend on thread order:
-//   1. every thread takes the largest key among its strided candidates;
-//   2. tau = the (k)-th largest of those per-thread maxima (rank counting) --
-//      tau is a lower bound of the k-th largest key overall, because the
-//      per-thread maxima are k distinct candidates;
+//   1. every thread takes the largest key among its strided candidates
+//      (the scores are staged in shared memory on the way when they fit);
+//   2. every warp sorts its 32 per-thread maxima (bitonic, shuffles) and
+//      takes the k-th largest: that is a lower bound of the k-th largest key
+//      overall (k distinct candidates reach it); tau = the largest bound;
 //   3. candidates >= tau are gathered (a handful for typical data) and
 //      ranked exactly by counting; the k best are placed by rank;
 //   4. if more than kCandCap candidates pass the threshold (adversarial
@@ -24,10 +25,12 @@
 namespace msa {
 
 constexpr int kCandCap = 512;
+constexpr int kSelStage = 4096;  // pooled scores staged in shared memory up to this many blocks
 
 template <int NT>
 struct SelectSmem {
-    uint64_t thread_max[NT];
+    float vals[kSelStage];
+    uint64_t warp_tau[NT / 32];
     uint64_t cand[kCandCap];
     uint64_t red[NT / 32];
     uint64_t tau;
@@ -69,30 +72,43 @@ __device__ int cta_select(const float* pooled, int J, int top_k, int* sel, Selec
         __syncthreads();
         return J + 1;
     }
-    // 1. per-thread maxima
+    // 1. per-thread maxima (and the scores staged in shared memory)
+    const bool staged = J <= kSelStage;
     uint64_t mine = 0;
 #pragma unroll 8
     for (int j = tid; j < J; j += NT) {
-        uint64_t key = block_key(pooled[j], j);
+        const float v = pooled[j];
+        if (staged) sm.vals[j] = v;
+        const uint64_t key = block_key(v, j);
         mine = key > mine ? key : mine;
     }
-    sm.thread_max[tid] = mine;
+    // 2. per-warp bound: sort the 32 maxima descending, take the others-th;
+    // warp 0 always holds min(J, 32) >= others candidates, so tau > 0
+    {
+        const int lane = tid & 31;
+        uint64_t key = mine;
+#pragma unroll
+        for (int k = 2; k <= 32; k <<= 1)
+#pragma unroll
+            for (int jj = k >> 1; jj > 0; jj >>= 1) {
+                const uint64_t other = __shfl_xor_sync(0xffffffffu, key, jj);
+                const bool keep_max = ((lane & k) == 0) == ((lane & jj) == 0);
+                key = keep_max ? (other > key ? other : key) : (other < key ? other : key);
+            }
+        const uint64_t bound = __shfl_sync(0xffffffffu, key, others - 1);
+        if (lane == 0) sm.warp_tau[tid >> 5] = bound;
+    }
     if (tid == 0) sm.count = 0;
     __syncthreads();
-    // 2. tau = the others-th largest per-thread maximum (others >= 1 here)
-    if (mine != 0) {
-        int rank = 0;
-        for (int u = 0; u < NT; ++u) rank += sm.thread_max[u] > mine;
-        if (rank == others - 1) sm.tau = mine;
-    }
-    __syncthreads();
-    const uint64_t tau = sm.tau;
+    uint64_t tau = 0;
+#pragma unroll
+    for (int w = 0; w < NT / 32; ++w) tau = sm.warp_tau[w] > tau ? sm.warp_tau[w] : tau;
     // 3. gather candidates >= tau
 #pragma unroll 8
     for (int j = tid; j < J; j += NT) {
-        uint64_t key = block_key(pooled[j], j);
+        const uint64_t key = block_key(staged ? sm.vals[j] : pooled[j], j);
         if (key >= tau) {
-            int slot = atomicAdd(&sm.count, 1);
+            const int slot = atomicAdd(&sm.count, 1);
             if (slot < kCandCap) sm.cand[slot] = key;
         }
     }
