@@ -99,13 +99,27 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
+// try_wait that may park the thread for up to `hint_ns` (woken when the phase
+// completes), so waiting warps do not take issue slots from working ones.
+__device__ __forceinline__ bool mbar_try_wait_hint(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n"
+        " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+        " selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
 // Wait for phase `parity` of `bar` to complete, giving up after kWaitLimitNs.
 // On time-out sets kErrWaitTimeout in *err (if given) and returns false.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* err) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait_hint(bar, parity, 1000000u)) return true;
         if (globaltimer_ns() - t0 > kWaitLimitNs) {
             if (err) atomicOr(err, kErrWaitTimeout);
             return false;
@@ -186,6 +200,17 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
     d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
     d |= 1ull << 46;  // descriptor version for tcgen05
     d |= 2ull << 61;  // SWIZZLE_128B
+    return d;
+}
+
+// Same with 64-byte swizzle (8 rows of 64 bytes per 512-byte atom).
+__device__ __forceinline__ uint64_t smem_desc_sw64(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+    d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+    d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+    d |= 1ull << 46;  // descriptor version for tcgen05
+    d |= 4ull << 61;  // SWIZZLE_64B
     return d;
 }
 

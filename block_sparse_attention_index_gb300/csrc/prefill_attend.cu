@@ -7,50 +7,82 @@
 // for all of them.  The row's selection is used as it stands (a tile never
 // attends to a block the row did not keep).
 //
-// Work item = (query row, KV head), 16 kept blocks = 8 pairs of 64 keys.  The
-// MMAs are transposed so that the 16 heads are the N dimension and the keys
-// (or head dims) the M = 128 dimension:
+// Work item = (query row, KV head), up to 16 kept blocks = 8 pairs of 64
+// keys.  The MMAs are transposed so that the 16 heads are the N dimension and
+// the keys (or head dims) the M = 128 dimension:
 //   S^T[128 keys, 16 heads]  = K_pair[128 keys, 128 dims] . Q^T        per pair
 //   O^T[128 dims, 32]       += V_pair^T[128 dims, 128 keys] . [P_hi; P_lo]^T
-// K and V pairs arrive by TMA (128-byte swizzle) in a 4-stage ring; V is read
-// as an MN-major operand straight from its [key][dim] tile.  All 8 pairs'
-// S^T (128 TMEM columns) are computed first, so the softmax is exact in one
-// pass (no running rescale): thread t of the four softmax warps owns key t
-// of every pair, reduces per-head maxima and sums across the CTA, and writes
-// P as bf16 hi and lo parts (N = 32: heads 0-15 hi, 16-31 lo) so the
-// weights keep ~16 significant bits.  The epilogue adds the two halves of
-// O^T, divides by the sums and stores out[row, h*G+g, :].
+// K and V pairs arrive by TMA (128-byte swizzle) in two 3-stage rings, each
+// fed by its own producer warp, so K pairs of the next items keep loading
+// while V pairs wait for the softmax of the current one; V is read
+// as an MN-major operand straight from its [key][dim] tile.  All pairs' S^T
+// (128 TMEM columns) are computed before the softmax, so it is exact with a
+// single max (no running rescale); P is written as bf16 hi and lo parts (N =
+// 32: heads 0-15 hi, 16-31 lo, ~16 significant bits) pair by pair into a
+// small ring that the PV MMAs drain.  P is stored key-major (one 64-byte row
+// per key, 64-byte swizzle), the MN-major form of the B operand, so a thread
+// writes its key's 32 values with four 16-byte stores.
 //
-// Warp roles: warps 0-3 softmax and epilogue, warp 4 TMA producer, warp 5
-// MMA issuer and tensor-memory owner.  Items are strided over a grid of one
-// CTA per SM.
+// Items overlap: S and O are double-buffered in tensor memory (2 x 128 + 2 x
+// 32 columns), so the tensor cores compute S of item i+1 while the softmax
+// warps work on item i, and the epilogue warps store item i while the
+// softmax warps start item i+1.  The MMA issue order is S(0), S(1), PV(0),
+// S(2), PV(1), ...; each producer loads its pairs in item order.
+//
+// Warp roles: 0-3 softmax, 4-7 epilogue (each group covers TMEM lanes
+// 0-127), 8 K producer, 9 V producer, 10 MMA issuer and tensor-memory owner.  Items are
+// strided over a grid of one CTA per SM.
 #include "common.cuh"
 #include "internal.h"
 
 namespace msa {
 
-constexpr int kPaThreads = 192;
-constexpr int kPaStages = 4;
+constexpr int kPaThreads = 352;
+constexpr int kKStages = 3;                       // K pairs ring (its own producer warp)
+constexpr int kVStages = 3;                       // V pairs ring (its own producer warp)
 constexpr int kPairBytes = 2 * 2 * 64 * 64 * 2;  // [dim half][2 blocks x 64 keys][64 dims] bf16 = 32 KB
 constexpr int kQBytes = 2 * 16 * 64 * 2;         // [dim half][16 heads][64 dims] = 4 KB
-constexpr int kPChunkBytes = 32 * 64 * 2;        // [32 rows: hi heads, lo heads][64 keys] = 4 KB
-constexpr int kTmemCols = 256;
-constexpr int kOCol = 128;                       // O^T columns [128, 160)
+constexpr int kPSlots = 2;
+constexpr int kPSlotBytes = 128 * 32 * 2;        // one pair: [128 keys][32 = 16 hi + 16 lo heads] bf16 = 8 KB
+constexpr int kTmemCols = 512;
+constexpr int kSCol = 0;                         // S^T buffers: columns [0,128) and [128,256)
+constexpr int kOCol = 256;                       // O^T buffers: columns [256,288) and [288,320)
+constexpr int kInfoSlots = 6;                    // decoded items published by the K producer
+constexpr int kInfoReaders = 1 + 1 + 4 + 4;      // V producer, MMA issuer, softmax warps, epilogue warps
+
+// One decoded work item, shared through shared memory so that only one
+// thread per CTA walks the sequence metadata and reads the selection.
+struct ItemInfo {
+    int32_t r, h, p, nsel, end;
+    int32_t pad;
+    int64_t start;
+    int32_t blk[kMaxTopK];
+};
 
 struct __align__(1024) AttendSmem {
-    uint8_t stage[kPaStages][kPairBytes];
-    uint8_t p[16][kPChunkBytes];                 // 16 chunks of 64 keys
+    uint8_t kst[kKStages][kPairBytes];
+    uint8_t vst[kVStages][kPairBytes];
+    uint8_t p[kPSlots][kPSlotBytes];
     uint8_t q[2][kQBytes];
-    uint64_t full[kPaStages];
-    uint64_t empty[kPaStages];
+    uint64_t kfull[kKStages];
+    uint64_t kempty[kKStages];
+    uint64_t vfull[kVStages];
+    uint64_t vempty[kVStages];
     uint64_t q_full[2];
     uint64_t q_empty[2];
-    uint64_t s_full;
-    uint64_t p_full;
-    uint64_t o_full;
+    uint64_t s_full[2];
+    uint64_t s_empty[2];
+    uint64_t p_full[kPSlots];
+    uint64_t p_empty[kPSlots];
+    uint64_t o_full[2];
+    uint64_t o_empty[2];
+    uint64_t rs_full[2];
+    uint64_t rs_empty[2];
+    uint64_t info_full[kInfoSlots];
+    uint64_t info_empty[kInfoSlots];
+    ItemInfo info[kInfoSlots];
     float red[4][16];
-    float rowmax[16];
-    float rowsum[16];
+    float rowsum[2][16];
     uint32_t tmem_base;
 };
 
@@ -105,6 +137,7 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+
 __global__ void __launch_bounds__(kPaThreads, 1) prefill_attend_kernel(const __grid_constant__ CUtensorMap q_map,
                                                                        const __grid_constant__ CUtensorMap k_map,
                                                                        const __grid_constant__ CUtensorMap v_map,
@@ -115,146 +148,234 @@ __global__ void __launch_bounds__(kPaThreads, 1) prefill_attend_kernel(const __g
     const int n_items = a.total_rows * a.H;
 
     if (tid == 0) {
-        for (int s = 0; s < kPaStages; ++s) {
-            mbar_init(&sm.full[s], 1);
-            mbar_init(&sm.empty[s], 1);
+        for (int s = 0; s < kKStages; ++s) {
+            mbar_init(&sm.kfull[s], 1);
+            mbar_init(&sm.kempty[s], 1);
+        }
+        for (int s = 0; s < kVStages; ++s) {
+            mbar_init(&sm.vfull[s], 1);
+            mbar_init(&sm.vempty[s], 1);
+        }
+        for (int s = 0; s < kPSlots; ++s) {
+            mbar_init(&sm.p_full[s], 4);  // one arrival per softmax warp
+            mbar_init(&sm.p_empty[s], 1);
         }
         for (int s = 0; s < 2; ++s) {
             mbar_init(&sm.q_full[s], 1);
             mbar_init(&sm.q_empty[s], 1);
+            mbar_init(&sm.s_full[s], 1);
+            mbar_init(&sm.s_empty[s], 4);
+            mbar_init(&sm.o_full[s], 1);
+            mbar_init(&sm.o_empty[s], 4);
+            mbar_init(&sm.rs_full[s], 4);
+            mbar_init(&sm.rs_empty[s], 4);
         }
-        mbar_init(&sm.s_full, 1);
-        mbar_init(&sm.p_full, 128);
-        mbar_init(&sm.o_full, 1);
+        for (int s = 0; s < kInfoSlots; ++s) {
+            mbar_init(&sm.info_full[s], 1);
+            mbar_init(&sm.info_empty[s], kInfoReaders);
+        }
         fence_mbar_init();
     }
-    if (warp == 5) tmem_alloc(&sm.tmem_base, kTmemCols);
+    if (warp == 10) tmem_alloc(&sm.tmem_base, kTmemCols);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = sm.tmem_base;
 
-    if (warp == 4) {
-        // ---------------- TMA producer
+    if (warp == 8) {
+        // ---------------- K producer: decodes the items, publishes them, loads Q(i)
+        // and the K pairs of S(i)
         if (lane == 0) {
             prefetch_tmap(&q_map);
             prefetch_tmap(&k_map);
-            prefetch_tmap(&v_map);
-            uint32_t g = 0, it = 0;
+            uint32_t g = 0, n = 0;
             bool alive = true;
             for (int item = blockIdx.x; alive && item < n_items; item += gridDim.x) {
                 Item x;
                 bool bad;
-                if (!load_item(a, item, x, bad)) continue;
-                const int qb = it & 1;
-                if (it >= 2 && !mbar_wait(&sm.q_empty[qb], ((it >> 1) - 1) & 1, a.err)) break;
+                if (!load_item(a, item, x, bad)) {
+                    if (bad) atomicOr(a.err, kErrBadMetadata);
+                    continue;
+                }
+                const int slot = n % kInfoSlots;
+                if (n >= kInfoSlots && !mbar_wait(&sm.info_empty[slot], ((n / kInfoSlots) - 1) & 1, a.err)) break;
+                ItemInfo& inf = sm.info[slot];
+                inf.r = x.r;
+                inf.h = x.h;
+                inf.p = x.p;
+                inf.nsel = x.nsel;
+                inf.start = x.start;
+                inf.end = 0;
+                for (int i = 0; i < kMaxTopK; ++i) inf.blk[i] = x.blk[i];
+                mbar_arrive(&sm.info_full[slot]);  // release: the fields above are visible
+                const int qb = n & 1;
+                if (n >= 2 && !mbar_wait(&sm.q_empty[qb], ((n >> 1) - 1) & 1, a.err)) break;
                 mbar_arrive_expect_tx(&sm.q_full[qb], kQBytes);
                 const int hq0 = x.h * a.G;
                 tma_load_3d(sm.q[qb], &q_map, &sm.q_full[qb], 0, hq0, x.r);
                 tma_load_3d(sm.q[qb] + kQBytes / 2, &q_map, &sm.q_full[qb], 64, hq0, x.r);
                 const int npairs = (x.nsel + 1) >> 1;
-                for (int pass = 0; pass < 2 && alive; ++pass) {
-                    const CUtensorMap* map = pass == 0 ? &k_map : &v_map;
-                    for (int q = 0; q < npairs; ++q, ++g) {
-                        const int s = g % kPaStages;
-                        if (g >= kPaStages && !mbar_wait(&sm.empty[s], ((g / kPaStages) - 1) & 1, a.err)) {
-                            alive = false;
-                            break;
-                        }
-                        mbar_arrive_expect_tx(&sm.full[s], kPairBytes);
-                        for (int half = 0; half < 2; ++half) {
-                            const int blk = x.blk[min(2 * q + half, x.nsel - 1)];
-                            const int tok = static_cast<int>(x.start + static_cast<int64_t>(blk) * kBlock);
-                            uint8_t* dst = sm.stage[s] + half * 8192;
-                            tma_load_3d(dst, map, &sm.full[s], 0, x.h, tok);
-                            tma_load_3d(dst + 16384, map, &sm.full[s], 64, x.h, tok);
-                        }
+                for (int q = 0; q < npairs; ++q, ++g) {
+                    const int s = g % kKStages;
+                    if (g >= static_cast<uint32_t>(kKStages) &&
+                        !mbar_wait(&sm.kempty[s], ((g / kKStages) - 1) & 1, a.err)) {
+                        alive = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&sm.kfull[s], kPairBytes);
+                    for (int half = 0; half < 2; ++half) {
+                        const int blk = x.blk[min(2 * q + half, x.nsel - 1)];
+                        const int tok = static_cast<int>(x.start + static_cast<int64_t>(blk) * kBlock);
+                        tma_load_3d(sm.kst[s] + half * 8192, &k_map, &sm.kfull[s], 0, x.h, tok);
+                        tma_load_3d(sm.kst[s] + half * 8192 + 16384, &k_map, &sm.kfull[s], 64, x.h, tok);
                     }
                 }
-                ++it;
+                ++n;
+            }
+            // end marker (also after an abandoned loop, so that every reader stops)
+            const int slot = n % kInfoSlots;
+            if (n < kInfoSlots || mbar_wait(&sm.info_empty[slot], ((n / kInfoSlots) - 1) & 1, a.err)) {
+                sm.info[slot].end = 1;
+                mbar_arrive(&sm.info_full[slot]);
             }
         }
-    } else if (warp == 5) {
-        // ---------------- MMA issuer
+    } else if (warp == 9) {
+        // ---------------- V producer: the V pairs of PV(i), in item order
+        if (lane == 0) {
+            prefetch_tmap(&v_map);
+            uint32_t g = 0;
+            for (uint32_t n = 0;; ++n) {
+                const int slot = n % kInfoSlots;
+                if (!mbar_wait(&sm.info_full[slot], (n / kInfoSlots) & 1, a.err)) break;
+                const ItemInfo& inf = sm.info[slot];
+                if (inf.end) break;
+                const int npairs = (inf.nsel + 1) >> 1;
+                bool alive = true;
+                for (int q = 0; q < npairs; ++q, ++g) {
+                    const int s = g % kVStages;
+                    if (g >= static_cast<uint32_t>(kVStages) &&
+                        !mbar_wait(&sm.vempty[s], ((g / kVStages) - 1) & 1, a.err)) {
+                        alive = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&sm.vfull[s], kPairBytes);
+                    for (int half = 0; half < 2; ++half) {
+                        const int blk = inf.blk[min(2 * q + half, inf.nsel - 1)];
+                        const int tok = static_cast<int>(inf.start + static_cast<int64_t>(blk) * kBlock);
+                        tma_load_3d(sm.vst[s] + half * 8192, &v_map, &sm.vfull[s], 0, inf.h, tok);
+                        tma_load_3d(sm.vst[s] + half * 8192 + 16384, &v_map, &sm.vfull[s], 64, inf.h, tok);
+                    }
+                }
+                mbar_arrive(&sm.info_empty[slot]);
+                if (!alive) break;
+            }
+        }
+    } else if (warp == 10) {
+        // ---------------- MMA issuer: S(0), S(1), PV(0), S(2), PV(1), ...
         if (lane == 0) {
             constexpr uint32_t idesc_s = idesc_bf16_f32(128, 16, 0, 0);
-            constexpr uint32_t idesc_o = idesc_bf16_f32(128, 32, 1, 0);
-            uint32_t g = 0, it = 0;
+            constexpr uint32_t idesc_o = idesc_bf16_f32(128, 32, 1, 1);
+            uint32_t gk = 0, gv = 0, pc = 0;
             bool alive = true;
-            for (int item = blockIdx.x; alive && item < n_items; item += gridDim.x) {
-                Item x;
-                bool bad;
-                if (!load_item(a, item, x, bad)) continue;
-                const int qb = it & 1;
-                const int npairs = (x.nsel + 1) >> 1;
-                if (!mbar_wait(&sm.q_full[qb], (it >> 1) & 1, a.err)) break;
-                const uint32_t q_addr = smem_u32(sm.q[qb]);
-                for (int q = 0; q < npairs; ++q, ++g) {  // S^T per pair
-                    const int s = g % kPaStages;
-                    if (!mbar_wait(&sm.full[s], (g / kPaStages) & 1, a.err)) { alive = false; break; }
+            int prev_pairs = -1;
+            auto issue_pv = [&](int npairs, uint32_t j) {  // O(j) += V^T P^T over item j's pairs
+                const int ob = j & 1;
+                if (j >= 2 && !mbar_wait(&sm.o_empty[ob], ((j >> 1) - 1) & 1, a.err)) { alive = false; return; }
+                for (int q = 0; q < npairs; ++q, ++gv, ++pc) {
+                    const int s = gv % kVStages, ps = pc % kPSlots;
+                    if (!mbar_wait(&sm.vfull[s], (gv / kVStages) & 1, a.err) ||
+                        !mbar_wait(&sm.p_full[ps], (pc / kPSlots) & 1, a.err)) {
+                        alive = false;
+                        return;
+                    }
                     tc_fence_after();
-                    const uint32_t k_addr = smem_u32(sm.stage[s]);
+                    const uint32_t v_addr = smem_u32(sm.vst[s]);
+                    const uint32_t p_addr = smem_u32(sm.p[ps]);
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {  // 16 keys per step
+                        const uint64_t ad = smem_desc_sw128(v_addr + kk * 2048, 16384, 1024);
+                        const uint64_t bd = smem_desc_sw64(p_addr + kk * 1024, 8192, 512);
+                        tc_mma_ss(tmem + kOCol + ob * 32, ad, bd, idesc_o, (q > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    tc_commit(&sm.vempty[s]);
+                    tc_commit(&sm.p_empty[ps]);
+                }
+                tc_commit(&sm.o_full[ob]);
+            };
+            uint32_t n = 0;
+            for (;; ++n) {
+                const int slot = n % kInfoSlots;
+                if (!mbar_wait(&sm.info_full[slot], (n / kInfoSlots) & 1, a.err)) { alive = false; break; }
+                if (sm.info[slot].end) break;
+                const int npairs = (sm.info[slot].nsel + 1) >> 1;
+                mbar_arrive(&sm.info_empty[slot]);
+                const int qb = n & 1, sb = n & 1;
+                if (!mbar_wait(&sm.q_full[qb], (n >> 1) & 1, a.err)) { alive = false; break; }
+                if (n >= 2 && !mbar_wait(&sm.s_empty[sb], ((n >> 1) - 1) & 1, a.err)) { alive = false; break; }
+                const uint32_t q_addr = smem_u32(sm.q[qb]);
+                for (int q = 0; q < npairs; ++q, ++gk) {  // S^T(n) per pair
+                    const int s = gk % kKStages;
+                    if (!mbar_wait(&sm.kfull[s], (gk / kKStages) & 1, a.err)) { alive = false; break; }
+                    tc_fence_after();
+                    const uint32_t k_addr = smem_u32(sm.kst[s]);
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk) {
                         const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
                         const uint64_t ad = smem_desc_sw128(k_addr + off, 16, 1024);
-                        const uint64_t bd = smem_desc_sw128(q_addr + (kk >> 2) * (kQBytes / 2) + (kk & 3) * 32, 16, 1024);
-                        tc_mma_ss(tmem + q * 16, ad, bd, idesc_s, kk > 0);
+                        const uint64_t bd =
+                            smem_desc_sw128(q_addr + (kk >> 2) * (kQBytes / 2) + (kk & 3) * 32, 16, 1024);
+                        tc_mma_ss(tmem + kSCol + sb * 128 + q * 16, ad, bd, idesc_s, kk > 0);
                     }
-                    tc_commit(&sm.empty[s]);
+                    tc_commit(&sm.kempty[s]);
                 }
                 if (!alive) break;
                 tc_commit(&sm.q_empty[qb]);
-                tc_commit(&sm.s_full);
-                if (!mbar_wait(&sm.p_full, it & 1, a.err)) break;
-                tc_fence_after();
-                for (int q = 0; q < npairs; ++q, ++g) {  // O^T += V^T P^T per pair
-                    const int s = g % kPaStages;
-                    if (!mbar_wait(&sm.full[s], (g / kPaStages) & 1, a.err)) { alive = false; break; }
-                    tc_fence_after();
-                    const uint32_t v_addr = smem_u32(sm.stage[s]);
-#pragma unroll
-                    for (int kk = 0; kk < 8; ++kk) {  // 16 keys per step
-                        const uint64_t ad = smem_desc_sw128(v_addr + kk * 2048, 16384, 1024);
-                        const int chunk = 2 * q + (kk >> 2);
-                        const uint64_t bd = smem_desc_sw128(smem_u32(sm.p[chunk]) + (kk & 3) * 32, 16, 1024);
-                        tc_mma_ss(tmem + kOCol, ad, bd, idesc_o, (q > 0 || kk > 0) ? 1u : 0u);
-                    }
-                    tc_commit(&sm.empty[s]);
+                tc_commit(&sm.s_full[sb]);
+                if (prev_pairs >= 0) {
+                    issue_pv(prev_pairs, n - 1);
+                    if (!alive) break;
                 }
-                if (!alive) break;
-                tc_commit(&sm.o_full);
-                ++it;
+                prev_pairs = npairs;
             }
+            if (alive && prev_pairs >= 0) issue_pv(prev_pairs, n - 1);
         }
-    } else {
-        // ---------------- softmax + epilogue (128 threads; thread = TMEM lane)
+    } else if (warp < 4) {
+        // ---------------- softmax (128 threads; thread = TMEM lane = key of a pair)
         const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
         const int key_in_blk = tid & 63, half = tid >> 6;
-        uint32_t it = 0;
-        for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
-            Item x;
-            bool bad;
-            if (!load_item(a, item, x, bad)) {
-                if (bad && tid == 0) atomicOr(a.err, kErrBadMetadata);
-                continue;
+        uint32_t pc = 0;
+        for (uint32_t n = 0;; ++n) {
+            const int slot = n % kInfoSlots;
+            if (!mbar_wait(&sm.info_full[slot], (n / kInfoSlots) & 1, a.err)) break;
+            const ItemInfo& inf = sm.info[slot];
+            if (inf.end) break;
+            const int nsel = inf.nsel, pos = inf.p;
+            const int npairs = (nsel + 1) >> 1;
+            // key validity per pair: the pair's block on this thread's half exists and t <= p
+            uint32_t valid_mask = 0;
+            for (int q = 0; q < npairs; ++q) {
+                const int idx = 2 * q + half;
+                if (idx < nsel && inf.blk[idx] * kBlock + key_in_blk <= pos) valid_mask |= 1u << q;
             }
-            const int npairs = (x.nsel + 1) >> 1;
-            if (!mbar_wait(&sm.s_full, it & 1, a.err)) break;
+            const int sb = n & 1;
+            if (!mbar_wait(&sm.s_full[sb], (n >> 1) & 1, a.err)) break;
             tc_fence_after();
+            const uint32_t s_addr = lane_addr + kSCol + sb * 128;
             // pass 1: per-head maxima of the raw scores over valid keys
             float mx[16];
 #pragma unroll
             for (int g = 0; g < 16; ++g) mx[g] = -INFINITY;
-            for (int q = 0; q < npairs; ++q) {
-                uint32_t v[16];
-                tmem_ld16(lane_addr + q * 16, v);
-                tmem_ld_wait();
-                const int idx = 2 * q + half;
-                const bool valid = idx < x.nsel && x.blk[idx] * kBlock + key_in_blk <= x.p;
-                if (valid) {
+            for (int q0 = 0; q0 < npairs; q0 += 4) {  // four pairs per TMEM round trip
+                uint32_t v[4][16];
 #pragma unroll
-                    for (int g = 0; g < 16; ++g) mx[g] = fmaxf(mx[g], __uint_as_float(v[g]));
+                for (int k = 0; k < 4; ++k) tmem_ld16(s_addr + (q0 + k) * 16, v[k]);
+                tmem_ld_wait();
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    if (valid_mask & (1u << (q0 + k))) {
+#pragma unroll
+                        for (int g = 0; g < 16; ++g) mx[g] = fmaxf(mx[g], __uint_as_float(v[k][g]));
+                    }
                 }
             }
 #pragma unroll
@@ -273,31 +394,57 @@ __global__ void __launch_bounds__(kPaThreads, 1) prefill_attend_kernel(const __g
 #pragma unroll
             for (int g = 0; g < 16; ++g)
                 ms[g] = fmaxf(fmaxf(sm.red[0][g], sm.red[1][g]), fmaxf(sm.red[2][g], sm.red[3][g])) * a.scale_log2;
-            named_sync_softmax();
-            // pass 2: P = 2^(s*scale*log2e - max), hi/lo bf16 parts, sums
+            named_sync_softmax();  // everyone has its maxima before red is reused
+            // pass 2: P = 2^(s*scale*log2e - max) as bf16 hi + lo, pair by pair
             float sum[16];
 #pragma unroll
             for (int g = 0; g < 16; ++g) sum[g] = 0.f;
-            for (int q = 0; q < npairs; ++q) {
-                uint32_t v[16];
-                tmem_ld16(lane_addr + q * 16, v);
-                tmem_ld_wait();
-                const int idx = 2 * q + half;
-                const bool valid = idx < x.nsel && x.blk[idx] * kBlock + key_in_blk <= x.p;
-                uint8_t* chunk = sm.p[2 * q + half];
-                const int ch = key_in_blk >> 3, within = (key_in_blk & 7) * 2;
+            bool alive2 = true;
+            for (int q0 = 0; q0 < npairs && alive2; q0 += 4) {  // four pairs per TMEM round trip
+                uint32_t vv[4][16];
 #pragma unroll
-                for (int g = 0; g < 16; ++g) {
-                    const float pr = valid ? exp2f(fmaf(__uint_as_float(v[g]), a.scale_log2, -ms[g])) : 0.f;
-                    sum[g] += pr;
-                    const __nv_bfloat16 hi_b = __float2bfloat16_rn(pr);
-                    const __nv_bfloat16 lo_b = __float2bfloat16_rn(pr - __bfloat162float(hi_b));
-                    const uint32_t sw = static_cast<uint32_t>((ch ^ (g & 7)) << 4) + within;
-                    *reinterpret_cast<__nv_bfloat16*>(chunk + g * 128 + sw) = hi_b;
-                    *reinterpret_cast<__nv_bfloat16*>(chunk + (16 + g) * 128 + sw) = lo_b;
+                for (int k = 0; k < 4; ++k) tmem_ld16(s_addr + (q0 + k) * 16, vv[k]);
+                tmem_ld_wait();
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int q = q0 + k;
+                    if (q >= npairs) break;
+                    const int ps = pc % kPSlots;
+                    if (pc >= kPSlots && !mbar_wait(&sm.p_empty[ps], ((pc / kPSlots) - 1) & 1, a.err)) {
+                        alive2 = false;
+                        break;
+                    }
+                    const uint32_t* v = vv[k];
+                    const bool valid = (valid_mask >> q) & 1u;
+                    uint32_t hi[8], lo[8];
+#pragma unroll
+                    for (int g2 = 0; g2 < 8; ++g2) {
+                        const float p0 =
+                            valid ? exp2f(fmaf(__uint_as_float(v[2 * g2]), a.scale_log2, -ms[2 * g2])) : 0.f;
+                        const float p1 =
+                            valid ? exp2f(fmaf(__uint_as_float(v[2 * g2 + 1]), a.scale_log2, -ms[2 * g2 + 1])) : 0.f;
+                        sum[2 * g2] += p0;
+                        sum[2 * g2 + 1] += p1;
+                        hi[g2] = pack_bf16x2(p0, p1);
+                        lo[g2] = pack_bf16x2(p0 - bf16_lo(hi[g2]), p1 - bf16_hi(hi[g2]));
+                    }
+                    // row tid of the slot: 4 chunks of 16 bytes (hi 0-7, hi 8-15, lo 0-7,
+                    // lo 8-15), chunk c at position c ^ ((row >> 1) & 3)
+                    uint8_t* row = sm.p[ps] + tid * 64;
+                    const int sw = (tid >> 1) & 3;
+                    *reinterpret_cast<uint4*>(row + ((0 ^ sw) << 4)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                    *reinterpret_cast<uint4*>(row + ((1 ^ sw) << 4)) = make_uint4(hi[4], hi[5], hi[6], hi[7]);
+                    *reinterpret_cast<uint4*>(row + ((2 ^ sw) << 4)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                    *reinterpret_cast<uint4*>(row + ((3 ^ sw) << 4)) = make_uint4(lo[4], lo[5], lo[6], lo[7]);
+                    fence_proxy_async_smem();  // P is read by the tensor cores
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&sm.p_full[ps]);
+                    ++pc;
                 }
             }
-            fence_proxy_async_smem();  // P is read by the tensor cores
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.s_empty[sb]);  // S(n) fully read
 #pragma unroll
             for (int g = 0; g < 16; ++g) {
 #pragma unroll
@@ -310,33 +457,61 @@ __global__ void __launch_bounds__(kPaThreads, 1) prefill_attend_kernel(const __g
                 sm.red[warp][lane] = m;
             }
             named_sync_softmax();
-            if (tid < 16) sm.rowsum[tid] = sm.red[0][tid] + sm.red[1][tid] + sm.red[2][tid] + sm.red[3][tid];
-            tc_fence_before();
-            mbar_arrive(&sm.p_full);
-            // epilogue: out[r, h*G + g, d] = (O_hi + O_lo)[d, g] / sum[g]
-            if (!mbar_wait(&sm.o_full, it & 1, a.err)) break;
+            if (n >= 2) mbar_wait(&sm.rs_empty[sb], ((n >> 1) - 1) & 1, a.err);
+            if (tid < 16) sm.rowsum[sb][tid] = sm.red[0][tid] + sm.red[1][tid] + sm.red[2][tid] + sm.red[3][tid];
+            named_sync_softmax();  // red is free again; rowsum written
+            if (lane == 0) {
+                mbar_arrive(&sm.rs_full[sb]);
+                mbar_arrive(&sm.info_empty[slot]);
+            }
+            if (!alive2) break;
+        }
+    } else {
+        // ---------------- epilogue (warps 4-7; thread = TMEM lane = output dim)
+        const int quarter = warp - 4;
+        const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+        const int d = quarter * 32 + lane;
+        for (uint32_t n = 0;; ++n) {
+            const int slot = n % kInfoSlots;
+            if (!mbar_wait(&sm.info_full[slot], (n / kInfoSlots) & 1, a.err)) break;
+            if (sm.info[slot].end) break;
+            const int r = sm.info[slot].r, h = sm.info[slot].h;
+            const int ob = n & 1;
+            if (!mbar_wait(&sm.o_full[ob], (n >> 1) & 1, a.err)) break;
             tc_fence_after();
             uint32_t ohi[16], olo[16];
-            tmem_ld16(lane_addr + kOCol, ohi);
-            tmem_ld16(lane_addr + kOCol + 16, olo);
+            tmem_ld16(lane_addr + kOCol + ob * 32, ohi);
+            tmem_ld16(lane_addr + kOCol + ob * 32 + 16, olo);
             tmem_ld_wait();
-            named_sync_softmax();  // rowsum visible
-            const int d = tid;
-            const int64_t base = (static_cast<int64_t>(x.r) * a.H * a.G + static_cast<int64_t>(x.h) * a.G) * kHeadDim + d;
-            for (int g = 0; g < a.G; ++g) {
-                const float o = (__uint_as_float(ohi[g]) + __uint_as_float(olo[g])) / sm.rowsum[g];
-                if (a.out_bf16)
-                    reinterpret_cast<__nv_bfloat16*>(a.out)[base + static_cast<int64_t>(g) * kHeadDim] = __float2bfloat16_rn(o);
-                else
-                    reinterpret_cast<float*>(a.out)[base + static_cast<int64_t>(g) * kHeadDim] = o;
-            }
             tc_fence_before();
-            ++it;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.o_empty[ob]);
+            if (!mbar_wait(&sm.rs_full[ob], (n >> 1) & 1, a.err)) break;
+            float inv[16];
+#pragma unroll
+            for (int g = 0; g < 16; ++g) inv[g] = 1.f / sm.rowsum[ob][g];
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&sm.rs_empty[ob]);
+                mbar_arrive(&sm.info_empty[slot]);
+            }
+            const int64_t base = (static_cast<int64_t>(r) * a.H * a.G + static_cast<int64_t>(h) * a.G) * kHeadDim + d;
+#pragma unroll
+            for (int g = 0; g < 16; ++g) {
+                if (g < a.G) {
+                    const float o = (__uint_as_float(ohi[g]) + __uint_as_float(olo[g])) * inv[g];
+                    if (a.out_bf16)
+                        reinterpret_cast<__nv_bfloat16*>(a.out)[base + static_cast<int64_t>(g) * kHeadDim] =
+                            __float2bfloat16_rn(o);
+                    else
+                        reinterpret_cast<float*>(a.out)[base + static_cast<int64_t>(g) * kHeadDim] = o;
+                }
+            }
         }
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 5) {
+    if (warp == 10) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
