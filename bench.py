@@ -153,6 +153,26 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+# ---------------------------------------------------------------- ranks
+
+def max_over_ranks(value: float, device=None) -> float:
+    """The largest `value` over all ranks of the default process group (the
+    value itself when no group is initialised).  `device`: where the
+    reduction tensor lives (a CUDA device for NCCL, None/CPU for gloo)."""
+    import torch
+    import torch.distributed as td
+    if not (td.is_available() and td.is_initialized()) or td.get_world_size() == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device if device is not None else "cpu")
+    td.all_reduce(t, op=td.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank: int, world_size: int, ms_per_step: float) -> float:
+    """Units all ranks processed per second, timed by the slowest rank."""
+    return units_per_rank * world_size / (ms_per_step * 1e-3)
+
+
 # ---------------------------------------------------------------- the GPU arm
 
 def _dist():
@@ -258,11 +278,7 @@ def measure_gpu(w, steps, warmup, dev, dist_on, flush_bytes=512 << 20, e2e_steps
             step(marks)
         marks[4].synchronize()
         stage_ms.append([marks[j].elapsed_time(marks[j + 1]) for j in range(4)])
-    total_ms = float(sum(step_ms))
-    if dist_on:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        td.all_reduce(t, op=td.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(float(sum(step_ms)), dev if dist_on else None)
     res = dict(ms_per_step=total_ms / steps, stage_ms=np.mean(np.array(stage_ms), axis=0).tolist(),
                wall_s=wall, clocks=clk.summary(), launches=pb.forward_launches() * steps,
                graph=graph is not None)
@@ -389,7 +405,7 @@ def main():
     res = measure_gpu(w, args.steps, args.warmup, dev, dist_on, with_e2e=not args.no_e2e,
                       use_graph=not args.no_graph)
     rows = w.total_rows
-    value = rows * ws / (res["ms_per_step"] * 1e-3)
+    value = whole_job_rate(rows, ws, res["ms_per_step"])
     line = {"metric": _metric_for(w), "value": round(value, 1), "unit": "rows/s", "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(res["ms_per_step"], 5), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
@@ -409,7 +425,8 @@ def main():
     if step_bytes and wc["pre_rows"] == 0:
         line["step_hbm_frac"] = round(step_bytes / (res["ms_per_step"] * 1e-3) / 1e9 / hbm, 4)
     if "e2e_ms" in res:
-        line["e2e"] = {"value": round(rows * ws / (res["e2e_ms"] * 1e-3), 1), "unit": "rows/s",
+        line["e2e"] = {"value": round(whole_job_rate(rows, ws, max_over_ranks(res["e2e_ms"], dev if dist_on else None)), 1),
+                       "unit": "rows/s",
                        "h2d_bytes_per_step": res["h2d"], "d2h_bytes_per_step": res["d2h"],
                        "note": "every step copies q, iq and the k, v, ik caches from pinned host memory and reads "
                                "the output back"}
@@ -418,7 +435,7 @@ def main():
         res2 = measure_gpu(w2, max(3, args.steps // 2), args.warmup, dev, dist_on, with_e2e=False,
                            use_graph=not args.no_graph)
         line["secondary"] = {"metric": _metric_for(w2), "workload": w2.name,
-                             "value": round(w2.total_rows * ws / (res2["ms_per_step"] * 1e-3), 1), "unit": "rows/s",
+                             "value": round(whole_job_rate(w2.total_rows, ws, res2["ms_per_step"]), 1), "unit": "rows/s",
                              "ms_per_step": round(res2["ms_per_step"], 5),
                              "stage_us": {"prefill_index": round(res2["stage_ms"][2] * 1e3, 2),
                                           "prefill_attend": round(res2["stage_ms"][3] * 1e3, 2)},
