@@ -29,15 +29,16 @@
 // softmax warps start item i+1.  The MMA issue order is S(0), S(1), PV(0),
 // S(2), PV(1), ...; each producer loads its pairs in item order.
 //
-// Warp roles: 0-3 softmax, 4-7 epilogue (each group covers TMEM lanes
-// 0-127), 8 K producer, 9 V producer, 10 MMA issuer and tensor-memory owner.  Items are
+// Warp roles: 0-7 softmax (warps w and w+4 share TMEM lane quarter w and
+// take heads 0-7 and 8-15), 8-11 epilogue, 12 K producer, 13 V producer,
+// 14 MMA issuer and tensor-memory owner.  Items are
 // strided over a grid of one CTA per SM.
 #include "common.cuh"
 #include "internal.h"
 
 namespace msa {
 
-constexpr int kPaThreads = 352;
+constexpr int kPaThreads = 480;
 constexpr int kKStages = 3;                       // K pairs ring (its own producer warp)
 constexpr int kVStages = 3;                       // V pairs ring (its own producer warp)
 constexpr int kPairBytes = 2 * 2 * 64 * 64 * 2;  // [dim half][2 blocks x 64 keys][64 dims] bf16 = 32 KB
@@ -48,7 +49,7 @@ constexpr int kTmemCols = 512;
 constexpr int kSCol = 0;                         // S^T buffers: columns [0,128) and [128,256)
 constexpr int kOCol = 256;                       // O^T buffers: columns [256,288) and [288,320)
 constexpr int kInfoSlots = 6;                    // decoded items published by the K producer
-constexpr int kInfoReaders = 1 + 1 + 4 + 4;      // V producer, MMA issuer, softmax warps, epilogue warps
+constexpr int kInfoReaders = 1 + 1 + 8 + 4;      // V producer, MMA issuer, softmax warps, epilogue warps
 
 // One decoded work item, shared through shared memory so that only one
 // thread per CTA walks the sequence metadata and reads the selection.
@@ -85,6 +86,8 @@ struct __align__(1024) AttendSmem {
     float rowsum[2][16];
     uint32_t tmem_base;
 };
+
+static_assert(sizeof(AttendSmem) + 1024 <= 227 * 1024, "prompt-chunk attention exceeds 227 KB of shared memory");
 
 struct Item {
     int r, h, p, nsel;
@@ -131,7 +134,7 @@ __device__ bool load_item(const PrefillAttendArgs& a, int it, Item& x, bool& bad
     return true;
 }
 
-__device__ __forceinline__ void named_sync_softmax() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+__device__ __forceinline__ void named_sync_softmax() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -157,17 +160,17 @@ __global__ void __launch_bounds__(kPaThreads, 1) prefill_attend_kernel(const __g
             mbar_init(&sm.vempty[s], 1);
         }
         for (int s = 0; s < kPSlots; ++s) {
-            mbar_init(&sm.p_full[s], 4);  // one arrival per softmax warp
+            mbar_init(&sm.p_full[s], 8);  // one arrival per softmax warp
             mbar_init(&sm.p_empty[s], 1);
         }
         for (int s = 0; s < 2; ++s) {
             mbar_init(&sm.q_full[s], 1);
             mbar_init(&sm.q_empty[s], 1);
             mbar_init(&sm.s_full[s], 1);
-            mbar_init(&sm.s_empty[s], 4);
+            mbar_init(&sm.s_empty[s], 8);
             mbar_init(&sm.o_full[s], 1);
             mbar_init(&sm.o_empty[s], 4);
-            mbar_init(&sm.rs_full[s], 4);
+            mbar_init(&sm.rs_full[s], 8);
             mbar_init(&sm.rs_empty[s], 4);
         }
         for (int s = 0; s < kInfoSlots; ++s) {
@@ -176,13 +179,13 @@ __global__ void __launch_bounds__(kPaThreads, 1) prefill_attend_kernel(const __g
         }
         fence_mbar_init();
     }
-    if (warp == 10) tmem_alloc(&sm.tmem_base, kTmemCols);
+    if (warp == 14) tmem_alloc(&sm.tmem_base, kTmemCols);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = sm.tmem_base;
 
-    if (warp == 8) {
+    if (warp == 12) {
         // ---------------- K producer: decodes the items, publishes them, loads Q(i)
         // and the K pairs of S(i)
         if (lane == 0) {
@@ -239,7 +242,7 @@ __global__ void __launch_bounds__(kPaThreads, 1) prefill_attend_kernel(const __g
                 mbar_arrive(&sm.info_full[slot]);
             }
         }
-    } else if (warp == 9) {
+    } else if (warp == 13) {
         // ---------------- V producer: the V pairs of PV(i), in item order
         if (lane == 0) {
             prefetch_tmap(&v_map);
@@ -270,7 +273,7 @@ __global__ void __launch_bounds__(kPaThreads, 1) prefill_attend_kernel(const __g
                 if (!alive) break;
             }
         }
-    } else if (warp == 10) {
+    } else if (warp == 14) {
         // ---------------- MMA issuer: S(0), S(1), PV(0), S(2), PV(1), ...
         if (lane == 0) {
             constexpr uint32_t idesc_s = idesc_bf16_f32(128, 16, 0, 0);
@@ -278,9 +281,21 @@ __global__ void __launch_bounds__(kPaThreads, 1) prefill_attend_kernel(const __g
             uint32_t gk = 0, gv = 0, pc = 0;
             bool alive = true;
             int prev_pairs = -1;
+            // Descriptor bases, built once: the start-address field counts 16-byte
+            // units in the low bits, so a k-step adds (byte offset >> 4).
+            uint64_t kdesc[kKStages], vdesc[kVStages], qdesc[2], pdesc[kPSlots];
+#pragma unroll
+            for (int i = 0; i < kKStages; ++i) kdesc[i] = smem_desc_sw128(smem_u32(sm.kst[i]), 16, 1024);
+#pragma unroll
+            for (int i = 0; i < kVStages; ++i) vdesc[i] = smem_desc_sw128(smem_u32(sm.vst[i]), 16384, 1024);
+#pragma unroll
+            for (int i = 0; i < 2; ++i) qdesc[i] = smem_desc_sw128(smem_u32(sm.q[i]), 16, 1024);
+#pragma unroll
+            for (int i = 0; i < kPSlots; ++i) pdesc[i] = smem_desc_sw64(smem_u32(sm.p[i]), 8192, 512);
             auto issue_pv = [&](int npairs, uint32_t j) {  // O(j) += V^T P^T over item j's pairs
                 const int ob = j & 1;
                 if (j >= 2 && !mbar_wait(&sm.o_empty[ob], ((j >> 1) - 1) & 1, a.err)) { alive = false; return; }
+                const uint32_t d_tmem = tmem + kOCol + ob * 32;
                 for (int q = 0; q < npairs; ++q, ++gv, ++pc) {
                     const int s = gv % kVStages, ps = pc % kPSlots;
                     if (!mbar_wait(&sm.vfull[s], (gv / kVStages) & 1, a.err) ||
@@ -289,14 +304,11 @@ __global__ void __launch_bounds__(kPaThreads, 1) prefill_attend_kernel(const __g
                         return;
                     }
                     tc_fence_after();
-                    const uint32_t v_addr = smem_u32(sm.vst[s]);
-                    const uint32_t p_addr = smem_u32(sm.p[ps]);
+                    const uint64_t vb = vdesc[s], pb = pdesc[ps];
 #pragma unroll
-                    for (int kk = 0; kk < 8; ++kk) {  // 16 keys per step
-                        const uint64_t ad = smem_desc_sw128(v_addr + kk * 2048, 16384, 1024);
-                        const uint64_t bd = smem_desc_sw64(p_addr + kk * 1024, 8192, 512);
-                        tc_mma_ss(tmem + kOCol + ob * 32, ad, bd, idesc_o, (q > 0 || kk > 0) ? 1u : 0u);
-                    }
+                    for (int kk = 0; kk < 8; ++kk)  // 16 keys per step: V rows +2 KB, P rows +1 KB
+                        tc_mma_ss(d_tmem, vb + static_cast<uint64_t>(kk * 2048 >> 4), pb + static_cast<uint64_t>(kk * 1024 >> 4),
+                                  idesc_o, (q > 0 || kk > 0) ? 1u : 0u);
                     tc_commit(&sm.vempty[s]);
                     tc_commit(&sm.p_empty[ps]);
                 }
@@ -312,19 +324,19 @@ __global__ void __launch_bounds__(kPaThreads, 1) prefill_attend_kernel(const __g
                 const int qb = n & 1, sb = n & 1;
                 if (!mbar_wait(&sm.q_full[qb], (n >> 1) & 1, a.err)) { alive = false; break; }
                 if (n >= 2 && !mbar_wait(&sm.s_empty[sb], ((n >> 1) - 1) & 1, a.err)) { alive = false; break; }
-                const uint32_t q_addr = smem_u32(sm.q[qb]);
+                const uint64_t qb_desc = qdesc[qb];
                 for (int q = 0; q < npairs; ++q, ++gk) {  // S^T(n) per pair
                     const int s = gk % kKStages;
                     if (!mbar_wait(&sm.kfull[s], (gk / kKStages) & 1, a.err)) { alive = false; break; }
                     tc_fence_after();
-                    const uint32_t k_addr = smem_u32(sm.kst[s]);
+                    const uint64_t kb = kdesc[s];
+                    const uint32_t d_tmem = tmem + kSCol + sb * 128 + q * 16;
 #pragma unroll
-                    for (int kk = 0; kk < 8; ++kk) {
-                        const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-                        const uint64_t ad = smem_desc_sw128(k_addr + off, 16, 1024);
-                        const uint64_t bd =
-                            smem_desc_sw128(q_addr + (kk >> 2) * (kQBytes / 2) + (kk & 3) * 32, 16, 1024);
-                        tc_mma_ss(tmem + kSCol + sb * 128 + q * 16, ad, bd, idesc_s, kk > 0);
+                    for (int kk = 0; kk < 8; ++kk) {  // 16 dims per step
+                        const uint32_t koff = (kk >> 2) * 16384 + (kk & 3) * 32;
+                        const uint32_t qoff = (kk >> 2) * (kQBytes / 2) + (kk & 3) * 32;
+                        tc_mma_ss(d_tmem, kb + static_cast<uint64_t>(koff >> 4), qb_desc + static_cast<uint64_t>(qoff >> 4),
+                                  idesc_s, kk > 0);
                     }
                     tc_commit(&sm.kempty[s]);
                 }
@@ -339,10 +351,13 @@ __global__ void __launch_bounds__(kPaThreads, 1) prefill_attend_kernel(const __g
             }
             if (alive && prev_pairs >= 0) issue_pv(prev_pairs, n - 1);
         }
-    } else if (warp < 4) {
-        // ---------------- softmax (128 threads; thread = TMEM lane = key of a pair)
-        const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-        const int key_in_blk = tid & 63, half = tid >> 6;
+    } else if (warp < 8) {
+        // ---------------- softmax (256 threads; row = TMEM lane = key of a pair; warp
+        // w takes lane quarter w & 3 and heads 8 * (w >> 2) .. + 7)
+        const int quarter = warp & 3, hh = warp >> 2;
+        const int row = quarter * 32 + lane;
+        const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+        const int key_in_blk = row & 63, half = row >> 6;
         uint32_t pc = 0;
         for (uint32_t n = 0;; ++n) {
             const int slot = n % kInfoSlots;
@@ -351,7 +366,7 @@ __global__ void __launch_bounds__(kPaThreads, 1) prefill_attend_kernel(const __g
             if (inf.end) break;
             const int nsel = inf.nsel, pos = inf.p;
             const int npairs = (nsel + 1) >> 1;
-            // key validity per pair: the pair's block on this thread's half exists and t <= p
+            // key validity per pair: the pair's block on this row's half exists and t <= p
             uint32_t valid_mask = 0;
             for (int q = 0; q < npairs; ++q) {
                 const int idx = 2 * q + half;
@@ -360,50 +375,52 @@ __global__ void __launch_bounds__(kPaThreads, 1) prefill_attend_kernel(const __g
             const int sb = n & 1;
             if (!mbar_wait(&sm.s_full[sb], (n >> 1) & 1, a.err)) break;
             tc_fence_after();
-            const uint32_t s_addr = lane_addr + kSCol + sb * 128;
+            const uint32_t s_addr = lane_addr + kSCol + sb * 128 + hh * 8;
             // pass 1: per-head maxima of the raw scores over valid keys
-            float mx[16];
+            float mx[8];
 #pragma unroll
-            for (int g = 0; g < 16; ++g) mx[g] = -INFINITY;
+            for (int g = 0; g < 8; ++g) mx[g] = -INFINITY;
             for (int q0 = 0; q0 < npairs; q0 += 4) {  // four pairs per TMEM round trip
-                uint32_t v[4][16];
+                uint32_t v[4][8];
 #pragma unroll
-                for (int k = 0; k < 4; ++k) tmem_ld16(s_addr + (q0 + k) * 16, v[k]);
+                for (int k = 0; k < 4; ++k) tmem_ld8(s_addr + (q0 + k) * 16, v[k]);
                 tmem_ld_wait();
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
                     if (valid_mask & (1u << (q0 + k))) {
 #pragma unroll
-                        for (int g = 0; g < 16; ++g) mx[g] = fmaxf(mx[g], __uint_as_float(v[k][g]));
+                        for (int g = 0; g < 8; ++g) mx[g] = fmaxf(mx[g], __uint_as_float(v[k][g]));
                     }
                 }
             }
 #pragma unroll
-            for (int g = 0; g < 16; ++g) {
+            for (int g = 0; g < 8; ++g) {
 #pragma unroll
                 for (int o = 16; o > 0; o >>= 1) mx[g] = fmaxf(mx[g], __shfl_xor_sync(0xffffffffu, mx[g], o));
             }
-            if (lane < 16) {
+            if (lane < 8) {
                 float m = mx[0];
 #pragma unroll
-                for (int g = 1; g < 16; ++g) m = lane == g ? mx[g] : m;
-                sm.red[warp][lane] = m;
+                for (int g = 1; g < 8; ++g) m = lane == g ? mx[g] : m;
+                sm.red[quarter][hh * 8 + lane] = m;
             }
             named_sync_softmax();
-            float ms[16];
+            float ms[8];
 #pragma unroll
-            for (int g = 0; g < 16; ++g)
-                ms[g] = fmaxf(fmaxf(sm.red[0][g], sm.red[1][g]), fmaxf(sm.red[2][g], sm.red[3][g])) * a.scale_log2;
+            for (int g = 0; g < 8; ++g) {
+                const int hg = hh * 8 + g;
+                ms[g] = fmaxf(fmaxf(sm.red[0][hg], sm.red[1][hg]), fmaxf(sm.red[2][hg], sm.red[3][hg])) * a.scale_log2;
+            }
             named_sync_softmax();  // everyone has its maxima before red is reused
             // pass 2: P = 2^(s*scale*log2e - max) as bf16 hi + lo, pair by pair
-            float sum[16];
+            float sum[8];
 #pragma unroll
-            for (int g = 0; g < 16; ++g) sum[g] = 0.f;
+            for (int g = 0; g < 8; ++g) sum[g] = 0.f;
             bool alive2 = true;
             for (int q0 = 0; q0 < npairs && alive2; q0 += 4) {  // four pairs per TMEM round trip
-                uint32_t vv[4][16];
+                uint32_t vv[4][8];
 #pragma unroll
-                for (int k = 0; k < 4; ++k) tmem_ld16(s_addr + (q0 + k) * 16, vv[k]);
+                for (int k = 0; k < 4; ++k) tmem_ld8(s_addr + (q0 + k) * 16, vv[k]);
                 tmem_ld_wait();
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
@@ -414,28 +431,26 @@ __global__ void __launch_bounds__(kPaThreads, 1) prefill_attend_kernel(const __g
                         alive2 = false;
                         break;
                     }
-                    const uint32_t* v = vv[k];
                     const bool valid = (valid_mask >> q) & 1u;
-                    uint32_t hi[8], lo[8];
+                    uint32_t hi[4], lo[4];
 #pragma unroll
-                    for (int g2 = 0; g2 < 8; ++g2) {
+                    for (int g2 = 0; g2 < 4; ++g2) {
                         const float p0 =
-                            valid ? exp2f(fmaf(__uint_as_float(v[2 * g2]), a.scale_log2, -ms[2 * g2])) : 0.f;
+                            valid ? exp2f(fmaf(__uint_as_float(vv[k][2 * g2]), a.scale_log2, -ms[2 * g2])) : 0.f;
                         const float p1 =
-                            valid ? exp2f(fmaf(__uint_as_float(v[2 * g2 + 1]), a.scale_log2, -ms[2 * g2 + 1])) : 0.f;
+                            valid ? exp2f(fmaf(__uint_as_float(vv[k][2 * g2 + 1]), a.scale_log2, -ms[2 * g2 + 1])) : 0.f;
                         sum[2 * g2] += p0;
                         sum[2 * g2 + 1] += p1;
                         hi[g2] = pack_bf16x2(p0, p1);
                         lo[g2] = pack_bf16x2(p0 - bf16_lo(hi[g2]), p1 - bf16_hi(hi[g2]));
                     }
-                    // row tid of the slot: 4 chunks of 16 bytes (hi 0-7, hi 8-15, lo 0-7,
-                    // lo 8-15), chunk c at position c ^ ((row >> 1) & 3)
-                    uint8_t* row = sm.p[ps] + tid * 64;
-                    const int sw = (tid >> 1) & 3;
-                    *reinterpret_cast<uint4*>(row + ((0 ^ sw) << 4)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-                    *reinterpret_cast<uint4*>(row + ((1 ^ sw) << 4)) = make_uint4(hi[4], hi[5], hi[6], hi[7]);
-                    *reinterpret_cast<uint4*>(row + ((2 ^ sw) << 4)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-                    *reinterpret_cast<uint4*>(row + ((3 ^ sw) << 4)) = make_uint4(lo[4], lo[5], lo[6], lo[7]);
+                    // row `row` of the slot: 4 chunks of 16 bytes (hi 0-7, hi 8-15, lo 0-7,
+                    // lo 8-15), chunk c at position c ^ ((row >> 1) & 3); this warp writes
+                    // chunks hh (hi) and 2 + hh (lo)
+                    uint8_t* rp = sm.p[ps] + row * 64;
+                    const int sw = (row >> 1) & 3;
+                    *reinterpret_cast<uint4*>(rp + ((hh ^ sw) << 4)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                    *reinterpret_cast<uint4*>(rp + (((2 + hh) ^ sw) << 4)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
                     fence_proxy_async_smem();  // P is read by the tensor cores
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&sm.p_full[ps]);
@@ -446,15 +461,15 @@ __global__ void __launch_bounds__(kPaThreads, 1) prefill_attend_kernel(const __g
             __syncwarp();
             if (lane == 0) mbar_arrive(&sm.s_empty[sb]);  // S(n) fully read
 #pragma unroll
-            for (int g = 0; g < 16; ++g) {
+            for (int g = 0; g < 8; ++g) {
 #pragma unroll
                 for (int o = 16; o > 0; o >>= 1) sum[g] += __shfl_xor_sync(0xffffffffu, sum[g], o);
             }
-            if (lane < 16) {
+            if (lane < 8) {
                 float m = sum[0];
 #pragma unroll
-                for (int g = 1; g < 16; ++g) m = lane == g ? sum[g] : m;
-                sm.red[warp][lane] = m;
+                for (int g = 1; g < 8; ++g) m = lane == g ? sum[g] : m;
+                sm.red[quarter][hh * 8 + lane] = m;
             }
             named_sync_softmax();
             if (n >= 2) mbar_wait(&sm.rs_empty[sb], ((n >> 1) - 1) & 1, a.err);
@@ -468,7 +483,7 @@ __global__ void __launch_bounds__(kPaThreads, 1) prefill_attend_kernel(const __g
         }
     } else {
         // ---------------- epilogue (warps 4-7; thread = TMEM lane = output dim)
-        const int quarter = warp - 4;
+        const int quarter = warp - 8;
         const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
         const int d = quarter * 32 + lane;
         for (uint32_t n = 0;; ++n) {
@@ -511,7 +526,7 @@ __global__ void __launch_bounds__(kPaThreads, 1) prefill_attend_kernel(const __g
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 10) {
+    if (warp == 14) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
