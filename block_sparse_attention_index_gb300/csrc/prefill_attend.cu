@@ -14,42 +14,47 @@
 //   O^T[128 dims, 32]       += V_pair^T[128 dims, 128 keys] . [P_hi; P_lo]^T
 // K and V pairs arrive by TMA (128-byte swizzle) in two 3-stage rings, each
 // fed by its own producer warp, so K pairs of the next items keep loading
-// while V pairs wait for the softmax of the current one; V is read
-// as an MN-major operand straight from its [key][dim] tile.  All pairs' S^T
+// while V pairs wait for the softmax of the current one; V is read as an
+// MN-major operand straight from its [key][dim] tile.  Slot i of the V ring
+// and slot i of the P ring belong to the same PV pair and share one barrier
+// (the V bytes plus one arrival per softmax warp), so the PV issuer tests one
+// barrier per pair: on these small-N MMAs each barrier test costs the issuing
+// thread a few hundred cycles, about as long as the pair's eight MMAs.  All pairs' S^T
 // (128 TMEM columns) are computed before the softmax, so it is exact with a
 // single max (no running rescale); P is written as bf16 hi and lo parts (N =
 // 32: heads 0-15 hi, 16-31 lo, ~16 significant bits) pair by pair into a
-// small ring that the PV MMAs drain.  P is stored key-major (one 64-byte row
+// small ring (three slots) that the PV MMAs drain.  P is stored key-major (one 64-byte row
 // per key, 64-byte swizzle), the MN-major form of the B operand, so a thread
 // writes its key's 32 values with four 16-byte stores.
 //
 // Items overlap: S and O are double-buffered in tensor memory (2 x 128 + 2 x
 // 32 columns), so the tensor cores compute S of item i+1 while the softmax
 // warps work on item i, and the epilogue warps store item i while the
-// softmax warps start item i+1.  The MMA issue order is S(0), S(1), PV(0),
-// S(2), PV(1), ...; each producer loads its pairs in item order.
+// softmax warps start item i+1.  S and PV MMAs are issued by two threads of
+// their own (tcgen05.commit tracks each thread's MMAs separately), so the
+// tensor pipe runs one's MMAs while the other waits on a barrier; each
+// producer loads its pairs in item order.
 //
 // Warp roles: 0-7 softmax (warps w and w+4 share TMEM lane quarter w and
 // take heads 0-7 and 8-15), 8-11 epilogue, 12 K producer, 13 V producer,
-// 14 MMA issuer and tensor-memory owner.  Items are
-// strided over a grid of one CTA per SM.
+// 14 S issuer and tensor-memory owner, 15 PV issuer.  Items are strided over
+// a grid of one CTA per SM.
 #include "common.cuh"
 #include "internal.h"
 
 namespace msa {
 
-constexpr int kPaThreads = 480;
+constexpr int kPaThreads = 512;
 constexpr int kKStages = 3;                       // K pairs ring (its own producer warp)
-constexpr int kVStages = 3;                       // V pairs ring (its own producer warp)
+constexpr int kPvStages = 3;                      // V pairs + P pairs ring: slot i holds both operands of one PV pair
 constexpr int kPairBytes = 2 * 2 * 64 * 64 * 2;  // [dim half][2 blocks x 64 keys][64 dims] bf16 = 32 KB
 constexpr int kQBytes = 2 * 16 * 64 * 2;         // [dim half][16 heads][64 dims] = 4 KB
-constexpr int kPSlots = 2;
 constexpr int kPSlotBytes = 128 * 32 * 2;        // one pair: [128 keys][32 = 16 hi + 16 lo heads] bf16 = 8 KB
 constexpr int kTmemCols = 512;
 constexpr int kSCol = 0;                         // S^T buffers: columns [0,128) and [128,256)
 constexpr int kOCol = 256;                       // O^T buffers: columns [256,288) and [288,320)
 constexpr int kInfoSlots = 6;                    // decoded items published by the K producer
-constexpr int kInfoReaders = 1 + 1 + 8 + 4;      // V producer, MMA issuer, softmax warps, epilogue warps
+constexpr int kInfoReaders = 1 + 2 + 8 + 4;      // V producer, S and PV issuers, softmax warps, epilogue warps
 
 // One decoded work item, shared through shared memory so that only one
 // thread per CTA walks the sequence metadata and reads the selection.
@@ -62,19 +67,17 @@ struct ItemInfo {
 
 struct __align__(1024) AttendSmem {
     uint8_t kst[kKStages][kPairBytes];
-    uint8_t vst[kVStages][kPairBytes];
-    uint8_t p[kPSlots][kPSlotBytes];
+    uint8_t vst[kPvStages][kPairBytes];
+    uint8_t p[kPvStages][kPSlotBytes];
     uint8_t q[2][kQBytes];
     uint64_t kfull[kKStages];
     uint64_t kempty[kKStages];
-    uint64_t vfull[kVStages];
-    uint64_t vempty[kVStages];
+    uint64_t pv_full[kPvStages];   // V pair landed and the 8 softmax warps wrote P
+    uint64_t pv_empty[kPvStages];  // PV pair done: V and P slot free
     uint64_t q_full[2];
     uint64_t q_empty[2];
     uint64_t s_full[2];
     uint64_t s_empty[2];
-    uint64_t p_full[kPSlots];
-    uint64_t p_empty[kPSlots];
     uint64_t o_full[2];
     uint64_t o_empty[2];
     uint64_t rs_full[2];
@@ -155,13 +158,9 @@ __global__ void __launch_bounds__(kPaThreads, 1) prefill_attend_kernel(const __g
             mbar_init(&sm.kfull[s], 1);
             mbar_init(&sm.kempty[s], 1);
         }
-        for (int s = 0; s < kVStages; ++s) {
-            mbar_init(&sm.vfull[s], 1);
-            mbar_init(&sm.vempty[s], 1);
-        }
-        for (int s = 0; s < kPSlots; ++s) {
-            mbar_init(&sm.p_full[s], 8);  // one arrival per softmax warp
-            mbar_init(&sm.p_empty[s], 1);
+        for (int s = 0; s < kPvStages; ++s) {
+            mbar_init(&sm.pv_full[s], 1 + 8);  // V producer (with the pair's bytes) + one arrival per softmax warp
+            mbar_init(&sm.pv_empty[s], 1);
         }
         for (int s = 0; s < 2; ++s) {
             mbar_init(&sm.q_full[s], 1);
@@ -255,18 +254,18 @@ __global__ void __launch_bounds__(kPaThreads, 1) prefill_attend_kernel(const __g
                 const int npairs = (inf.nsel + 1) >> 1;
                 bool alive = true;
                 for (int q = 0; q < npairs; ++q, ++g) {
-                    const int s = g % kVStages;
-                    if (g >= static_cast<uint32_t>(kVStages) &&
-                        !mbar_wait(&sm.vempty[s], ((g / kVStages) - 1) & 1, a.err)) {
+                    const int s = g % kPvStages;
+                    if (g >= static_cast<uint32_t>(kPvStages) &&
+                        !mbar_wait(&sm.pv_empty[s], ((g / kPvStages) - 1) & 1, a.err)) {
                         alive = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(&sm.vfull[s], kPairBytes);
+                    mbar_arrive_expect_tx(&sm.pv_full[s], kPairBytes);
                     for (int half = 0; half < 2; ++half) {
                         const int blk = inf.blk[min(2 * q + half, inf.nsel - 1)];
                         const int tok = static_cast<int>(inf.start + static_cast<int64_t>(blk) * kBlock);
-                        tma_load_3d(sm.vst[s] + half * 8192, &v_map, &sm.vfull[s], 0, inf.h, tok);
-                        tma_load_3d(sm.vst[s] + half * 8192 + 16384, &v_map, &sm.vfull[s], 64, inf.h, tok);
+                        tma_load_3d(sm.vst[s] + half * 8192, &v_map, &sm.pv_full[s], 0, inf.h, tok);
+                        tma_load_3d(sm.vst[s] + half * 8192 + 16384, &v_map, &sm.pv_full[s], 64, inf.h, tok);
                     }
                 }
                 mbar_arrive(&sm.info_empty[slot]);
@@ -274,60 +273,31 @@ __global__ void __launch_bounds__(kPaThreads, 1) prefill_attend_kernel(const __g
             }
         }
     } else if (warp == 14) {
-        // ---------------- MMA issuer: S(0), S(1), PV(0), S(2), PV(1), ...
+        // ---------------- S issuer (tensor-memory owner): S^T(i) = K_pair . Q^T per pair
         if (lane == 0) {
             constexpr uint32_t idesc_s = idesc_bf16_f32(128, 16, 0, 0);
-            constexpr uint32_t idesc_o = idesc_bf16_f32(128, 32, 1, 1);
-            uint32_t gk = 0, gv = 0, pc = 0;
-            bool alive = true;
-            int prev_pairs = -1;
             // Descriptor bases, built once: the start-address field counts 16-byte
             // units in the low bits, so a k-step adds (byte offset >> 4).
-            uint64_t kdesc[kKStages], vdesc[kVStages], qdesc[2], pdesc[kPSlots];
+            uint64_t kdesc[kKStages], qdesc[2];
 #pragma unroll
             for (int i = 0; i < kKStages; ++i) kdesc[i] = smem_desc_sw128(smem_u32(sm.kst[i]), 16, 1024);
 #pragma unroll
-            for (int i = 0; i < kVStages; ++i) vdesc[i] = smem_desc_sw128(smem_u32(sm.vst[i]), 16384, 1024);
-#pragma unroll
             for (int i = 0; i < 2; ++i) qdesc[i] = smem_desc_sw128(smem_u32(sm.q[i]), 16, 1024);
-#pragma unroll
-            for (int i = 0; i < kPSlots; ++i) pdesc[i] = smem_desc_sw64(smem_u32(sm.p[i]), 8192, 512);
-            auto issue_pv = [&](int npairs, uint32_t j) {  // O(j) += V^T P^T over item j's pairs
-                const int ob = j & 1;
-                if (j >= 2 && !mbar_wait(&sm.o_empty[ob], ((j >> 1) - 1) & 1, a.err)) { alive = false; return; }
-                const uint32_t d_tmem = tmem + kOCol + ob * 32;
-                for (int q = 0; q < npairs; ++q, ++gv, ++pc) {
-                    const int s = gv % kVStages, ps = pc % kPSlots;
-                    if (!mbar_wait(&sm.vfull[s], (gv / kVStages) & 1, a.err) ||
-                        !mbar_wait(&sm.p_full[ps], (pc / kPSlots) & 1, a.err)) {
-                        alive = false;
-                        return;
-                    }
-                    tc_fence_after();
-                    const uint64_t vb = vdesc[s], pb = pdesc[ps];
-#pragma unroll
-                    for (int kk = 0; kk < 8; ++kk)  // 16 keys per step: V rows +2 KB, P rows +1 KB
-                        tc_mma_ss(d_tmem, vb + static_cast<uint64_t>(kk * 2048 >> 4), pb + static_cast<uint64_t>(kk * 1024 >> 4),
-                                  idesc_o, (q > 0 || kk > 0) ? 1u : 0u);
-                    tc_commit(&sm.vempty[s]);
-                    tc_commit(&sm.p_empty[ps]);
-                }
-                tc_commit(&sm.o_full[ob]);
-            };
-            uint32_t n = 0;
-            for (;; ++n) {
+            uint32_t g = 0;
+            for (uint32_t n = 0;; ++n) {
                 const int slot = n % kInfoSlots;
-                if (!mbar_wait(&sm.info_full[slot], (n / kInfoSlots) & 1, a.err)) { alive = false; break; }
+                if (!mbar_wait(&sm.info_full[slot], (n / kInfoSlots) & 1, a.err)) break;
                 if (sm.info[slot].end) break;
                 const int npairs = (sm.info[slot].nsel + 1) >> 1;
                 mbar_arrive(&sm.info_empty[slot]);
                 const int qb = n & 1, sb = n & 1;
-                if (!mbar_wait(&sm.q_full[qb], (n >> 1) & 1, a.err)) { alive = false; break; }
-                if (n >= 2 && !mbar_wait(&sm.s_empty[sb], ((n >> 1) - 1) & 1, a.err)) { alive = false; break; }
+                if (!mbar_wait(&sm.q_full[qb], (n >> 1) & 1, a.err)) break;
+                if (n >= 2 && !mbar_wait(&sm.s_empty[sb], ((n >> 1) - 1) & 1, a.err)) break;
                 const uint64_t qb_desc = qdesc[qb];
-                for (int q = 0; q < npairs; ++q, ++gk) {  // S^T(n) per pair
-                    const int s = gk % kKStages;
-                    if (!mbar_wait(&sm.kfull[s], (gk / kKStages) & 1, a.err)) { alive = false; break; }
+                bool alive = true;
+                for (int q = 0; q < npairs; ++q, ++g) {
+                    const int s = g % kKStages;
+                    if (!mbar_wait(&sm.kfull[s], (g / kKStages) & 1, a.err)) { alive = false; break; }
                     tc_fence_after();
                     const uint64_t kb = kdesc[s];
                     const uint32_t d_tmem = tmem + kSCol + sb * 128 + q * 16;
@@ -343,13 +313,45 @@ __global__ void __launch_bounds__(kPaThreads, 1) prefill_attend_kernel(const __g
                 if (!alive) break;
                 tc_commit(&sm.q_empty[qb]);
                 tc_commit(&sm.s_full[sb]);
-                if (prev_pairs >= 0) {
-                    issue_pv(prev_pairs, n - 1);
-                    if (!alive) break;
-                }
-                prev_pairs = npairs;
             }
-            if (alive && prev_pairs >= 0) issue_pv(prev_pairs, n - 1);
+        }
+    } else if (warp == 15) {
+        // ---------------- PV issuer: O^T(i) += V_pair^T . [P_hi; P_lo]^T per pair.  A
+        // second issuing thread, so that its barrier waits and those of the S
+        // issuer overlap each other's MMAs.
+        if (lane == 0) {
+            constexpr uint32_t idesc_o = idesc_bf16_f32(128, 32, 1, 1);
+            uint64_t vdesc[kPvStages], pdesc[kPvStages];
+#pragma unroll
+            for (int i = 0; i < kPvStages; ++i) {
+                vdesc[i] = smem_desc_sw128(smem_u32(sm.vst[i]), 16384, 1024);
+                pdesc[i] = smem_desc_sw64(smem_u32(sm.p[i]), 8192, 512);
+            }
+            uint32_t g = 0;
+            for (uint32_t n = 0;; ++n) {
+                const int slot = n % kInfoSlots;
+                if (!mbar_wait(&sm.info_full[slot], (n / kInfoSlots) & 1, a.err)) break;
+                if (sm.info[slot].end) break;
+                const int npairs = (sm.info[slot].nsel + 1) >> 1;
+                mbar_arrive(&sm.info_empty[slot]);
+                const int ob = n & 1;
+                if (n >= 2 && !mbar_wait(&sm.o_empty[ob], ((n >> 1) - 1) & 1, a.err)) break;
+                const uint32_t d_tmem = tmem + kOCol + ob * 32;
+                bool alive = true;
+                for (int q = 0; q < npairs; ++q, ++g) {
+                    const int s = g % kPvStages;
+                    if (!mbar_wait(&sm.pv_full[s], (g / kPvStages) & 1, a.err)) { alive = false; break; }
+                    tc_fence_after();
+                    const uint64_t vb = vdesc[s], pb = pdesc[s];
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk)  // 16 keys per step: V rows +2 KB, P rows +1 KB
+                        tc_mma_ss(d_tmem, vb + static_cast<uint64_t>(kk * 2048 >> 4), pb + static_cast<uint64_t>(kk * 1024 >> 4),
+                                  idesc_o, (q > 0 || kk > 0) ? 1u : 0u);
+                    tc_commit(&sm.pv_empty[s]);
+                }
+                if (!alive) break;
+                tc_commit(&sm.o_full[ob]);
+            }
         }
     } else if (warp < 8) {
         // ---------------- softmax (256 threads; row = TMEM lane = key of a pair; warp
@@ -426,8 +428,8 @@ __global__ void __launch_bounds__(kPaThreads, 1) prefill_attend_kernel(const __g
                 for (int k = 0; k < 4; ++k) {
                     const int q = q0 + k;
                     if (q >= npairs) break;
-                    const int ps = pc % kPSlots;
-                    if (pc >= kPSlots && !mbar_wait(&sm.p_empty[ps], ((pc / kPSlots) - 1) & 1, a.err)) {
+                    const int ps = pc % kPvStages;
+                    if (pc >= kPvStages && !mbar_wait(&sm.pv_empty[ps], ((pc / kPvStages) - 1) & 1, a.err)) {
                         alive2 = false;
                         break;
                     }
@@ -453,7 +455,7 @@ __global__ void __launch_bounds__(kPaThreads, 1) prefill_attend_kernel(const __g
                     *reinterpret_cast<uint4*>(rp + (((2 + hh) ^ sw) << 4)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
                     fence_proxy_async_smem();  // P is read by the tensor cores
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(&sm.p_full[ps]);
+                    if (lane == 0) mbar_arrive(&sm.pv_full[ps]);
                     ++pc;
                 }
             }
