@@ -345,8 +345,10 @@ def roofline_for(w, res, hbm, bf16, bf16_sus, peak_kind):
                 "peak_source": f"{peak_kind} hbm_gbs (copy)"}
     if stage[3] > 0:
         achieved = wc["att_flops"] / (stage[3] * 1e-3) / 1e12
+        traffic = (ncu_traffic("prefill_attend_4096_at_8192.md", ["prefill_attend.cu", "common.cuh"])
+                   if w.name == "prefill_4096_at_8192" else None)
         return {"kernel": "prefill_attend_kernel", "bound": "tensor", "achieved": round(achieved, 1), "peak": bf16,
-                "unit": "TFLOP/s", "frac": round(achieved / bf16, 4), "traffic": None,
+                "unit": "TFLOP/s", "frac": round(achieved / bf16, 4), "traffic": traffic,
                 "algorithmic_flops": wc["att_flops"], "kernel_us": round(stage[3] * 1e3, 2),
                 "peak_source": f"{peak_kind} bf16_tflops (burst)"}
     return None

@@ -97,8 +97,7 @@ Layout layout_of(const msa_problem* p) {
     off = align256(off);
     l.pooled = off;
     off = align256(off + B * H * MB * sizeof(float));
-    l.partials = off;
-    off = align256(off + B * H * K * msa::kPartialFloats * sizeof(float));
+    l.partials = off;  // none: decode partials are combined on chip (thread-block clusters)
     l.sel = off;
     off = align256(off + R * H * K * sizeof(int32_t));
     l.nsel = off;
@@ -313,7 +312,7 @@ static msa::DecodeAttendArgs decode_args(const msa_problem* p, const CUtensorMap
     a.scale_log2 = scale_log2(p);
     a.out = out;
     a.out_bf16 = p->out_dtype == MSA_OUT_BF16;
-    a.partials = reinterpret_cast<float*>(ws + l.partials);
+    a.partials = nullptr;  // the cluster kernel keeps its partials in distributed shared memory
     a.tickets = reinterpret_cast<int32_t*>(ws + l.tickets);
     a.err = reinterpret_cast<uint32_t*>(ws + l.err);
     return a;

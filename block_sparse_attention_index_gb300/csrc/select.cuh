@@ -9,8 +9,10 @@
 //
 // Each candidate j is a distinct 64-bit key (ordered score, ~j), so the
 // result does not depend on thread order:
-//   1. every thread takes the largest key among its strided candidates
-//      (the scores are staged in shared memory on the way when they fit);
+//   1. every thread takes the largest key among its strided candidates; the
+//      scores are read kChunk per thread at a time, all loads issued before
+//      any use, and kept in registers when J <= kChunk x NT (otherwise staged
+//      in shared memory on the way when they fit);
 //   2. every warp sorts its 32 per-thread maxima (bitonic, shuffles) and
 //      takes the k-th largest: that is a lower bound of the k-th largest key
 //      overall (k distinct candidates reach it); tau = the largest bound;
@@ -25,6 +27,7 @@
 namespace msa {
 
 constexpr int kCandCap = 512;
+constexpr int kChunk = 8;  // pooled scores per thread and load round
 constexpr int kSelStage = 4096;  // pooled scores staged in shared memory up to this many blocks
 
 template <int NT>
@@ -60,7 +63,8 @@ __device__ __forceinline__ uint64_t cta_argmax_below(const float* pooled, int J,
     return r;
 }
 
-// Selects from pooled[0..J) (+ the local block J).  All NT threads call it.
+// Selects from pooled[0..J) (+ the local block J).  All NT threads call it;
+// pooled may point to global or shared memory (generic loads only).
 // Writes the kept blocks ascending to sel[0..top_k) (-1 padded; sel may be
 // shared or global memory, written by threads < top_k) and returns nsel.
 template <int NT>
@@ -72,15 +76,28 @@ __device__ int cta_select(const float* pooled, int J, int top_k, int* sel, Selec
         __syncthreads();
         return J + 1;
     }
-    // 1. per-thread maxima (and the scores staged in shared memory)
-    const bool staged = J <= kSelStage;
+    // 1. per-thread maxima; the first round's scores stay in registers
+    const bool in_regs = J <= kChunk * NT;
+    const bool staged = !in_regs && J <= kSelStage;
     uint64_t mine = 0;
-#pragma unroll 8
-    for (int j = tid; j < J; j += NT) {
-        const float v = pooled[j];
-        if (staged) sm.vals[j] = v;
-        const uint64_t key = block_key(v, j);
-        mine = key > mine ? key : mine;
+    float v0[kChunk];
+    for (int base = 0; base < J; base += kChunk * NT) {
+        float v[kChunk];
+#pragma unroll
+        for (int i = 0; i < kChunk; ++i) {  // independent loads, all in flight together
+            const int j = base + i * NT + tid;
+            v[i] = j < J ? pooled[j] : 0.f;  // generic load: pooled may be shared memory
+        }
+#pragma unroll
+        for (int i = 0; i < kChunk; ++i) {
+            const int j = base + i * NT + tid;
+            if (j < J) {
+                if (staged) sm.vals[j] = v[i];
+                const uint64_t key = block_key(v[i], j);
+                mine = key > mine ? key : mine;
+            }
+            if (base == 0) v0[i] = v[i];
+        }
     }
     // 2. per-warp bound: sort the 32 maxima descending, take the others-th;
     // warp 0 always holds min(J, 32) >= others candidates, so tau > 0
@@ -104,12 +121,23 @@ __device__ int cta_select(const float* pooled, int J, int top_k, int* sel, Selec
 #pragma unroll
     for (int w = 0; w < NT / 32; ++w) tau = sm.warp_tau[w] > tau ? sm.warp_tau[w] : tau;
     // 3. gather candidates >= tau
-#pragma unroll 8
-    for (int j = tid; j < J; j += NT) {
-        const uint64_t key = block_key(staged ? sm.vals[j] : pooled[j], j);
-        if (key >= tau) {
-            const int slot = atomicAdd(&sm.count, 1);
-            if (slot < kCandCap) sm.cand[slot] = key;
+    if (in_regs) {
+#pragma unroll
+        for (int i = 0; i < kChunk; ++i) {
+            const int j = i * NT + tid;
+            const uint64_t key = j < J ? block_key(v0[i], j) : 0;
+            if (key >= tau) {
+                const int slot = atomicAdd(&sm.count, 1);
+                if (slot < kCandCap) sm.cand[slot] = key;
+            }
+        }
+    } else {
+        for (int j = tid; j < J; j += NT) {
+            const uint64_t key = block_key(staged ? sm.vals[j] : pooled[j], j);
+            if (key >= tau) {
+                const int slot = atomicAdd(&sm.count, 1);
+                if (slot < kCandCap) sm.cand[slot] = key;
+            }
         }
     }
     __syncthreads();

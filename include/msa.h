@@ -137,9 +137,10 @@ msa_status msa_select_blocks(const msa_problem* p, const float* scores, int64_t 
                              int32_t* sel, int32_t* nsel, void* stream);
 
 /* Stage 3, decode form: every sequence has exactly one row
- * (max_rows_per_seq == 1).  Each kept block is one split whose partial
- * softmax state (running max, sum, unnormalised output) is combined by
- * log-sum-exp in the last split to finish.  sel/nsel as msa_select_blocks
+ * (max_rows_per_seq == 1).  The kept blocks of one (sequence, KV head) are
+ * split over a cluster of 8 CTAs (two blocks each); their partial softmax
+ * states (running max, sum, unnormalised output) are combined by
+ * log-sum-exp on chip, through distributed shared memory.  sel/nsel as msa_select_blocks
  * writes them (entries must be causal blocks <= J, ascending, distinct).
  * Needs msa_workspace_size bytes of workspace. */
 msa_status msa_attend_decode(const msa_problem* p, const void* q, const void* k_cache,
