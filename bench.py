@@ -20,6 +20,7 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
+import platform
 import os
 import re
 import subprocess
@@ -193,15 +194,24 @@ def _pinned(a):
 
 
 def measure_gpu(w, steps, warmup, dev, dist_on, flush_bytes=512 << 20, e2e_steps=3, with_e2e=True,
-                use_graph=True):
+                use_graph=True, page_size=0):
     import torch
     import torch.distributed as td
 
     import block_sparse_attention_index_gb300 as msa
 
     x = synth.make_inputs(w)
-    dx = {k: _to_dev(x[k], dev) for k in ("q", "iq", "k", "v", "ik")}
-    pb = msa.Problem(w.H, w.G, w.seqs, dev, top_k=w.top_k, scale=w.softmax_scale)
+    if page_size:  # the same caches as a shuffled page pool with a block table
+        pl = synth.paged_layout(w, x, page_size, seed=page_size)
+        dx = {k: _to_dev(x[k], dev) for k in ("q", "iq")}
+        dx.update({k: _to_dev(pl[k], dev) for k in ("k", "v", "ik")})
+        pb = msa.Problem(w.H, w.G, w.seqs, dev, top_k=w.top_k, scale=w.softmax_scale,
+                         block_table=torch.from_numpy(pl["table"]), page_size=page_size,
+                         cache_tokens=pl["num_pages"] * page_size)
+        with_e2e = False
+    else:
+        dx = {k: _to_dev(x[k], dev) for k in ("q", "iq", "k", "v", "ik")}
+        pb = msa.Problem(w.H, w.G, w.seqs, dev, top_k=w.top_k, scale=w.softmax_scale)
     ws = pb.workspace()
     out = pb.new_out()
     sel, nsel = pb.new_sel()
@@ -338,18 +348,42 @@ def measure_gpu(w, steps, warmup, dev, dist_on, flush_bytes=512 << 20, e2e_steps
     return res
 
 
-def cpu_baseline(w, rows_sample, reps=1):
+_ORACLE_INPUTS = {}
+
+
+def cpu_baseline(w, rows_sample, reps=1, single_thread=True):
     import oracle
-    x = synth.make_inputs(w)
-    pr = oracle.Problem.from_workload(w, x)
+    if w.name not in _ORACLE_INPUTS:  # draw the workload once per process
+        x = synth.make_inputs(w)
+        _ORACLE_INPUTS[w.name] = (x, oracle.Problem.from_workload(w, x))
+    x, pr = _ORACLE_INPUTS[w.name]
     threads = oracle.num_threads()
     t0 = time.perf_counter()
     for _ in range(reps):
         oracle.forward(pr, x, rows=rows_sample, threads=threads)
     dt = time.perf_counter() - t0
-    return dict(value=len(rows_sample) * reps / dt, unit="rows/s", cores=threads, kind="oracle",
-                sample=f"{len(rows_sample)} of {w.total_rows} rows of {w.name}, {reps} rep(s), fp64 C oracle, "
-                       f"{threads} OpenMP threads", seconds=dt)
+    res = dict(value=len(rows_sample) * reps / dt, unit="rows/s", cores=threads, kind="oracle",
+               sample=f"{len(rows_sample)} of {w.total_rows} rows of {w.name}, {reps} rep(s), fp64 C oracle, "
+                      f"{threads} OpenMP threads", seconds=dt, cpu_model=_cpu_model())
+    if single_thread:  # the same oracle on one core, one row
+        one = rows_sample[:1]
+        t1 = time.perf_counter()
+        oracle.forward(pr, x, rows=one, threads=1)
+        res["value_1_thread"] = round(len(one) / (time.perf_counter() - t1), 3)
+    return res
+
+
+def _cpu_model():
+    """CPU model of the host (for the oracle baseline), from /proc/cpuinfo."""
+    try:
+        info = open("/proc/cpuinfo").read().splitlines()
+    except OSError:
+        return platform.machine()
+    for key in ("model name", "Model", "CPU part"):
+        for ln in info:
+            if ln.split(":")[0].strip() == key:
+                return f"{platform.machine()} {key}: {ln.split(':', 1)[1].strip()}"
+    return platform.machine()
 
 
 def _sample_rows(w, max_rows):
@@ -399,6 +433,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="launch each step directly instead of replaying a CUDA graph")
+    ap.add_argument("--paged-page-size", type=int, default=64,
+                    help="also time the primary workload from a paged cache with this page size (0: skip)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -412,7 +448,7 @@ def main():
         steps_done, t_total = 0, 0.0
         rows = _sample_rows(w, 4 if all(n == 1 for n, _ in w.seqs) else 64)
         for i in range(args.warmup + args.steps):
-            r = cpu_baseline(w, rows)
+            r = cpu_baseline(w, rows, single_thread=False)
             if i >= args.warmup:
                 steps_done += 1
                 t_total += r["seconds"]
@@ -478,6 +514,14 @@ def main():
                              "roofline": roofline_for(w2, res2, hbm, bf16, bf16_sus, peak_kind),
                              "gpu_launches": res2["launches"]}
         line["gpu_launches"] += res2["launches"]
+    if args.paged_page_size > 0:
+        resp = measure_gpu(w, args.steps, args.warmup, dev, dist_on, with_e2e=False, use_graph=not args.no_graph,
+                           page_size=args.paged_page_size)
+        line["paged"] = {"page_size": args.paged_page_size, "workload": w.name,
+                         "value": round(whole_job_rate(rows, ws, max_over_ranks(resp["ms_per_step"], dev if dist_on else None)), 1),
+                         "unit": "rows/s", "ms_per_step": round(resp["ms_per_step"], 5),
+                         "note": "same inputs from a shuffled page pool addressed through a block table"}
+        line["gpu_launches"] += resp["launches"]
     if rank == 0 and not args.no_cpu_baseline:
         cb = cpu_baseline(w, _sample_rows(w, 4 if wc["pre_rows"] == 0 else 64), reps=3 if wc["pre_rows"] == 0 else 1)
         cb.pop("seconds")

@@ -35,7 +35,8 @@ class MsaProblem(C.Structure):
         ("softmax_scale", C.c_float), ("out_dtype", C.c_int32), ("total_rows", C.c_int32),
         ("max_rows_per_seq", C.c_int32), ("max_cache_len", C.c_int32), ("cache_tokens", C.c_int64),
         ("num_decode_seqs", C.c_int32), ("cu_rows", C.c_void_p), ("cache_lens", C.c_void_p),
-        ("cache_starts", C.c_void_p),
+        ("cache_starts", C.c_void_p), ("block_table", C.c_void_p), ("block_table_stride", C.c_int32),
+        ("page_size", C.c_int32),
     ]
 
 
@@ -114,11 +115,14 @@ class Problem:
 
     seqs_host: list of (n_rows, cache_len); the device metadata (cu_rows,
     cache_lens, cache_starts) is built from it on `device` with the caches
-    packed in sequence order unless cache_starts is given.
+    packed in sequence order unless cache_starts is given.  Paged caches:
+    block_table ([B, stride] int32 page numbers, tensor or nested list) and
+    page_size, with cache_tokens = rows of the page pool.
     """
 
     def __init__(self, H, G, seqs_host, device, top_k=16, scale=None, out_dtype=torch.float32,
-                 cache_starts=None, cache_tokens=None, D=128, Di=64, S=64, num_decode_seqs="auto"):
+                 cache_starts=None, cache_tokens=None, D=128, Di=64, S=64, num_decode_seqs="auto",
+                 block_table=None, page_size=0):
         self.H, self.G, self.D, self.Di, self.S, self.top_k = H, G, D, Di, S, top_k
         self.device = torch.device(device)
         if self.device.type == "cuda" and self.device.index is None:
@@ -129,7 +133,15 @@ class Problem:
         cu = [0]
         for n in rows:
             cu.append(cu[-1] + n)
-        if cache_starts is None:
+        self.block_table = None
+        if block_table is not None:
+            if cache_starts is not None or cache_tokens is None:
+                raise ValueError("a block table replaces cache_starts and needs cache_tokens (rows of the page pool)")
+            self.block_table = torch.as_tensor(block_table, dtype=torch.int32).to(self.device).contiguous()
+            if self.block_table.dim() != 2 or self.block_table.shape[0] != len(self.seqs):
+                raise ValueError("block_table must be [num_seqs, stride]")
+            cache_starts = []
+        elif cache_starts is None:
             cache_starts, acc = [], 0
             for L in lens:
                 cache_starts.append(acc)
@@ -148,7 +160,10 @@ class Problem:
             len(self.seqs), H, G, D, Di, S, top_k, self.scale,
             MSA_OUT_BF16 if out_dtype == torch.bfloat16 else MSA_OUT_F32,
             self.total_rows, max(rows), max(lens), self.cache_tokens, num_decode_seqs,
-            self.cu_rows.data_ptr(), self.cache_lens.data_ptr(), self.cache_starts.data_ptr())
+            self.cu_rows.data_ptr(), self.cache_lens.data_ptr(),
+            self.cache_starts.data_ptr() if self.block_table is None else None,
+            None if self.block_table is None else self.block_table.data_ptr(),
+            0 if self.block_table is None else int(self.block_table.shape[1]), int(page_size))
 
     @property
     def max_cache_len(self):

@@ -80,8 +80,7 @@ __global__ void __launch_bounds__(kAttThreads) decode_attend_kernel(const __grid
     const int r = a.cu_rows[b];
     if (a.cu_rows[b + 1] - r != 1) return;  // not a decode sequence
     const int L = a.cache_lens[b];
-    const int64_t start = a.cache_starts[b];
-    if (r < 0 || r >= a.total_rows || L < 1 || L > a.max_cache_len || start < 0 || start + L > a.cache_tokens) {
+    if (r < 0 || r >= a.total_rows || L < 1 || L > a.max_cache_len || !seq_rows_ok(a.cache, b, L, a.cache_tokens)) {
         if (tid == 0 && split == 0) atomicOr(a.err, kErrBadMetadata);
         return;
     }
@@ -116,7 +115,12 @@ __global__ void __launch_bounds__(kAttThreads) decode_attend_kernel(const __grid
     }
 
     // ---- stage K/V of the block (TMA) and the group's queries
-    const int tok0 = static_cast<int>(start + static_cast<int64_t>(blk) * kBlock);
+    int64_t row0 = block_row(a.cache, b, static_cast<int64_t>(blk) * kBlock);
+    if (row0 < 0) {  // page outside the pool
+        if (tid == 0) atomicOr(a.err, kErrBadMetadata);
+        row0 = 0;
+    }
+    const int tok0 = static_cast<int>(row0);
     if (tid == 0) {
         mbar_arrive_expect_tx(&sm.bar, 4 * 64 * 64 * 2);
         tma_load_3d(sm.k[0], &k_map, &sm.bar, 0, h, tok0);

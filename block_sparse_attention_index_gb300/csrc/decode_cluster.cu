@@ -109,9 +109,8 @@ __global__ void __launch_bounds__(kClThreads) decode_cluster_kernel(const __grid
     const int r = a.cu_rows[b];
     if (a.cu_rows[b + 1] - r != 1) return;  // not a decode sequence (the whole cluster returns)
     const int L = a.cache_lens[b];
-    const int64_t start = a.cache_starts[b];
-    const bool meta_ok = !(r < 0 || r >= a.total_rows || L < 1 || L > a.max_cache_len || start < 0 ||
-                           start + L > a.cache_tokens);
+    const bool meta_ok = !(r < 0 || r >= a.total_rows || L < 1 || L > a.max_cache_len) &&
+                         seq_rows_ok(a.cache, b, L, a.cache_tokens);
     if (tid == 0) {
         mbar_init(&sm.bar, 1);
         fence_mbar_init();
@@ -164,7 +163,12 @@ __global__ void __launch_bounds__(kClThreads) decode_cluster_kernel(const __grid
     if (tid == 0 && nmy > 0) {
         mbar_arrive_expect_tx(&sm.bar, nmy * 4 * 64 * 64 * 2);
         for (int i = 0; i < nmy; ++i) {
-            const int tok = static_cast<int>(start + static_cast<int64_t>(blk[i]) * kBlock);
+            int64_t row = block_row(a.cache, b, static_cast<int64_t>(blk[i]) * kBlock);
+            if (row < 0) {  // page outside the pool
+                atomicOr(a.err, kErrBadMetadata);
+                row = 0;
+            }
+            const int tok = static_cast<int>(row);
             tma_load_3d(sm.k[i][0], &k_map, &sm.bar, 0, h, tok);
             tma_load_3d(sm.k[i][1], &k_map, &sm.bar, 64, h, tok);
             tma_load_3d(sm.v[i][0], &v_map, &sm.bar, 0, h, tok);

@@ -53,7 +53,6 @@ __device__ __forceinline__ void mma_bf16_16816(float (&c)[4], uint32_t a0, uint3
 
 struct ScanSeqState {
     int b = -1, L = 0, r = 0;
-    int64_t start = 0;
 };
 
 // Advance to the sequence holding unit u and refresh its metadata.
@@ -64,11 +63,9 @@ __device__ __forceinline__ bool scan_locate(const ScanArgs& a, const int32_t* pr
         st.b = b;
         const int r = a.cu_rows[b];
         int L = min(max(a.cache_lens[b], 0), a.max_cache_len);
-        const int64_t start = a.cache_starts[b];
-        if (r < 0 || r >= a.total_rows || start < 0 || start + L > a.cache_tokens) L = 0;  // inconsistent: skip
+        if (r < 0 || r >= a.total_rows || !seq_rows_ok(a.cache, b, L, a.cache_tokens)) L = 0;  // inconsistent: skip
         st.L = L;
         st.r = r < 0 ? 0 : (r >= a.total_rows ? a.total_rows - 1 : r);
-        st.start = start;
         return true;
     }
     return false;
@@ -161,7 +158,12 @@ __global__ void __launch_bounds__(ScanCfg<H>::kThreads, 1) decode_scan_kernel(co
                     // whole 64-position boxes; rows past the sequence are masked by the consumer
                     // and rows past the cache are zero-filled by the copy engine
                     mbar_arrive_expect_tx(&full[s], Cfg::kUnitBytes);
-                    const int tok = static_cast<int>(st.start + static_cast<int64_t>(j) * kBlock);
+                    int64_t row = block_row(a.cache, b, static_cast<int64_t>(j) * kBlock);
+                    if (row < 0) {  // page outside the pool
+                        atomicOr(a.err, kErrBadMetadata);
+                        row = 0;
+                    }
+                    const int tok = static_cast<int>(row);
 #pragma unroll
                     for (int h = 0; h < H; ++h)
                         tma_load_3d(ring + s * Cfg::kUnitBytes + h * Cfg::kHeadBytes, &ik_map, &full[s], 0, h, tok);

@@ -8,6 +8,39 @@
 
 namespace msa {
 
+// Where the cache rows of a sequence live in k, v and ik: contiguous
+// (position t of sequence b at row starts[b] + t) or paged (row
+// table[b * stride + t / page] * page + t % page, page = 2^page_shift >= 64,
+// so a 64-position block never straddles two pages).
+struct CacheRows {
+    const int64_t* starts;  // contiguous layout (table == nullptr)
+    const int32_t* table;   // paged layout: [num_seqs, stride] page numbers
+    int32_t stride;
+    int32_t page_shift;
+    int64_t num_pages;
+};
+
+#ifdef __CUDACC__
+// Row of the first position of the 64-position block holding position t
+// (t a multiple of 64, t < L_b) of sequence b, or -1 when its page number is
+// outside the pool: the caller flags bad metadata and reads nothing there.
+// (The contiguous layout is checked per sequence by seq_rows_ok.)
+__device__ __forceinline__ int64_t block_row(const CacheRows& c, int b, int64_t t) {
+    if (c.table == nullptr) return c.starts[b] + t;
+    const int32_t pg = c.table[static_cast<int64_t>(b) * c.stride + (t >> c.page_shift)];
+    if (pg < 0 || pg >= c.num_pages) return -1;
+    return (static_cast<int64_t>(pg) << c.page_shift) + (t & ((int64_t{1} << c.page_shift) - 1));
+}
+
+// Whole-sequence check of the contiguous layout (paged layouts are checked
+// block by block in block_row).
+__device__ __forceinline__ bool seq_rows_ok(const CacheRows& c, int b, int L, int64_t cache_tokens) {
+    if (c.table != nullptr) return true;
+    const int64_t start = c.starts[b];
+    return start >= 0 && start + L <= cache_tokens;
+}
+#endif
+
 // Per-(sequence, KV head, split) partial softmax state of decode attention:
 // unnormalised output O[16][128], running max m[16] (log2 domain), sum l[16].
 constexpr int kPartialFloats = 16 * 128 + 16 + 16;
@@ -19,7 +52,7 @@ struct ScanArgs {
     const uint16_t* ik;
     const int32_t* cu_rows;
     const int32_t* cache_lens;
-    const int64_t* cache_starts;
+    CacheRows cache;
     int num_seqs;
     int total_rows;
     int max_cache_len;
@@ -42,7 +75,7 @@ struct DecodeAttendArgs {
     const int32_t* nsel_in;
     const int32_t* cu_rows;
     const int32_t* cache_lens;
-    const int64_t* cache_starts;
+    CacheRows cache;
     int num_seqs, H, G, top_k, total_rows, max_cache_len;
     int64_t cache_tokens;
     float scale_log2;          // softmax scale * log2(e)
@@ -60,15 +93,15 @@ struct StagedArgs {
     int64_t cache_tokens;
     const int32_t* cu_rows;
     const int32_t* cache_lens;
-    const int64_t* cache_starts;
+    CacheRows cache;
 };
 
 struct PrefillIndexArgs {
     const CUtensorMap* iq_map;  // iq as (Di, H, rows)
-    const CUtensorMap* ik_map;  // ik as (Di, H, tokens)
+    const CUtensorMap* ik_map;  // ik as (Di, H, tokens), box 64 x 1 x 256 (64 x 1 x 64 when paged)
     const int32_t* cu_rows;
     const int32_t* cache_lens;
-    const int64_t* cache_starts;
+    CacheRows cache;
     int num_seqs, H, top_k, total_rows, max_rows_per_seq, max_cache_len;
     int64_t cache_tokens;
     int32_t* sel;   // [R, H, top_k]
@@ -84,7 +117,7 @@ struct PrefillAttendArgs {
     const int32_t* nsel;
     const int32_t* cu_rows;
     const int32_t* cache_lens;
-    const int64_t* cache_starts;
+    CacheRows cache;
     int num_seqs, H, G, top_k, total_rows, max_rows_per_seq, max_cache_len;
     int64_t cache_tokens;
     float scale_log2;

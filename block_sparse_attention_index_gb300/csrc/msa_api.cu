@@ -64,10 +64,21 @@ msa_status check_problem(const msa_problem* p) {
         return fail(MSA_ERR_INVALID_ARG, "num_decode_seqs out of range");
     if (p->max_rows_per_seq == 1 && p->num_decode_seqs != -1 && p->num_decode_seqs != p->num_seqs)
         return fail(MSA_ERR_INVALID_ARG, "max_rows_per_seq == 1 implies num_decode_seqs == num_seqs");
-    if (!p->cu_rows || !p->cache_lens || !p->cache_starts) return fail(MSA_ERR_INVALID_ARG, "device metadata is null");
+    if (!p->cu_rows || !p->cache_lens) return fail(MSA_ERR_INVALID_ARG, "device metadata is null");
     if (!aligned16(p->cu_rows) && (reinterpret_cast<uintptr_t>(p->cu_rows) & 3u))
         return fail(MSA_ERR_INVALID_ARG, "cu_rows misaligned");
-    if (reinterpret_cast<uintptr_t>(p->cache_starts) & 7u) return fail(MSA_ERR_INVALID_ARG, "cache_starts misaligned");
+    if (p->block_table == nullptr) {
+        if (!p->cache_starts) return fail(MSA_ERR_INVALID_ARG, "cache_starts is null (and no block table)");
+        if (reinterpret_cast<uintptr_t>(p->cache_starts) & 7u) return fail(MSA_ERR_INVALID_ARG, "cache_starts misaligned");
+    } else {
+        const int32_t ps = p->page_size;
+        if (ps < msa::kBlock || ps > (1 << 20) || (ps & (ps - 1)) != 0)
+            return fail(MSA_ERR_UNSUPPORTED, "page_size must be a power of two in [64, 2^20] (got %d)", ps);
+        if (p->cache_tokens % ps != 0) return fail(MSA_ERR_INVALID_ARG, "cache_tokens must be a multiple of page_size");
+        if (static_cast<int64_t>(p->block_table_stride) * ps < p->max_cache_len)
+            return fail(MSA_ERR_INVALID_ARG, "block_table_stride * page_size < max_cache_len");
+        if (reinterpret_cast<uintptr_t>(p->block_table) & 3u) return fail(MSA_ERR_INVALID_ARG, "block_table misaligned");
+    }
     return MSA_OK;
 }
 
@@ -78,6 +89,20 @@ msa_status check_ptr(const void* ptr, const char* name) {
 }
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+msa::CacheRows cache_rows_of(const msa_problem* p) {
+    msa::CacheRows c{};
+    c.starts = p->cache_starts;
+    c.table = p->block_table;
+    if (c.table != nullptr) {
+        c.stride = p->block_table_stride;
+        int shift = 0;
+        while ((1 << shift) < p->page_size) ++shift;
+        c.page_shift = shift;
+        c.num_pages = p->cache_tokens / p->page_size;
+    }
+    return c;
+}
 
 struct Layout {
     size_t err = 0, tickets = 0, pooled = 0, partials = 0, sel = 0, nsel = 0, total = 0;
@@ -148,7 +173,7 @@ msa::StagedArgs staged_args(const msa_problem* p) {
     a.cache_tokens = p->cache_tokens;
     a.cu_rows = p->cu_rows;
     a.cache_lens = p->cache_lens;
-    a.cache_starts = p->cache_starts;
+    a.cache = cache_rows_of(p);
     return a;
 }
 
@@ -301,7 +326,7 @@ static msa::DecodeAttendArgs decode_args(const msa_problem* p, const CUtensorMap
     a.max_blocks = static_cast<int>((p->max_cache_len + msa::kBlock - 1) / msa::kBlock);
     a.cu_rows = p->cu_rows;
     a.cache_lens = p->cache_lens;
-    a.cache_starts = p->cache_starts;
+    a.cache = cache_rows_of(p);
     a.num_seqs = p->num_seqs;
     a.H = p->num_kv_heads;
     a.G = p->group_size;
@@ -354,7 +379,7 @@ static msa::PrefillAttendArgs prefill_attend_args(const msa_problem* p, const CU
     a.nsel = nsel;
     a.cu_rows = p->cu_rows;
     a.cache_lens = p->cache_lens;
-    a.cache_starts = p->cache_starts;
+    a.cache = cache_rows_of(p);
     a.num_seqs = p->num_seqs;
     a.H = p->num_kv_heads;
     a.G = p->group_size;
@@ -466,7 +491,9 @@ msa_status msa_forward_marked(const msa_problem* p, const void* q, const void* i
     if ((s = attention_maps(p, q, k_cache, v_cache, pre ? &qm : nullptr, &km, &vm)) != MSA_OK) return s;
     if (pre) {
         if ((s = make_map(&iqm, iq, 64, H, p->total_rows, 64, 1, 128, "iq")) != MSA_OK) return s;
-        if ((s = make_map(&ikm, ik_cache, 64, H, T, 64, 1, 256, "ik_cache")) != MSA_OK) return s;
+        // a whole 256-position tile per box, or one box per 64-position block when paged
+        const uint32_t box = p->block_table == nullptr ? 256 : 64;
+        if ((s = make_map(&ikm, ik_cache, 64, H, T, 64, 1, box, "ik_cache")) != MSA_OK) return s;
     }
     CUtensorMap ik_scan;
     if (dec && (s = make_map(&ik_scan, ik_cache, 64, H, T, 64, 1, 64, "ik_cache")) != MSA_OK) return s;
@@ -480,7 +507,7 @@ msa_status msa_forward_marked(const msa_problem* p, const void* q, const void* i
         sa.ik = static_cast<const uint16_t*>(ik_cache);
         sa.cu_rows = p->cu_rows;
         sa.cache_lens = p->cache_lens;
-        sa.cache_starts = p->cache_starts;
+        sa.cache = cache_rows_of(p);
         sa.num_seqs = p->num_seqs;
         sa.total_rows = p->total_rows;
         sa.max_cache_len = p->max_cache_len;
@@ -512,7 +539,7 @@ msa_status msa_forward_marked(const msa_problem* p, const void* q, const void* i
         ia.ik_map = &ikm;
         ia.cu_rows = p->cu_rows;
         ia.cache_lens = p->cache_lens;
-        ia.cache_starts = p->cache_starts;
+        ia.cache = cache_rows_of(p);
         ia.num_seqs = p->num_seqs;
         ia.H = p->num_kv_heads;
         ia.top_k = p->top_k;

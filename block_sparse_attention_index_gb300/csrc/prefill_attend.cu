@@ -60,9 +60,9 @@ constexpr int kInfoReaders = 1 + 2 + 8 + 4;      // V producer, S and PV issuers
 // thread per CTA walks the sequence metadata and reads the selection.
 struct ItemInfo {
     int32_t r, h, p, nsel, end;
-    int32_t pad;
-    int64_t start;
-    int32_t blk[kMaxTopK];
+    int32_t b;                // sequence
+    int32_t blk[kMaxTopK];    // kept blocks
+    int32_t row[kMaxTopK];    // their first cache rows
 };
 
 struct __align__(1024) AttendSmem {
@@ -93,9 +93,9 @@ struct __align__(1024) AttendSmem {
 static_assert(sizeof(AttendSmem) + 1024 <= 227 * 1024, "prompt-chunk attention exceeds 227 KB of shared memory");
 
 struct Item {
-    int r, h, p, nsel;
-    int64_t start;
+    int r, h, p, nsel, b;
     int blk[kMaxTopK];
+    int row[kMaxTopK];
 };
 
 // Decodes work item `it`; false when the item is skipped (a row of a decode
@@ -113,10 +113,10 @@ __device__ bool load_item(const PrefillAttendArgs& a, int it, Item& x, bool& bad
     const int n = a.cu_rows[b + 1] - a.cu_rows[b];
     if (a.only_multi_row && n <= 1) return false;
     const int L = a.cache_lens[b];
-    x.start = a.cache_starts[b];
+    x.b = b;
     x.p = L - n + (x.r - a.cu_rows[b]);
-    if (x.r < a.cu_rows[b] || x.r >= a.cu_rows[b + 1] || L < 1 || L > a.max_cache_len || x.p < 0 || x.start < 0 ||
-        x.start + L > a.cache_tokens) {
+    if (x.r < a.cu_rows[b] || x.r >= a.cu_rows[b + 1] || L < 1 || L > a.max_cache_len || x.p < 0 ||
+        !seq_rows_ok(a.cache, b, L, a.cache_tokens)) {
         bad = true;
         return false;
     }
@@ -133,6 +133,16 @@ __device__ bool load_item(const PrefillAttendArgs& a, int it, Item& x, bool& bad
             bad = true;
             return false;
         }
+    }
+    const int64_t start = a.cache.table == nullptr ? a.cache.starts[b] : 0;
+    for (int i = 0; i < kMaxTopK; ++i) {  // cache rows of the kept blocks (independent loads when paged)
+        const int64_t t = static_cast<int64_t>(x.blk[i]) * kBlock;
+        const int64_t row = i >= x.nsel ? 0 : (a.cache.table == nullptr ? start + t : block_row(a.cache, b, t));
+        if (row < 0) {  // page outside the pool
+            bad = true;
+            return false;
+        }
+        x.row[i] = static_cast<int>(row);
     }
     return true;
 }
@@ -206,9 +216,12 @@ __global__ void __launch_bounds__(kPaThreads, 1) prefill_attend_kernel(const __g
                 inf.h = x.h;
                 inf.p = x.p;
                 inf.nsel = x.nsel;
-                inf.start = x.start;
+                inf.b = x.b;
                 inf.end = 0;
-                for (int i = 0; i < kMaxTopK; ++i) inf.blk[i] = x.blk[i];
+                for (int i = 0; i < kMaxTopK; ++i) {
+                    inf.blk[i] = x.blk[i];
+                    inf.row[i] = x.row[i];
+                }
                 mbar_arrive(&sm.info_full[slot]);  // release: the fields above are visible
                 const int qb = n & 1;
                 if (n >= 2 && !mbar_wait(&sm.q_empty[qb], ((n >> 1) - 1) & 1, a.err)) break;
@@ -226,8 +239,7 @@ __global__ void __launch_bounds__(kPaThreads, 1) prefill_attend_kernel(const __g
                     }
                     mbar_arrive_expect_tx(&sm.kfull[s], kPairBytes);
                     for (int half = 0; half < 2; ++half) {
-                        const int blk = x.blk[min(2 * q + half, x.nsel - 1)];
-                        const int tok = static_cast<int>(x.start + static_cast<int64_t>(blk) * kBlock);
+                        const int tok = x.row[min(2 * q + half, x.nsel - 1)];
                         tma_load_3d(sm.kst[s] + half * 8192, &k_map, &sm.kfull[s], 0, x.h, tok);
                         tma_load_3d(sm.kst[s] + half * 8192 + 16384, &k_map, &sm.kfull[s], 64, x.h, tok);
                     }
@@ -262,8 +274,7 @@ __global__ void __launch_bounds__(kPaThreads, 1) prefill_attend_kernel(const __g
                     }
                     mbar_arrive_expect_tx(&sm.pv_full[s], kPairBytes);
                     for (int half = 0; half < 2; ++half) {
-                        const int blk = inf.blk[min(2 * q + half, inf.nsel - 1)];
-                        const int tok = static_cast<int>(inf.start + static_cast<int64_t>(blk) * kBlock);
+                        const int tok = inf.row[min(2 * q + half, inf.nsel - 1)];
                         tma_load_3d(sm.vst[s] + half * 8192, &v_map, &sm.pv_full[s], 0, inf.h, tok);
                         tma_load_3d(sm.vst[s] + half * 8192 + 16384, &v_map, &sm.pv_full[s], 64, inf.h, tok);
                     }

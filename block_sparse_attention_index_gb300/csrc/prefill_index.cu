@@ -40,7 +40,7 @@ struct __align__(1024) IndexSmem {
     uint64_t acc_empty[2];
     uint32_t tmem_base;
     int32_t seq, row0, nrows, ntiles, p0, L;
-    int64_t start;
+
 };
 
 // Which (sequence, row tile) CTA `tile` handles; false when beyond the end.
@@ -89,17 +89,15 @@ __global__ void __launch_bounds__(kIdxThreads, 1) prefill_index_kernel(const __g
         sm.seq = -1;
         if (find_tile(a, blockIdx.x, b, i0, n)) {
             const int L = a.cache_lens[b];
-            const int64_t start = a.cache_starts[b];
             const int r0 = a.cu_rows[b] + i0;
             const int nr = min(kIdxRows, n - i0);
-            const bool ok = L >= n && L <= a.max_cache_len && start >= 0 && start + L <= a.cache_tokens &&
+            const bool ok = L >= n && L <= a.max_cache_len && seq_rows_ok(a.cache, b, L, a.cache_tokens) &&
                             r0 >= 0 && r0 + nr <= a.total_rows;
             if (ok) {
                 sm.seq = b;
                 sm.row0 = r0;
                 sm.nrows = nr;
                 sm.L = L;
-                sm.start = start;
                 sm.p0 = L - n + i0;                              // position of the tile's first row
                 const int pmax = sm.p0 + nr - 1;
                 sm.ntiles = (pmax + kIdxCols) / kIdxCols;        // tiles covering positions 0..pmax
@@ -134,12 +132,38 @@ __global__ void __launch_bounds__(kIdxThreads, 1) prefill_index_kernel(const __g
             prefetch_tmap(&ik_map);
             mbar_arrive_expect_tx(&sm.a_full, kIdxABytes);
             tma_load_3d(sm.a, &iq_map, &sm.a_full, 0, h, sm.row0);
-            const int tok0 = static_cast<int>(sm.start);
             for (int n = 0; n < ntiles; ++n) {
                 const int s = n % kIdxStages;
                 if (n >= kIdxStages && !mbar_wait(&sm.empty[s], ((n / kIdxStages) - 1) & 1, a.err)) break;
-                mbar_arrive_expect_tx(&sm.full[s], kIdxTileBytes);
-                tma_load_3d(sm.b[s], &ik_map, &sm.full[s], 0, h, tok0 + n * kIdxCols);
+                if (a.cache.table == nullptr) {  // contiguous: the tile is one 256-position box
+                    mbar_arrive_expect_tx(&sm.full[s], kIdxTileBytes);
+                    tma_load_3d(sm.b[s], &ik_map, &sm.full[s], 0, h,
+                                static_cast<int>(a.cache.starts[sm.seq] + static_cast<int64_t>(n) * kIdxCols));
+                    continue;
+                }
+                // paged: one 64-position box per block (blocks sit on separate pages);
+                // blocks at or past L are not loaded (their positions are masked)
+                int64_t rows[kIdxCols / kBlock];
+                int nbox = 0;
+#pragma unroll
+                for (int qq = 0; qq < kIdxCols / kBlock; ++qq) {
+                    const int64_t t = static_cast<int64_t>(n) * kIdxCols + qq * kBlock;
+                    rows[qq] = -1;
+                    if (t < sm.L) {
+                        rows[qq] = block_row(a.cache, sm.seq, t);
+                        if (rows[qq] < 0) {  // page outside the pool
+                            atomicOr(a.err, kErrBadMetadata);
+                            rows[qq] = 0;
+                        }
+                        ++nbox;
+                    }
+                }
+                mbar_arrive_expect_tx(&sm.full[s], nbox * (kIdxTileBytes / (kIdxCols / kBlock)));
+#pragma unroll
+                for (int qq = 0; qq < kIdxCols / kBlock; ++qq)
+                    if (rows[qq] >= 0)
+                        tma_load_3d(sm.b[s] + qq * (kIdxTileBytes / (kIdxCols / kBlock)), &ik_map, &sm.full[s], 0, h,
+                                    static_cast<int>(rows[qq]));
             }
         }
     } else if (warp == 5) {

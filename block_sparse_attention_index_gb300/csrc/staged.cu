@@ -10,7 +10,7 @@ namespace msa {
 
 constexpr int kStagedThreads = 128;
 
-__device__ __forceinline__ bool row_position(const StagedArgs& a, int r, int& b, int& p, int64_t& start) {
+__device__ __forceinline__ bool row_position(const StagedArgs& a, int r, int& b, int& p) {
     int lo = 0, hi = a.num_seqs;  // largest b with cu_rows[b] <= r
     while (hi - lo > 1) {
         const int mid = (lo + hi) >> 1;
@@ -19,10 +19,9 @@ __device__ __forceinline__ bool row_position(const StagedArgs& a, int r, int& b,
     b = lo;
     const int n = a.cu_rows[b + 1] - a.cu_rows[b];
     const int L = a.cache_lens[b];
-    start = a.cache_starts[b];
     p = L - n + (r - a.cu_rows[b]);
-    return r >= a.cu_rows[b] && r < a.cu_rows[b + 1] && L >= 1 && L <= a.max_cache_len && p >= 0 && start >= 0 &&
-           start + L <= a.cache_tokens;
+    return r >= a.cu_rows[b] && r < a.cu_rows[b + 1] && L >= 1 && L <= a.max_cache_len && p >= 0 &&
+           seq_rows_ok(a.cache, b, L, a.cache_tokens);
 }
 
 // grid (rows, H): one CTA per (row, head)
@@ -31,8 +30,7 @@ __global__ void __launch_bounds__(kStagedThreads) index_scores_kernel(StagedArgs
                                                                       float* __restrict__ scores, int64_t ld) {
     const int h = blockIdx.y, r = blockIdx.x;
     int b, p;
-    int64_t start;
-    const bool ok = row_position(a, r, b, p, start);
+    const bool ok = row_position(a, r, b, p);
     float q[kIndexDim];
     const uint16_t* qp = iq + (static_cast<int64_t>(r) * a.H + h) * kIndexDim;
 #pragma unroll
@@ -46,8 +44,9 @@ __global__ void __launch_bounds__(kStagedThreads) index_scores_kernel(StagedArgs
     float* out = scores + (static_cast<int64_t>(r) * a.H + h) * ld;
     for (int64_t t = threadIdx.x; t < ld; t += kStagedThreads) {
         float s = -INFINITY;
-        if (ok && t <= p) {
-            const uint16_t* kp = ik + ((start + t) * a.H + h) * kIndexDim;
+        const int64_t row0 = ok && t <= p ? block_row(a.cache, b, t & ~int64_t{kBlock - 1}) : -1;
+        if (row0 >= 0) {  // (a page outside the pool leaves -inf)
+            const uint16_t* kp = ik + ((row0 + (t & (kBlock - 1))) * a.H + h) * kIndexDim;
             s = 0.f;
 #pragma unroll
             for (int c = 0; c < kIndexDim / 8; ++c) {
@@ -70,9 +69,8 @@ __global__ void __launch_bounds__(kStagedThreads) select_blocks_kernel(StagedArg
     __shared__ SelectSmem<kStagedThreads> sm;
     const int h = blockIdx.y, r = blockIdx.x;
     int b, p;
-    int64_t start;
     int32_t* out = sel + (static_cast<int64_t>(r) * a.H + h) * a.top_k;
-    if (!row_position(a, r, b, p, start)) {
+    if (!row_position(a, r, b, p)) {
         for (int i = threadIdx.x; i < a.top_k; i += kStagedThreads) out[i] = -1;
         if (threadIdx.x == 0) nsel[static_cast<int64_t>(r) * a.H + h] = 0;
         return;

@@ -45,7 +45,7 @@
  *   - Errors: invalid or unsupported arguments are rejected on the host
  *     before anything is enqueued (MSA_ERR_INVALID_ARG, MSA_ERR_UNSUPPORTED,
  *     MSA_ERR_WORKSPACE).  A failed launch returns MSA_ERR_CUDA.  Device
- *     metadata (cu_rows, cache_lens, cache_starts) is read only by kernels:
+ *     metadata (cu_rows, cache_lens, cache_starts, block_table) is read only by kernels:
  *     values inconsistent with the host-side bounds in msa_problem are the
  *     caller's error; kernels clamp them so that they never read or write
  *     out of the stated extents, and the affected outputs are unspecified.
@@ -101,7 +101,18 @@ typedef struct msa_problem {
                                  run and each skips the other's sequences)   */
     const int32_t* cu_rows;      /* device [B+1], cu_rows[0] = 0, ascending    */
     const int32_t* cache_lens;   /* device [B], 1 <= L_b <= max_cache_len      */
-    const int64_t* cache_starts; /* device [B], start + L_b <= cache_tokens    */
+    const int64_t* cache_starts; /* device [B], start + L_b <= cache_tokens;
+                                    NULL (not read) with a block table         */
+    /* Paged caches (optional).  With block_table set, position t of sequence
+     * b is row  block_table[b * block_table_stride + t / page_size] *
+     * page_size + t % page_size  of k, v and ik (each a pool of cache_tokens
+     * rows = num_pages * page_size); cache_starts is not read.  NULL: the
+     * contiguous layout through cache_starts.  Page numbers outside
+     * [0, cache_tokens / page_size) set the device error word (bad metadata)
+     * and are not read. */
+    const int32_t* block_table;  /* device [B, block_table_stride] int32 page numbers, or NULL */
+    int32_t block_table_stride;  /* >= ceil(max_cache_len / page_size)           */
+    int32_t page_size;           /* tokens per page: a power of two >= 64 (=S x 2^k) */
 } msa_problem;
 
 /* Human-readable name of a status code (static string). */

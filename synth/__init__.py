@@ -208,6 +208,45 @@ def make_inputs(w: Workload, with_kv: bool = True) -> dict:
     return out
 
 
+STREAM_PAGES, STREAM_POOL = 101, 102
+
+
+def paged_layout(w: Workload, x: dict, page_size: int, spare_pages: int = 3, seed: int = 0) -> dict:
+    """The same caches as a page pool: sequence b's positions [i*page, (i+1)*page)
+    live on page table[b, i] of the pool, the pages shuffled by a seeded
+    permutation; pool rows that hold no position (page tails, spare pages) get
+    other random values, so that reading a wrong row changes the result.
+    Returns pool arrays k, v, ik ([num_pages * page_size, H, width]), the block
+    table [B, stride] int32 (-1 past each sequence) and num_pages."""
+    lens = [int(L) for _, L in w.seqs]
+    pages = [(L + page_size - 1) // page_size for L in lens]
+    num_pages = sum(pages) + spare_pages
+    stride = max(pages)
+    order = np.argsort(uniform(seed, STREAM_PAGES, num_pages))  # a seeded permutation of the pages
+    table = np.full((len(lens), stride), -1, dtype=np.int32)
+    nxt = 0
+    for b, npg in enumerate(pages):
+        table[b, :npg] = order[nxt:nxt + npg]
+        nxt += npg
+    rows = num_pages * page_size
+    out = dict(table=table, num_pages=num_pages, page_size=page_size)
+    starts = x["cache_starts"]
+    for i, name in enumerate(n for n in ("k", "v", "ik") if n in x):
+        src = x[name]
+        width = src.shape[2]
+        if name == "ik":
+            pool = int_bf16(seed, STREAM_POOL + i, (rows, w.H, width))
+        else:
+            pool = normal_bf16(seed, STREAM_POOL + i, (rows, w.H, width))
+        for b, L in enumerate(lens):
+            for pg in range(pages[b]):
+                t0, t1 = pg * page_size, min(L, (pg + 1) * page_size)
+                r0 = int(table[b, pg]) * page_size
+                pool[r0:r0 + (t1 - t0)] = src[int(starts[b]) + t0:int(starts[b]) + t1]
+        out[name] = pool
+    return out
+
+
 def _c5_seqs(seed: int) -> list:
     lens = ragged_lengths(seed, 8, 1024, 196608)
     return [(1, L) for L in lens] + [(512, 32768 + 512)]

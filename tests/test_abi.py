@@ -60,7 +60,14 @@ def _problem(**over):
     (dict(num_seqs=0), 1), (dict(softmax_scale=float("nan")), 1), (dict(softmax_scale=-1.0), 1),
     (dict(out_dtype=7), 1), (dict(total_rows=0), 1), (dict(max_rows_per_seq=2), 1),
     (dict(max_cache_len=(1 << 21) + 1), 2), (dict(cache_tokens=0), 1), (dict(num_decode_seqs=2), 1),
-    (dict(cu_rows=None), 1), (dict(cache_starts=260), 1),
+    (dict(cu_rows=None), 1), (dict(cache_starts=260), 1), (dict(cache_starts=None), 1),
+    # paged caches: page size a power of two >= 64, pool a whole number of pages,
+    # table wide enough for max_cache_len, table aligned
+    (dict(cache_starts=None, block_table=1024, block_table_stride=64, page_size=32), 2),
+    (dict(cache_starts=None, block_table=1024, block_table_stride=64, page_size=96), 2),
+    (dict(cache_starts=None, block_table=1024, block_table_stride=64, page_size=64, cache_tokens=4000), 1),
+    (dict(cache_starts=None, block_table=1024, block_table_stride=63, page_size=64), 1),
+    (dict(cache_starts=None, block_table=1026, block_table_stride=64, page_size=64), 1),
 ])
 def test_invalid_problem_rejected_on_host(over, status):
     import block_sparse_attention_index_gb300 as m
@@ -94,3 +101,11 @@ def test_workspace_size_and_pointer_checks():
     assert L.msa_forward_launches(C.byref(_problem(max_rows_per_seq=4, total_rows=4, num_decode_seqs=0))) == 2
     assert L.msa_forward_launches(C.byref(_problem(num_seqs=2, max_rows_per_seq=4, total_rows=5,
                                                    num_decode_seqs=1))) == 4
+
+
+def test_paged_problem_accepted_on_host():
+    import block_sparse_attention_index_gb300 as m
+    n = C.c_size_t(0)
+    for ps, stride in ((64, 64), (256, 16), (4096, 1)):
+        pb = _problem(cache_starts=None, block_table=1024, block_table_stride=stride, page_size=ps)
+        assert m.lib().msa_workspace_size(C.byref(pb), C.byref(n)) == 0, m.lib().msa_last_error()
