@@ -34,6 +34,8 @@ sys.path.insert(0, ROOT)
 
 import synth  # noqa: E402
 
+DECODE_MAX_ROWS = 8  # sequences with up to this many rows take the decode kernels
+
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 PROFILES = os.path.join(ROOT, "profiles")
 FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS = 6800.0, 1900.0
@@ -60,12 +62,14 @@ def _kept_keys(p, top_k=16, S=64):
 def work_counts(w: synth.Workload):
     """Algorithmic bytes and FLOPs of one step, by stage."""
     H, G, D, Di = w.H, w.G, w.D, w.Di
-    dec = [(n, L) for n, L in w.seqs if n == 1]
-    pre = [(n, L) for n, L in w.seqs if n > 1]
-    # decode scan: every cached index key once, the index query, the pooled scores out
-    scan_bytes = sum(L * H * Di * 2 + H * Di * 2 + ((L + 63) // 64) * H * 4 for _, L in dec)
-    # decode attention: kept K/V blocks, q in, out (fp32) out
-    att_bytes = sum(H * (_kept_keys(L - 1, w.top_k) * D * 2 * 2) + H * G * D * (2 + 4) for _, L in dec)
+    dec = [(n, L) for n, L in w.seqs if n <= DECODE_MAX_ROWS]  # decode family: 1 to 8 rows per sequence
+    pre = [(n, L) for n, L in w.seqs if n > DECODE_MAX_ROWS]
+    # decode scan: every cached index key once (shared by the sequence's rows), the
+    # index queries, the pooled scores out
+    scan_bytes = sum(L * H * Di * 2 + n * H * Di * 2 + n * ((L + 63) // 64) * H * 4 for n, L in dec)
+    # decode attention: kept K/V blocks, q in, out (fp32) out, per row
+    att_bytes = sum(H * (_kept_keys(L - n + i, w.top_k) * D * 2 * 2) + H * G * D * (2 + 4)
+                    for n, L in dec for i in range(n))
     # prompt chunks: causal index-score FLOPs and kept-block attention FLOPs
     idx_flops = 0
     att_flops = 0
@@ -75,7 +79,7 @@ def work_counts(w: synth.Workload):
             idx_flops += 2 * Di * (p + 1) * H
             att_flops += 4 * D * _kept_keys(p, w.top_k) * H * G
     return dict(scan_bytes=scan_bytes, dec_att_bytes=att_bytes, idx_flops=idx_flops, att_flops=att_flops,
-                dec_rows=len(dec), pre_rows=sum(n for n, _ in pre))
+                dec_rows=sum(n for n, _ in dec), pre_rows=sum(n for n, _ in pre))
 
 
 # ---------------------------------------------------------------- ncu traffic
@@ -395,8 +399,8 @@ def _sample_rows(w, max_rows):
 
 
 def _metric_for(w):
-    dec = all(n == 1 for n, _ in w.seqs)
-    pre = all(n > 1 for n, _ in w.seqs)
+    dec = all(n <= DECODE_MAX_ROWS for n, _ in w.seqs)
+    pre = all(n > DECODE_MAX_ROWS for n, _ in w.seqs)
     return "MSA decode rows/s" if dec else ("MSA prefill rows/s" if pre else "MSA rows/s (mixed decode + prefill)")
 
 
@@ -433,6 +437,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="launch each step directly instead of replaying a CUDA graph")
+    ap.add_argument("--multirow", default="decode_4x4_65536",
+                    help="decode workload with several rows per sequence measured in the same run ('none' to skip)")
     ap.add_argument("--paged-page-size", type=int, default=64,
                     help="also time the primary workload from a paged cache with this page size (0: skip)")
     args = ap.parse_args()
@@ -446,7 +452,7 @@ def main():
         if rank != 0:
             return
         steps_done, t_total = 0, 0.0
-        rows = _sample_rows(w, 4 if all(n == 1 for n, _ in w.seqs) else 64)
+        rows = _sample_rows(w, 4 if all(n <= DECODE_MAX_ROWS for n, _ in w.seqs) else 64)
         for i in range(args.warmup + args.steps):
             r = cpu_baseline(w, rows, single_thread=False)
             if i >= args.warmup:
@@ -522,6 +528,17 @@ def main():
                          "unit": "rows/s", "ms_per_step": round(resp["ms_per_step"], 5),
                          "note": "same inputs from a shuffled page pool addressed through a block table"}
         line["gpu_launches"] += resp["launches"]
+    if args.multirow != "none" and args.multirow != args.workload:
+        w3 = synth.workload(args.multirow)
+        res3 = measure_gpu(w3, args.steps, args.warmup, dev, dist_on, with_e2e=False, use_graph=not args.no_graph)
+        line["multirow"] = {"metric": _metric_for(w3), "workload": w3.name,
+                            "value": round(whole_job_rate(w3.total_rows, ws, res3["ms_per_step"]), 1),
+                            "unit": "rows/s", "ms_per_step": round(res3["ms_per_step"], 5),
+                            "stage_us": {"decode_scan": round(res3["stage_ms"][0] * 1e3, 2),
+                                         "decode_attend": round(res3["stage_ms"][1] * 1e3, 2)},
+                            "roofline": roofline_for(w3, res3, hbm, bf16, bf16_sus, peak_kind),
+                            "note": w3.note}
+        line["gpu_launches"] += res3["launches"]
     if rank == 0 and not args.no_cpu_baseline:
         cb = cpu_baseline(w, _sample_rows(w, 4 if wc["pre_rows"] == 0 else 64), reps=3 if wc["pre_rows"] == 0 else 1)
         cb.pop("seconds")

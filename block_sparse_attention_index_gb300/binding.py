@@ -27,6 +27,9 @@ EXPORTED = [
 ]
 
 
+DECODE_MAX_ROWS = 8  # sequences with up to this many rows take the decode kernels
+
+
 class MsaProblem(C.Structure):
     """Mirror of struct msa_problem."""
     _fields_ = [
@@ -155,7 +158,7 @@ class Problem:
         self.scale = scale if scale is not None else 1.0 / math.sqrt(D)
         self.out_dtype = out_dtype
         if num_decode_seqs == "auto":
-            num_decode_seqs = sum(1 for n in rows if n == 1)
+            num_decode_seqs = sum(1 for n in rows if n <= DECODE_MAX_ROWS)
         self.c = MsaProblem(
             len(self.seqs), H, G, D, Di, S, top_k, self.scale,
             MSA_OUT_BF16 if out_dtype == torch.bfloat16 else MSA_OUT_F32,

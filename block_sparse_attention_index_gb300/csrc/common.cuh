@@ -15,6 +15,7 @@ constexpr int kIndexDim = 64;   // Di
 constexpr int kBlock = 64;      // S, keys per block
 constexpr int kMaxTopK = 16;    // largest supported top_k
 constexpr int kMaxGroup = 16;   // largest supported G
+constexpr int kDecodeMaxRows = 8;  // sequences with up to this many rows take the decode kernels
 
 // Error bits a kernel may set in the workspace error word (never traps).
 enum : uint32_t {

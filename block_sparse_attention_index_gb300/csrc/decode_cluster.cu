@@ -1,4 +1,5 @@
-// Decode stage 2b+3 as one thread-block cluster per (sequence, KV head).
+// Decode stage 2b+3 as one thread-block cluster per (query row, KV head) of
+// the decode family (sequences with up to kDecodeMaxRows rows).
 //
 // PR #1388 "minimax_m3: a CUDA backend for MiniMax-M3.1-Flash ...", commit
 // text of the native Metal family: decode attention runs over the kept
@@ -101,15 +102,18 @@ __global__ void __launch_bounds__(kClThreads) decode_cluster_kernel(const __grid
     extern __shared__ uint8_t smem_raw[];
     ClusterSmem& sm = *reinterpret_cast<ClusterSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int rank = static_cast<int>(cluster_rank());
-    const int h = blockIdx.y, b = blockIdx.z;
+    const int h = blockIdx.y, row_slot = blockIdx.z;  // b * RS + i: row i of sequence b
+    const int b = row_slot / a.rows_per_seq, row_in_seq = row_slot - b * a.rows_per_seq;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int H = a.H, G = a.G;
 
     // ---- prologue: only inputs that no earlier kernel of the step writes
-    const int r = a.cu_rows[b];
-    if (a.cu_rows[b + 1] - r != 1) return;  // not a decode sequence (the whole cluster returns)
+    const int nrows = a.cu_rows[b + 1] - a.cu_rows[b];
+    // not a decode-family sequence, or no such row (the whole cluster returns)
+    if (nrows < 1 || nrows > kDecodeMaxRows || row_in_seq >= nrows) return;
+    const int r = a.cu_rows[b] + row_in_seq;
     const int L = a.cache_lens[b];
-    const bool meta_ok = !(r < 0 || r >= a.total_rows || L < 1 || L > a.max_cache_len) &&
+    const bool meta_ok = !(r < 0 || r >= a.total_rows || L < nrows || L > a.max_cache_len) &&
                          seq_rows_ok(a.cache, b, L, a.cache_tokens);
     if (tid == 0) {
         mbar_init(&sm.bar, 1);
@@ -135,10 +139,10 @@ __global__ void __launch_bounds__(kClThreads) decode_cluster_kernel(const __grid
         return;  // the whole cluster returns: before any cluster barrier
     }
     cluster_arrive_relaxed();  // matched by cluster_wait() before the first remote store
-    const int p = L - 1;
+    const int p = L - nrows + row_in_seq;  // this row's position
     const int J = p / kBlock;
     if constexpr (!kSelGiven) {
-        const float* pooled = a.pooled + (static_cast<int64_t>(b) * H + h) * a.max_blocks;
+        const float* pooled = a.pooled + (static_cast<int64_t>(row_slot) * H + h) * a.max_blocks;
         const int n = cta_select<kClThreads>(pooled, J, a.top_k, sm.sel, sm.select);
         if (tid == 0) sm.nsel = n;
     }
@@ -340,7 +344,7 @@ cudaError_t run_decode_cluster(const DecodeAttendArgs& a, bool after_scan, cudaS
     cudaError_t e = ensure_smem_limit(fn, smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(kCluster, a.H, a.num_seqs);
+    cfg.gridDim = dim3(kCluster, a.H, a.num_seqs * a.rows_per_seq);
     cfg.blockDim = dim3(kClThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;

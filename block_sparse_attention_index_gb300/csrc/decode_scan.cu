@@ -52,7 +52,7 @@ __device__ __forceinline__ void mma_bf16_16816(float (&c)[4], uint32_t a0, uint3
 }
 
 struct ScanSeqState {
-    int b = -1, L = 0, r = 0;
+    int b = -1, L = 0, r = 0, n = 1;  // sequence, cache length, first row, rows
 };
 
 // Advance to the sequence holding unit u and refresh its metadata.
@@ -62,10 +62,12 @@ __device__ __forceinline__ bool scan_locate(const ScanArgs& a, const int32_t* pr
     if (b != st.b) {
         st.b = b;
         const int r = a.cu_rows[b];
-        int L = min(max(a.cache_lens[b], 0), a.max_cache_len);
-        if (r < 0 || r >= a.total_rows || !seq_rows_ok(a.cache, b, L, a.cache_tokens)) L = 0;  // inconsistent: skip
-        st.L = L;
-        st.r = r < 0 ? 0 : (r >= a.total_rows ? a.total_rows - 1 : r);
+        const int nr = min(max(a.cu_rows[b + 1] - r, 1), kDecodeMaxRows);
+        const int L = min(max(a.cache_lens[b], 0), a.max_cache_len);
+        const bool ok = r >= 0 && r + nr <= a.total_rows && L >= nr && seq_rows_ok(a.cache, b, L, a.cache_tokens);
+        st.L = ok ? L : 0;  // inconsistent metadata: the sequence is skipped
+        st.n = ok ? nr : 1;
+        st.r = ok ? r : 0;
         return true;
     }
     return false;
@@ -99,7 +101,8 @@ __global__ void __launch_bounds__(ScanCfg<H>::kThreads, 1) decode_scan_kernel(co
     for (int base = 0; base < a.num_seqs; base += Cfg::kThreads) {
         const int b = base + tid;
         int units = 0;
-        if (b < a.num_seqs && a.cu_rows[b + 1] - a.cu_rows[b] == 1) {
+        const int nrows = b < a.num_seqs ? a.cu_rows[b + 1] - a.cu_rows[b] : 0;
+        if (nrows >= 1 && nrows <= kDecodeMaxRows) {
             const int L = min(max(a.cache_lens[b], 0), a.max_cache_len);
             units = (L + kBlock - 1) / kBlock;
         }
@@ -178,8 +181,10 @@ __global__ void __launch_bounds__(ScanCfg<H>::kThreads, 1) decode_scan_kernel(co
     // ---------------- consumer warp `warp` owns stage `warp`
     // B fragment of mma.m16n8k16 (col-major 16 x 8): lane (grp = lane/4,
     // tig = lane%4) holds B[2tig, 2tig+1][grp] and B[2tig+8, 2tig+9][grp].
-    // Column 0 is the index query, the other columns are zero, so the scores
-    // land in column 0 of the accumulator (lanes with tig == 0).
+    // Column i < n is the index query of the sequence's row i (the other
+    // columns are zero), so one pass over the index keys serves all its rows;
+    // accumulator lane (grp, tig) holds columns 2tig and 2tig+1 of positions
+    // 16mt + grp and 16mt + grp + 8.
     const int grp = lane >> 2, tig = lane & 3;
     int b = b0;
     ScanSeqState st;
@@ -187,18 +192,23 @@ __global__ void __launch_bounds__(ScanCfg<H>::kThreads, 1) decode_scan_kernel(co
     for (int i = warp; i < n; i += Cfg::kStages) {
         const int64_t u = u0 + i;
         scan_locate(a, prefix, u, b, st);
-        const uint32_t* q32 = reinterpret_cast<const uint32_t*>(a.iq + static_cast<int64_t>(st.r) * H * kIndexDim);
+        // this lane's B column: row grp of the sequence (if it exists)
+        const uint32_t* q32 = reinterpret_cast<const uint32_t*>(
+            a.iq + static_cast<int64_t>(st.r + (grp < st.n ? grp : 0)) * H * kIndexDim);
         const int j = static_cast<int>(u - prefix[b]);
-        const int npos = max(0, min(kBlock, st.L - j * kBlock));
+        // valid positions of this block for the lane's two columns (rows 2tig, 2tig+1
+        // at p = L - n + row): npos = p + 1 - 64 j, clamped to [0, 64]
+        const int last0 = st.L - st.n + 2 * tig + 1 - j * kBlock;
+        const int npos0 = 2 * tig < st.n ? max(0, min(kBlock, last0)) : 0;
+        const int npos1 = 2 * tig + 1 < st.n ? max(0, min(kBlock, last0 + 1)) : 0;
         if (!mbar_wait(&full[warp], (i / Cfg::kStages) & 1, a.err)) break;
-        float mine = -INFINITY;  // lane h < H keeps head h's block maximum
 #pragma unroll 1
         for (int h = 0; h < H; ++h) {
-            uint32_t bq[4][2];  // this head's index query as B fragments (L1-resident row)
+            uint32_t bq[4][2];  // this head's index queries as B fragments (L1-resident rows)
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
-                bq[kk][0] = grp == 0 ? __ldg(q32 + h * 32 + kk * 8 + tig) : 0u;
-                bq[kk][1] = grp == 0 ? __ldg(q32 + h * 32 + kk * 8 + 4 + tig) : 0u;
+                bq[kk][0] = grp < st.n ? __ldg(q32 + h * 32 + kk * 8 + tig) : 0u;
+                bq[kk][1] = grp < st.n ? __ldg(q32 + h * 32 + kk * 8 + 4 + tig) : 0u;
             }
             float c[4][4];
 #pragma unroll
@@ -214,22 +224,30 @@ __global__ void __launch_bounds__(ScanCfg<H>::kThreads, 1) decode_scan_kernel(co
                     ldsm_x4(stage + h * Cfg::kHeadBytes + row * 128 + ((chunk ^ (row & 7)) << 4), a0, a1, a2, a3);
                     mma_bf16_16816(c[mt], a0, a1, a2, a3, bq[kk][0], bq[kk][1]);
                 }
-            // column 0: c[mt][0] is position 16mt + grp, c[mt][2] is 16mt + grp + 8
-            float m = -INFINITY;
+            // block maxima of columns 2tig (m0) and 2tig+1 (m1) over the valid positions
+            float m0 = -INFINITY, m1 = -INFINITY;
 #pragma unroll
             for (int mt = 0; mt < 4; ++mt) {
-                if (mt * 16 + grp < npos) m = fmaxf(m, c[mt][0]);
-                if (mt * 16 + grp + 8 < npos) m = fmaxf(m, c[mt][2]);
+                const int t0 = mt * 16 + grp, t1 = t0 + 8;
+                if (t0 < npos0) m0 = fmaxf(m0, c[mt][0]);
+                if (t1 < npos0) m0 = fmaxf(m0, c[mt][2]);
+                if (t0 < npos1) m1 = fmaxf(m1, c[mt][1]);
+                if (t1 < npos1) m1 = fmaxf(m1, c[mt][3]);
             }
-            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
-            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
-            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
-            m = __shfl_sync(0xffffffffu, m, 0);
-            if (lane == h) mine = m;
+#pragma unroll
+            for (int o = 4; o < 32; o <<= 1) {
+                m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, o));
+                m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, o));
+            }
+            if (grp == 0) {  // lanes 0-3 store rows 2tig and 2tig+1
+                float* pooled = a.pooled + (static_cast<int64_t>(b) * a.rows_per_seq * H + h) * a.max_blocks + j;
+                const int64_t row_stride = static_cast<int64_t>(H) * a.max_blocks;
+                if (npos0 > 0) pooled[(2 * tig) * row_stride] = m0;
+                if (npos1 > 0) pooled[(2 * tig + 1) * row_stride] = m1;
+            }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[warp]);  // stage reusable
-        if (npos > 0 && lane < H) a.pooled[(static_cast<int64_t>(b) * H + lane) * a.max_blocks + j] = mine;
     }
 }
 

@@ -58,8 +58,9 @@ struct ScanArgs {
     int max_cache_len;
     int64_t cache_tokens;
     int max_blocks;
+    int rows_per_seq;     // RS = min(max_rows_per_seq, kDecodeMaxRows): pooled row slots per sequence
     int64_t unit_bound;   // upper bound of the number of work units
-    float* pooled;        // [B, H, max_blocks]
+    float* pooled;        // [B * RS, H, max_blocks]: slot b * RS + i = row i of sequence b
     int32_t* clear_words; // zeroed by the scan (tickets of the attention kernel)
     int n_clear;
     uint32_t* err;
@@ -69,8 +70,9 @@ struct DecodeAttendArgs {
     const CUtensorMap* k_map;  // host copies, passed by value to the kernel
     const CUtensorMap* v_map;
     const uint16_t* q;
-    const float* pooled;       // fused path: pooled scores (nullptr when sel is given)
+    const float* pooled;       // fused path: pooled scores [B * RS, H, max_blocks] (nullptr when sel is given)
     int max_blocks;
+    int rows_per_seq;          // RS: grid z = B * RS (sequence b, row i at z = b * RS + i)
     const int32_t* sel_in;     // staged path: given selection
     const int32_t* nsel_in;
     const int32_t* cu_rows;
@@ -123,7 +125,7 @@ struct PrefillAttendArgs {
     float scale_log2;
     void* out;
     int out_bf16;
-    int only_multi_row;  // 1: skip sequences with a single row (fused path)
+    int only_multi_row;  // 1: skip decode-family sequences (<= kDecodeMaxRows rows; fused path)
     uint32_t* err;
 };
 

@@ -62,8 +62,8 @@ msa_status check_problem(const msa_problem* p) {
     if (p->cache_tokens < 1 || p->cache_tokens > INT32_MAX) return fail(MSA_ERR_INVALID_ARG, "cache_tokens out of range");
     if (p->num_decode_seqs < -1 || p->num_decode_seqs > p->num_seqs)
         return fail(MSA_ERR_INVALID_ARG, "num_decode_seqs out of range");
-    if (p->max_rows_per_seq == 1 && p->num_decode_seqs != -1 && p->num_decode_seqs != p->num_seqs)
-        return fail(MSA_ERR_INVALID_ARG, "max_rows_per_seq == 1 implies num_decode_seqs == num_seqs");
+    if (p->max_rows_per_seq <= msa::kDecodeMaxRows && p->num_decode_seqs != -1 && p->num_decode_seqs != p->num_seqs)
+        return fail(MSA_ERR_INVALID_ARG, "max_rows_per_seq <= 8 implies num_decode_seqs == num_seqs");
     if (!p->cu_rows || !p->cache_lens) return fail(MSA_ERR_INVALID_ARG, "device metadata is null");
     if (!aligned16(p->cu_rows) && (reinterpret_cast<uintptr_t>(p->cu_rows) & 3u))
         return fail(MSA_ERR_INVALID_ARG, "cu_rows misaligned");
@@ -109,9 +109,15 @@ struct Layout {
     size_t header_bytes = 0;  // error word + tickets, cleared at the start of a call
 };
 
+// Pooled-score row slots per sequence of the decode family.
+size_t decode_rows_per_seq(const msa_problem* p) {
+    return static_cast<size_t>(p->max_rows_per_seq < msa::kDecodeMaxRows ? p->max_rows_per_seq : msa::kDecodeMaxRows);
+}
+
 Layout layout_of(const msa_problem* p) {
     Layout l;
     const size_t B = p->num_seqs, H = p->num_kv_heads, R = p->total_rows, K = p->top_k;
+    const size_t RS = decode_rows_per_seq(p);
     const size_t MB = (static_cast<size_t>(p->max_cache_len) + msa::kBlock - 1) / msa::kBlock;
     size_t off = 0;
     l.err = off;
@@ -121,7 +127,7 @@ Layout layout_of(const msa_problem* p) {
     l.header_bytes = off;
     off = align256(off);
     l.pooled = off;
-    off = align256(off + B * H * MB * sizeof(float));
+    off = align256(off + B * RS * H * MB * sizeof(float));
     l.partials = off;  // none: decode partials are combined on chip (thread-block clusters)
     l.sel = off;
     off = align256(off + R * H * K * sizeof(int32_t));
@@ -201,7 +207,7 @@ struct Marks {
 
 bool decode_family(const msa_problem* p) { return p->num_decode_seqs != 0; }
 bool prefill_family(const msa_problem* p) {
-    return p->max_rows_per_seq > 1 && p->num_decode_seqs != p->num_seqs;
+    return p->max_rows_per_seq > msa::kDecodeMaxRows && p->num_decode_seqs != p->num_seqs;
 }
 
 }  // namespace
@@ -324,6 +330,7 @@ static msa::DecodeAttendArgs decode_args(const msa_problem* p, const CUtensorMap
     a.v_map = vm;
     a.q = static_cast<const uint16_t*>(q);
     a.max_blocks = static_cast<int>((p->max_cache_len + msa::kBlock - 1) / msa::kBlock);
+    a.rows_per_seq = static_cast<int>(decode_rows_per_seq(p));
     a.cu_rows = p->cu_rows;
     a.cache_lens = p->cache_lens;
     a.cache = cache_rows_of(p);
@@ -350,8 +357,8 @@ msa_status msa_attend_decode(const msa_problem* p, const void* q, const void* k_
     Layout l;
     msa_status s = attend_common(p, q, k_cache, v_cache, sel, nsel, out, workspace, workspace_bytes, &l);
     if (s != MSA_OK) return s;
-    if (p->max_rows_per_seq != 1)
-        return fail(MSA_ERR_INVALID_ARG, "msa_attend_decode needs one row per sequence (max_rows_per_seq == 1)");
+    if (p->max_rows_per_seq > msa::kDecodeMaxRows)
+        return fail(MSA_ERR_INVALID_ARG, "msa_attend_decode needs at most 8 rows per sequence (max_rows_per_seq <= 8)");
     const uint64_t T = p->cache_tokens, H = p->num_kv_heads;
     CUtensorMap km, vm;
     if ((s = make_map(&km, k_cache, 128, H, T, 64, 1, 64, "k_cache")) != MSA_OK) return s;
@@ -513,6 +520,7 @@ msa_status msa_forward_marked(const msa_problem* p, const void* q, const void* i
         sa.max_cache_len = p->max_cache_len;
         sa.cache_tokens = p->cache_tokens;
         sa.max_blocks = max_blocks;
+        sa.rows_per_seq = static_cast<int>(decode_rows_per_seq(p));
         const int64_t nd = p->num_decode_seqs >= 0 ? p->num_decode_seqs : p->num_seqs;
         sa.unit_bound = nd * max_blocks;
         sa.pooled = reinterpret_cast<float*>(ws + l.pooled);

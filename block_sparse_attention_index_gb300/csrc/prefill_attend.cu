@@ -98,8 +98,8 @@ struct Item {
     int row[kMaxTopK];
 };
 
-// Decodes work item `it`; false when the item is skipped (a row of a decode
-// sequence on the fused path, or inconsistent metadata / selection).
+// Decodes work item `it`; false when the item is skipped (a row of a
+// decode-family sequence on the fused path, or inconsistent metadata / selection).
 __device__ bool load_item(const PrefillAttendArgs& a, int it, Item& x, bool& bad) {
     bad = false;
     x.r = it / a.H;
@@ -111,7 +111,7 @@ __device__ bool load_item(const PrefillAttendArgs& a, int it, Item& x, bool& bad
     }
     const int b = lo;
     const int n = a.cu_rows[b + 1] - a.cu_rows[b];
-    if (a.only_multi_row && n <= 1) return false;
+    if (a.only_multi_row && n <= kDecodeMaxRows) return false;  // taken by the decode kernels
     const int L = a.cache_lens[b];
     x.b = b;
     x.p = L - n + (x.r - a.cu_rows[b]);

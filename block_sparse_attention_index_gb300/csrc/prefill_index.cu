@@ -44,13 +44,13 @@ struct __align__(1024) IndexSmem {
 };
 
 // Which (sequence, row tile) CTA `tile` handles; false when beyond the end.
-// Tiles of a sequence with n rows (n > 1, or any n when !only_multi):
+// Tiles of a sequence with n rows (n > kDecodeMaxRows):
 // ceil(n / 128).  Walks the sequences (num_seqs is small).
 __device__ bool find_tile(const PrefillIndexArgs& a, int tile, int& b, int& i0, int& n) {
     int acc = 0;
     for (int s = 0; s < a.num_seqs; ++s) {
         const int rows = a.cu_rows[s + 1] - a.cu_rows[s];
-        if (rows <= 1) continue;
+        if (rows <= kDecodeMaxRows) continue;  // the decode kernels take these
         const int t = (rows + kIdxRows - 1) / kIdxRows;
         if (tile < acc + t) {
             b = s;

@@ -93,12 +93,13 @@ typedef struct msa_problem {
     float softmax_scale;      /* finite, >= 0; typically 1/sqrt(D)             */
     int32_t out_dtype;        /* MSA_OUT_F32 or MSA_OUT_BF16                   */
     int32_t total_rows;       /* R = cu_rows[B] (host copy)                    */
-    int32_t max_rows_per_seq; /* >= every n_b (host bound); 1 = pure decode    */
+    int32_t max_rows_per_seq; /* >= every n_b (host bound); <= 8 = decode family only */
     int32_t max_cache_len;    /* >= every L_b (host bound)                     */
     int64_t cache_tokens;     /* rows in each of k, v, ik (host), < 2^31       */
-    int32_t num_decode_seqs;  /* host count of sequences with exactly one row,
-                                 or -1 if unknown (then both kernel families
-                                 run and each skips the other's sequences)   */
+    int32_t num_decode_seqs;  /* host count of decode-family sequences (1 to 8
+                                 rows), or -1 if unknown (then both kernel
+                                 families run and each skips the other's
+                                 sequences)                                   */
     const int32_t* cu_rows;      /* device [B+1], cu_rows[0] = 0, ascending    */
     const int32_t* cache_lens;   /* device [B], 1 <= L_b <= max_cache_len      */
     const int64_t* cache_starts; /* device [B], start + L_b <= cache_tokens;
@@ -147,8 +148,9 @@ msa_status msa_index_scores(const msa_problem* p, const void* iq, const void* ik
 msa_status msa_select_blocks(const msa_problem* p, const float* scores, int64_t ld,
                              int32_t* sel, int32_t* nsel, void* stream);
 
-/* Stage 3, decode form: every sequence has exactly one row
- * (max_rows_per_seq == 1).  The kept blocks of one (sequence, KV head) are
+/* Stage 3, decode form: every sequence has 1 to 8 rows
+ * (max_rows_per_seq <= 8), e.g. one decode row or a drafted window.  The
+ * kept blocks of one (row, KV head) are
  * split over a cluster of 8 CTAs (two blocks each); their partial softmax
  * states (running max, sum, unnormalised output) are combined by
  * log-sum-exp on chip, through distributed shared memory.  sel/nsel as msa_select_blocks
@@ -189,9 +191,11 @@ msa_status msa_attend_prefill(const msa_problem* p, const void* q, const void* k
                               void* out, void* workspace, size_t workspace_bytes, void* stream);
 
 /* The fused hot path: all three stages for every row of the batch.
- * Sequences with one row take the decode kernels (index-key scan with the
- * block max-pool fused in, then selection + split attention + combine);
- * sequences with more rows take the prompt-chunk kernels (tcgen05 indexer
+ * Sequences with 1 to 8 rows (the decode family: decode rows, drafted
+ * windows) take the decode kernels (index-key scan with the block max-pool
+ * fused in, one pass over the index keys for all of a sequence's rows, then
+ * selection + split attention + combine per row); sequences with more rows
+ * take the prompt-chunk kernels (tcgen05 indexer
  * with the pool and a running top-k in its epilogue, then tcgen05
  * attention).  No scores are materialised.  sel_out/nsel_out (nullable)
  * receive the selection. */

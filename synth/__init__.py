@@ -265,6 +265,9 @@ WORKLOADS = {
                                         note="long-context decode, 262,144 cached tokens"),
     "mixed_8dec_512pre": lambda: Workload("mixed_8dec_512pre", H=4, G=16, seqs=_c5_seqs(0),
                                           note="8 ragged decode rows (log-uniform 1,024..196,608) + a 512-row chunk at 32,768"),
+    # beyond the five configurations: drafted windows (several decode rows per sequence)
+    "decode_4x4_65536": lambda: Workload("decode_4x4_65536", H=4, G=16, seqs=[(4, 65536)] * 4,
+                                         note="drafted windows: 4 sequences x 4 rows, 65,536 cached tokens each"),
 }
 
 

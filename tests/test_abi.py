@@ -61,6 +61,7 @@ def _problem(**over):
     (dict(out_dtype=7), 1), (dict(total_rows=0), 1), (dict(max_rows_per_seq=2), 1),
     (dict(max_cache_len=(1 << 21) + 1), 2), (dict(cache_tokens=0), 1), (dict(num_decode_seqs=2), 1),
     (dict(cu_rows=None), 1), (dict(cache_starts=260), 1), (dict(cache_starts=None), 1),
+    (dict(num_seqs=2, max_rows_per_seq=8, total_rows=9, num_decode_seqs=1), 1),  # <= 8 rows: all decode family
     # paged caches: page size a power of two >= 64, pool a whole number of pages,
     # table wide enough for max_cache_len, table aligned
     (dict(cache_starts=None, block_table=1024, block_table_stride=64, page_size=32), 2),
@@ -98,9 +99,12 @@ def test_workspace_size_and_pointer_checks():
     assert L.msa_attend_decode(C.byref(pb2), fake, fake, fake, None, fake, fake, ws, 1 << 30, None) == 1
     assert L.msa_index_scores(C.byref(pb), fake, fake, fake, 100, None) == 1  # ld < max_cache_len
     assert L.msa_forward_launches(C.byref(pb)) == 2
-    assert L.msa_forward_launches(C.byref(_problem(max_rows_per_seq=4, total_rows=4, num_decode_seqs=0))) == 2
-    assert L.msa_forward_launches(C.byref(_problem(num_seqs=2, max_rows_per_seq=4, total_rows=5,
+    assert L.msa_forward_launches(C.byref(_problem(max_rows_per_seq=12, total_rows=12, num_decode_seqs=0))) == 2
+    assert L.msa_forward_launches(C.byref(_problem(num_seqs=2, max_rows_per_seq=9, total_rows=10,
                                                    num_decode_seqs=1))) == 4
+    # up to 8 rows per sequence is the decode family alone
+    assert L.msa_forward_launches(C.byref(_problem(num_seqs=2, max_rows_per_seq=8, total_rows=9,
+                                                   num_decode_seqs=2))) == 2
 
 
 def test_paged_problem_accepted_on_host():
