@@ -25,6 +25,7 @@ class _Problem(C.Structure):
         ("num_seqs", C.c_int32), ("H", C.c_int32), ("G", C.c_int32), ("D", C.c_int32),
         ("Di", C.c_int32), ("S", C.c_int32), ("top_k", C.c_int32), ("scale", C.c_double),
         ("cu_rows", C.c_void_p), ("cache_lens", C.c_void_p), ("cache_starts", C.c_void_p),
+        ("ik_heads", C.c_int32),
     ]
 
 
@@ -57,19 +58,21 @@ def _ptr(a):
 class Problem:
     """Shape and metadata of one MSA problem (arrays are kept alive here)."""
 
-    def __init__(self, H, G, cu_rows, cache_lens, cache_starts, D=128, Di=64, S=64, top_k=16, scale=None):
+    def __init__(self, H, G, cu_rows, cache_lens, cache_starts, D=128, Di=64, S=64, top_k=16, scale=None,
+                 ik_heads=None):
         self.cu_rows = np.ascontiguousarray(cu_rows, dtype=np.int32)
         self.cache_lens = np.ascontiguousarray(cache_lens, dtype=np.int32)
         self.cache_starts = np.ascontiguousarray(cache_starts, dtype=np.int64)
         self.H, self.G, self.D, self.Di, self.S, self.top_k = H, G, D, Di, S, top_k
         self.scale = scale if scale is not None else 1.0 / np.sqrt(D)
+        self.ik_heads = H if ik_heads is None else ik_heads  # 1: one index key shared by all KV heads
         self.c = _Problem(len(self.cache_lens), H, G, D, Di, S, top_k, self.scale,
-                          _ptr(self.cu_rows), _ptr(self.cache_lens), _ptr(self.cache_starts))
+                          _ptr(self.cu_rows), _ptr(self.cache_lens), _ptr(self.cache_starts), self.ik_heads)
 
     @classmethod
     def from_workload(cls, w, x):
         return cls(w.H, w.G, x["cu_rows"], x["cache_lens"], x["cache_starts"], D=w.D, Di=w.Di,
-                   S=w.S, top_k=w.top_k, scale=w.softmax_scale)
+                   S=w.S, top_k=w.top_k, scale=w.softmax_scale, ik_heads=int(x["ik"].shape[1]))
 
     @property
     def total_rows(self):

@@ -37,6 +37,13 @@
  *
  * Layouts (contiguous): q [R, H*G, D], iq [R, H, Di], k/v [T, H, D],
  * ik [T, H, Di]; token t of sequence b is cache row cache_starts[b] + t.
+ *
+ * Shared index key (ik_heads = 1): ik is [T, 1, Di] and every KV head's
+ * index query meets the same key, s_t = sum_d iq[r,h,d] * ik[t,0,d].  The
+ * pages print no formula for it; their cache arithmetic (MiniMax-M3 PR
+ * #1388, commit removing the int8 cache: 135 KiB of cache a token) leaves
+ * room for fewer index keys than one per KV head, and this is the plain
+ * reading of one key per position for all heads.
  * Rows of sequence b are cu_rows[b] .. cu_rows[b+1]-1; with n rows and cache
  * length L, row i sits at p = L - n + i.
  */
@@ -60,6 +67,7 @@ typedef struct oracle_problem {
     const int32_t* cu_rows;      /* [num_seqs + 1] */
     const int32_t* cache_lens;   /* [num_seqs] */
     const int64_t* cache_starts; /* [num_seqs] */
+    int32_t ik_heads;            /* index keys per position: H, or 1 (shared); 0 means H */
 } oracle_problem;
 
 static double widen_bf16(uint16_t b) {
@@ -91,7 +99,8 @@ int oracle_index_scores(const oracle_problem* pr, const uint16_t* iq, const uint
     if (b < 0 || p < 0 || p + 1 > cap) return -1;
     const uint16_t* qi = iq + (r * pr->H + h) * (int64_t)pr->Di;
     for (int64_t t = 0; t <= p; ++t) {
-        const uint16_t* ki = ik + ((pr->cache_starts[b] + t) * pr->H + h) * (int64_t)pr->Di;
+        const int kh = pr->ik_heads == 1 ? 1 : pr->H; /* index-key heads per position */
+        const uint16_t* ki = ik + ((pr->cache_starts[b] + t) * kh + (kh == 1 ? 0 : h)) * (int64_t)pr->Di;
         double acc = 0.0;
         for (int d = 0; d < pr->Di; ++d) acc += widen_bf16(qi[d]) * widen_bf16(ki[d]);
         s[t] = acc;

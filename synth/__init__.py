@@ -164,6 +164,7 @@ class Workload:
     scale: float | None = None
     note: str = ""
     extra: dict = field(default_factory=dict)
+    ik_heads: int = 0  # index keys per position: 0 = one per KV head, 1 = one shared by all heads
 
     @property
     def softmax_scale(self) -> float:
@@ -200,7 +201,7 @@ def make_inputs(w: Workload, with_kv: bool = True) -> dict:
         cache_starts=starts,
         q=normal_bf16(w.seed, STREAM_Q, (R, w.H * w.G, w.D)),
         iq=int_bf16(w.seed, STREAM_IQ, (R, w.H, w.Di)),
-        ik=int_bf16(w.seed, STREAM_IK, (T, w.H, w.Di)),
+        ik=int_bf16(w.seed, STREAM_IK, (T, 1 if w.ik_heads == 1 else w.H, w.Di)),
     )
     if with_kv:
         out["k"] = normal_bf16(w.seed, STREAM_K, (T, w.H, w.D))

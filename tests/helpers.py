@@ -128,6 +128,37 @@ def check_scores_integer_matmul(lib_path=None):
             assert np.array_equal(s, ref.astype(np.float64)), (r, h)
 
 
+def check_shared_key_integer_matmul(lib_path=None):
+    """One index key per position shared by every KV head: each head's scores
+    equal numpy's exact int64 matmul of the shared keys with its own query."""
+    w = synth.Workload("mm_shared", H=4, G=1, seqs=[(2, 130), (1, 77)], seed=12, ik_heads=1)
+    x = synth.make_inputs(w, with_kv=False)
+    assert x["ik"].shape[1] == 1
+    pr = oracle.Problem.from_workload(w, x)
+    iq = to_f64(x["iq"]).astype(np.int64)
+    ik = to_f64(x["ik"]).astype(np.int64)
+    for r in range(3):
+        b, p = pr.position(r)
+        start = int(x["cache_starts"][b])
+        for h in range(4):
+            ref = ik[start:start + p + 1, 0, :] @ iq[r, h, :]
+            s = oracle.index_scores(pr, x["iq"], x["ik"], r, h, lib_path=lib_path)
+            assert np.array_equal(s, ref.astype(np.float64)), (r, h)
+
+
+def check_shared_key_equals_replicated(lib_path=None):
+    """A shared index key gives exactly the per-head result with that key
+    copied into every head."""
+    w = synth.Workload("shared_rep", H=3, G=2, seqs=[(1, 2000), (5, 700)], seed=13, ik_heads=1, top_k=6)
+    x = synth.make_inputs(w)
+    ref = oracle.forward(oracle.Problem.from_workload(w, x), x, lib_path=lib_path)
+    x_rep = dict(x)
+    x_rep["ik"] = np.ascontiguousarray(np.repeat(x["ik"], w.H, axis=1))
+    rep = oracle.forward(oracle.Problem.from_workload(w, x_rep), x_rep, lib_path=lib_path)
+    assert np.array_equal(ref["sel"], rep["sel"]) and np.array_equal(ref["nsel"], rep["nsel"])
+    assert np.array_equal(ref["out"], rep["out"])
+
+
 def _dense_reference(w, x, r, h):
     """Dense causal attention of row r, KV head h, over all keys t <= p, by
     torch's scaled_dot_product_attention in float64 (math path on CPU)."""
@@ -288,5 +319,6 @@ ALL_CHECKS = [
     check_select_golden, check_select_golden_through_forward, check_pool_golden, check_scores_unit_query,
     check_scores_integer_matmul, check_dense_special_case, check_explicit_selection, check_two_key_closed_form,
     check_constant_values, check_single_key, check_zero_scale_is_mean, check_select_bruteforce,
-    check_select_invariants, check_future_blocks_never_selected,
+    check_select_invariants, check_future_blocks_never_selected, check_shared_key_integer_matmul,
+    check_shared_key_equals_replicated,
 ]

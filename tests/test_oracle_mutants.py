@@ -20,7 +20,7 @@ MUTANTS = {
     "flip_tie_break": [("return (x->j < y->j) ? -1 : (x->j > y->j);", "return (x->j > y->j) ? -1 : (x->j < y->j);")],
     "no_causal_rows": [("*p_out = (int64_t)pr->cache_lens[b] - n + i;", "*p_out = (int64_t)pr->cache_lens[b] - 1 + 0 * (n + i);")],
     "unscaled_logits": [("x[i] = pr->scale * acc;", "x[i] = acc;")],
-    "wrong_index_key_head": [("ik + ((pr->cache_starts[b] + t) * pr->H + h)", "ik + ((pr->cache_starts[b] + t) * pr->H + 0)")],
+    "wrong_index_key_head": [("* kh + (kh == 1 ? 0 : h))", "* kh + 0)")],
     "unnormalised_output": [("o[d] = nk > 0 ? o[d] / den : 0.0;", "o[d] = nk > 0 ? o[d] : 0.0;")],
     "last_not_max_pool": [("if (s[t] > best) best = s[t];", "best = s[t];")],
     "values_from_keys": [("const uint16_t* vt = v + ", "const uint16_t* vt = k + ")],
