@@ -66,7 +66,8 @@ def work_counts(w: synth.Workload):
     pre = [(n, L) for n, L in w.seqs if n > DECODE_MAX_ROWS]
     # decode scan: every cached index key once (shared by the sequence's rows), the
     # index queries, the pooled scores out
-    scan_bytes = sum(L * H * Di * 2 + n * H * Di * 2 + n * ((L + 63) // 64) * H * 4 for n, L in dec)
+    kh = 1 if w.ik_heads == 1 else H  # index-key heads per position
+    scan_bytes = sum(L * kh * Di * 2 + n * H * Di * 2 + n * ((L + 63) // 64) * H * 4 for n, L in dec)
     # decode attention: kept K/V blocks, q in, out (fp32) out, per row
     att_bytes = sum(H * (_kept_keys(L - n + i, w.top_k) * D * 2 * 2) + H * G * D * (2 + 4)
                     for n, L in dec for i in range(n))
@@ -211,11 +212,11 @@ def measure_gpu(w, steps, warmup, dev, dist_on, flush_bytes=512 << 20, e2e_steps
         dx.update({k: _to_dev(pl[k], dev) for k in ("k", "v", "ik")})
         pb = msa.Problem(w.H, w.G, w.seqs, dev, top_k=w.top_k, scale=w.softmax_scale,
                          block_table=torch.from_numpy(pl["table"]), page_size=page_size,
-                         cache_tokens=pl["num_pages"] * page_size)
+                         cache_tokens=pl["num_pages"] * page_size, ik_heads=w.ik_heads)
         with_e2e = False
     else:
         dx = {k: _to_dev(x[k], dev) for k in ("q", "iq", "k", "v", "ik")}
-        pb = msa.Problem(w.H, w.G, w.seqs, dev, top_k=w.top_k, scale=w.softmax_scale)
+        pb = msa.Problem(w.H, w.G, w.seqs, dev, top_k=w.top_k, scale=w.softmax_scale, ik_heads=w.ik_heads)
     ws = pb.workspace()
     out = pb.new_out()
     sel, nsel = pb.new_sel()
@@ -439,6 +440,8 @@ def main():
     ap.add_argument("--no-graph", action="store_true", help="launch each step directly instead of replaying a CUDA graph")
     ap.add_argument("--multirow", default="decode_4x4_65536",
                     help="decode workload with several rows per sequence measured in the same run ('none' to skip)")
+    ap.add_argument("--shared-key", default="decode_4x65536_shared_ik",
+                    help="decode workload with one index key shared by all KV heads ('none' to skip)")
     ap.add_argument("--paged-page-size", type=int, default=64,
                     help="also time the primary workload from a paged cache with this page size (0: skip)")
     args = ap.parse_args()
@@ -528,6 +531,18 @@ def main():
                          "unit": "rows/s", "ms_per_step": round(resp["ms_per_step"], 5),
                          "note": "same inputs from a shuffled page pool addressed through a block table"}
         line["gpu_launches"] += resp["launches"]
+    for key, name in (("shared_key", args.shared_key),):
+        if name == "none" or name == args.workload:
+            continue
+        w4 = synth.workload(name)
+        res4 = measure_gpu(w4, args.steps, args.warmup, dev, dist_on, with_e2e=False, use_graph=not args.no_graph)
+        line[key] = {"metric": _metric_for(w4), "workload": w4.name,
+                     "value": round(whole_job_rate(w4.total_rows, ws, res4["ms_per_step"]), 1),
+                     "unit": "rows/s", "ms_per_step": round(res4["ms_per_step"], 5),
+                     "stage_us": {"decode_scan": round(res4["stage_ms"][0] * 1e3, 2),
+                                  "decode_attend": round(res4["stage_ms"][1] * 1e3, 2)},
+                     "roofline": roofline_for(w4, res4, hbm, bf16, bf16_sus, peak_kind), "note": w4.note}
+        line["gpu_launches"] += res4["launches"]
     if args.multirow != "none" and args.multirow != args.workload:
         w3 = synth.workload(args.multirow)
         res3 = measure_gpu(w3, args.steps, args.warmup, dev, dist_on, with_e2e=False, use_graph=not args.no_graph)

@@ -39,7 +39,7 @@ class MsaProblem(C.Structure):
         ("max_rows_per_seq", C.c_int32), ("max_cache_len", C.c_int32), ("cache_tokens", C.c_int64),
         ("num_decode_seqs", C.c_int32), ("cu_rows", C.c_void_p), ("cache_lens", C.c_void_p),
         ("cache_starts", C.c_void_p), ("block_table", C.c_void_p), ("block_table_stride", C.c_int32),
-        ("page_size", C.c_int32),
+        ("page_size", C.c_int32), ("index_key_heads", C.c_int32),
     ]
 
 
@@ -120,12 +120,13 @@ class Problem:
     cache_lens, cache_starts) is built from it on `device` with the caches
     packed in sequence order unless cache_starts is given.  Paged caches:
     block_table ([B, stride] int32 page numbers, tensor or nested list) and
-    page_size, with cache_tokens = rows of the page pool.
+    page_size, with cache_tokens = rows of the page pool.  ik_heads=1: one
+    index key per position shared by every KV head (ik is [T, 1, Di]).
     """
 
     def __init__(self, H, G, seqs_host, device, top_k=16, scale=None, out_dtype=torch.float32,
                  cache_starts=None, cache_tokens=None, D=128, Di=64, S=64, num_decode_seqs="auto",
-                 block_table=None, page_size=0):
+                 block_table=None, page_size=0, ik_heads=0):
         self.H, self.G, self.D, self.Di, self.S, self.top_k = H, G, D, Di, S, top_k
         self.device = torch.device(device)
         if self.device.type == "cuda" and self.device.index is None:
@@ -166,7 +167,8 @@ class Problem:
             self.cu_rows.data_ptr(), self.cache_lens.data_ptr(),
             self.cache_starts.data_ptr() if self.block_table is None else None,
             None if self.block_table is None else self.block_table.data_ptr(),
-            0 if self.block_table is None else int(self.block_table.shape[1]), int(page_size))
+            0 if self.block_table is None else int(self.block_table.shape[1]), int(page_size), int(ik_heads))
+        self.KH = 1 if (ik_heads == 1 or H == 1) else H  # index-key heads per position
 
     @property
     def max_cache_len(self):
@@ -198,8 +200,8 @@ class Problem:
     def _check_iq(self, iq):
         _need(iq, "iq", torch.bfloat16, self.device, (self.total_rows, self.H, self.Di))
 
-    def _check_cache(self, t, name, width):
-        _need(t, name, torch.bfloat16, self.device, (self.cache_tokens, self.H, width))
+    def _check_cache(self, t, name, width, heads=None):
+        _need(t, name, torch.bfloat16, self.device, (self.cache_tokens, self.H if heads is None else heads, width))
 
     def _check_sel(self, sel, nsel):
         _need(sel, "sel", torch.int32, self.device, (self.total_rows, self.H, self.top_k))
@@ -209,7 +211,7 @@ class Problem:
 def index_scores(pb: Problem, iq, ik, ld=None):
     """msa_index_scores: [R, H, ld] fp32 scores (-inf past each row)."""
     pb._check_iq(iq)
-    pb._check_cache(ik, "ik", pb.Di)
+    pb._check_cache(ik, "ik", pb.Di, pb.KH)
     ld = ld or ((pb.max_cache_len + 3) // 4 * 4)
     scores = torch.empty(pb.total_rows, pb.H, ld, dtype=torch.float32, device=pb.device)
     _check(_lib.msa_index_scores(C.byref(pb.c), _ptr(iq), _ptr(ik), _ptr(scores), ld, _stream(pb.device)))
@@ -273,7 +275,7 @@ def forward(pb: Problem, q, iq, k, v, ik, out=None, sel=None, nsel=None, workspa
     pb._check_iq(iq)
     pb._check_cache(k, "k", pb.D)
     pb._check_cache(v, "v", pb.D)
-    pb._check_cache(ik, "ik", pb.Di)
+    pb._check_cache(ik, "ik", pb.Di, pb.KH)
     out = pb.new_out() if out is None else out
     _need(out, "out", pb.out_dtype, pb.device, (pb.total_rows, pb.H * pb.G, pb.D))
     if sel is None:

@@ -27,11 +27,14 @@
 
 namespace msa {
 
-template <int H>
+// kShared: one index key per position for all heads (a unit is one 8 KB box,
+// read once for the H heads' queries), else one key per head (H boxes).
+template <int H, bool kShared>
 struct ScanCfg {
     static constexpr int kHeadBytes = kBlock * kIndexDim * 2;                 // 8 KB: [64 pos][64 dims]
-    static constexpr int kUnitBytes = H * kHeadBytes;
-    static constexpr int kStages = (H == 8) ? 3 : 6;                          // <= 192 KB of ring
+    static constexpr int kKeyHeads = kShared ? 1 : H;
+    static constexpr int kUnitBytes = kKeyHeads * kHeadBytes;
+    static constexpr int kStages = kShared ? 16 : ((H == 8) ? 3 : 6);         // <= 192 KB of ring
     static constexpr int kConsumers = kStages;                                // one warp per stage
     static constexpr int kThreads = 32 * (kConsumers + 1);                    // + producer warp
 };
@@ -73,10 +76,10 @@ __device__ __forceinline__ bool scan_locate(const ScanArgs& a, const int32_t* pr
     return false;
 }
 
-template <int H>
-__global__ void __launch_bounds__(ScanCfg<H>::kThreads, 1) decode_scan_kernel(const __grid_constant__ CUtensorMap ik_map,
+template <int H, bool kShared>
+__global__ void __launch_bounds__(ScanCfg<H, kShared>::kThreads, 1) decode_scan_kernel(const __grid_constant__ CUtensorMap ik_map,
                                                                              const ScanArgs a) {
-    using Cfg = ScanCfg<H>;
+    using Cfg = ScanCfg<H, kShared>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* full = reinterpret_cast<uint64_t*>(ring + Cfg::kStages * Cfg::kUnitBytes);
@@ -168,7 +171,7 @@ __global__ void __launch_bounds__(ScanCfg<H>::kThreads, 1) decode_scan_kernel(co
                     }
                     const int tok = static_cast<int>(row);
 #pragma unroll
-                    for (int h = 0; h < H; ++h)
+                    for (int h = 0; h < Cfg::kKeyHeads; ++h)
                         tma_load_3d(ring + s * Cfg::kUnitBytes + h * Cfg::kHeadBytes, &ik_map, &full[s], 0, h, tok);
                 } else {
                     mbar_arrive_expect_tx(&full[s], 0);
@@ -221,7 +224,8 @@ __global__ void __launch_bounds__(ScanCfg<H>::kThreads, 1) decode_scan_kernel(co
                     const int row = mt * 16 + (mi & 1) * 8 + (lane & 7);
                     const int chunk = kk * 2 + (mi >> 1);
                     uint32_t a0, a1, a2, a3;
-                    ldsm_x4(stage + h * Cfg::kHeadBytes + row * 128 + ((chunk ^ (row & 7)) << 4), a0, a1, a2, a3);
+                    ldsm_x4(stage + (kShared ? 0 : h) * Cfg::kHeadBytes + row * 128 + ((chunk ^ (row & 7)) << 4), a0,
+                            a1, a2, a3);
                     mma_bf16_16816(c[mt], a0, a1, a2, a3, bq[kk][0], bq[kk][1]);
                 }
             // block maxima of columns 2tig (m0) and 2tig+1 (m1) over the valid positions
@@ -251,25 +255,25 @@ __global__ void __launch_bounds__(ScanCfg<H>::kThreads, 1) decode_scan_kernel(co
     }
 }
 
-template <int H>
+template <int H, bool kShared>
 static cudaError_t launch_scan(const ScanArgs& a, cudaStream_t stream) {
-    using Cfg = ScanCfg<H>;
+    using Cfg = ScanCfg<H, kShared>;
     const size_t smem = 1024 + static_cast<size_t>(Cfg::kStages) * Cfg::kUnitBytes + 2 * Cfg::kStages * sizeof(uint64_t) +
                         static_cast<size_t>(a.num_seqs + 1) * sizeof(int32_t);
-    cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(decode_scan_kernel<H>), smem);
+    cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(decode_scan_kernel<H, kShared>), smem);
     if (e != cudaSuccess) return e;
     int64_t grid = device_sm_count();
     if (a.unit_bound < grid) grid = a.unit_bound > 0 ? a.unit_bound : 1;
-    decode_scan_kernel<H><<<static_cast<unsigned>(grid), Cfg::kThreads, smem, stream>>>(*a.ik_map, a);
+    decode_scan_kernel<H, kShared><<<static_cast<unsigned>(grid), Cfg::kThreads, smem, stream>>>(*a.ik_map, a);
     return cudaGetLastError();
 }
 
 cudaError_t run_decode_scan(const ScanArgs& a, cudaStream_t stream) {
     switch (a.H) {
-        case 1: return launch_scan<1>(a, stream);
-        case 2: return launch_scan<2>(a, stream);
-        case 4: return launch_scan<4>(a, stream);
-        case 8: return launch_scan<8>(a, stream);
+        case 1: return launch_scan<1, false>(a, stream);
+        case 2: return a.ik_shared ? launch_scan<2, true>(a, stream) : launch_scan<2, false>(a, stream);
+        case 4: return a.ik_shared ? launch_scan<4, true>(a, stream) : launch_scan<4, false>(a, stream);
+        case 8: return a.ik_shared ? launch_scan<8, true>(a, stream) : launch_scan<8, false>(a, stream);
         default: return cudaErrorInvalidValue;
     }
 }

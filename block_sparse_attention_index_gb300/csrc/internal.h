@@ -46,8 +46,9 @@ __device__ __forceinline__ bool seq_rows_ok(const CacheRows& c, int b, int L, in
 constexpr int kPartialFloats = 16 * 128 + 16 + 16;
 
 struct ScanArgs {
-    const CUtensorMap* ik_map;  // ik as (Di, H, tokens), box 64 x 1 x 64, host copy
+    const CUtensorMap* ik_map;  // ik as (Di, KH, tokens), box 64 x 1 x 64, host copy
     int H;
+    int ik_shared;              // 1: one index key per position for all heads (KH = 1), else KH = H
     const uint16_t* iq;
     const uint16_t* ik;
     const int32_t* cu_rows;
@@ -92,6 +93,7 @@ struct DecodeAttendArgs {
 
 struct StagedArgs {
     int H, G, top_k, num_seqs, total_rows, max_cache_len;
+    int ik_shared;  // index keys per position: 1 (shared) or H
     int64_t cache_tokens;
     const int32_t* cu_rows;
     const int32_t* cache_lens;
@@ -100,7 +102,8 @@ struct StagedArgs {
 
 struct PrefillIndexArgs {
     const CUtensorMap* iq_map;  // iq as (Di, H, rows)
-    const CUtensorMap* ik_map;  // ik as (Di, H, tokens), box 64 x 1 x 256 (64 x 1 x 64 when paged)
+    const CUtensorMap* ik_map;  // ik as (Di, KH, tokens), box 64 x 1 x 256 (64 x 1 x 64 when paged)
+    int ik_shared;              // KH = 1: every head reads key head 0
     const int32_t* cu_rows;
     const int32_t* cache_lens;
     CacheRows cache;

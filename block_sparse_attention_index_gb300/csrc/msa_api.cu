@@ -67,6 +67,8 @@ msa_status check_problem(const msa_problem* p) {
     if (!p->cu_rows || !p->cache_lens) return fail(MSA_ERR_INVALID_ARG, "device metadata is null");
     if (!aligned16(p->cu_rows) && (reinterpret_cast<uintptr_t>(p->cu_rows) & 3u))
         return fail(MSA_ERR_INVALID_ARG, "cu_rows misaligned");
+    if (p->index_key_heads != 0 && p->index_key_heads != 1 && p->index_key_heads != H)
+        return fail(MSA_ERR_INVALID_ARG, "index_key_heads must be 0, 1 or num_kv_heads (got %d)", p->index_key_heads);
     if (p->block_table == nullptr) {
         if (!p->cache_starts) return fail(MSA_ERR_INVALID_ARG, "cache_starts is null (and no block table)");
         if (reinterpret_cast<uintptr_t>(p->cache_starts) & 7u) return fail(MSA_ERR_INVALID_ARG, "cache_starts misaligned");
@@ -89,6 +91,9 @@ msa_status check_ptr(const void* ptr, const char* name) {
 }
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// 1 when one index key per position serves every KV head.
+int ik_shared(const msa_problem* p) { return p->index_key_heads == 1 && p->num_kv_heads > 1 ? 1 : 0; }
 
 msa::CacheRows cache_rows_of(const msa_problem* p) {
     msa::CacheRows c{};
@@ -177,6 +182,7 @@ msa::StagedArgs staged_args(const msa_problem* p) {
     a.total_rows = p->total_rows;
     a.max_cache_len = p->max_cache_len;
     a.cache_tokens = p->cache_tokens;
+    a.ik_shared = ik_shared(p);
     a.cu_rows = p->cu_rows;
     a.cache_lens = p->cache_lens;
     a.cache = cache_rows_of(p);
@@ -492,6 +498,7 @@ msa_status msa_forward_marked(const msa_problem* p, const void* q, const void* i
     int32_t* sel = sel_out ? sel_out : reinterpret_cast<int32_t*>(ws + l.sel);
     int32_t* nsel = nsel_out ? nsel_out : reinterpret_cast<int32_t*>(ws + l.nsel);
     const uint64_t T = p->cache_tokens, H = p->num_kv_heads;
+    const uint64_t KH = ik_shared(p) ? 1 : H;  // index-key heads per position
     const int max_blocks = static_cast<int>((p->max_cache_len + msa::kBlock - 1) / msa::kBlock);
 
     CUtensorMap km, vm, qm, iqm, ikm;
@@ -500,16 +507,17 @@ msa_status msa_forward_marked(const msa_problem* p, const void* q, const void* i
         if ((s = make_map(&iqm, iq, 64, H, p->total_rows, 64, 1, 128, "iq")) != MSA_OK) return s;
         // a whole 256-position tile per box, or one box per 64-position block when paged
         const uint32_t box = p->block_table == nullptr ? 256 : 64;
-        if ((s = make_map(&ikm, ik_cache, 64, H, T, 64, 1, box, "ik_cache")) != MSA_OK) return s;
+        if ((s = make_map(&ikm, ik_cache, 64, KH, T, 64, 1, box, "ik_cache")) != MSA_OK) return s;
     }
     CUtensorMap ik_scan;
-    if (dec && (s = make_map(&ik_scan, ik_cache, 64, H, T, 64, 1, 64, "ik_cache")) != MSA_OK) return s;
+    if (dec && (s = make_map(&ik_scan, ik_cache, 64, KH, T, 64, 1, 64, "ik_cache")) != MSA_OK) return s;
     if ((s = marks.mark(0)) != MSA_OK) return s;
     cudaError_t e;
     if (dec) {
         msa::ScanArgs sa{};
         sa.ik_map = &ik_scan;
         sa.H = p->num_kv_heads;
+        sa.ik_shared = ik_shared(p);
         sa.iq = static_cast<const uint16_t*>(iq);
         sa.ik = static_cast<const uint16_t*>(ik_cache);
         sa.cu_rows = p->cu_rows;
@@ -550,6 +558,7 @@ msa_status msa_forward_marked(const msa_problem* p, const void* q, const void* i
         ia.cache = cache_rows_of(p);
         ia.num_seqs = p->num_seqs;
         ia.H = p->num_kv_heads;
+        ia.ik_shared = ik_shared(p);
         ia.top_k = p->top_k;
         ia.total_rows = p->total_rows;
         ia.max_rows_per_seq = p->max_rows_per_seq;

@@ -130,6 +130,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1) prefill_index_kernel(const __g
         if (lane == 0) {
             prefetch_tmap(&iq_map);
             prefetch_tmap(&ik_map);
+            const int key_head = a.ik_shared ? 0 : h;  // a shared index key is head 0 of ik
             mbar_arrive_expect_tx(&sm.a_full, kIdxABytes);
             tma_load_3d(sm.a, &iq_map, &sm.a_full, 0, h, sm.row0);
             for (int n = 0; n < ntiles; ++n) {
@@ -137,7 +138,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1) prefill_index_kernel(const __g
                 if (n >= kIdxStages && !mbar_wait(&sm.empty[s], ((n / kIdxStages) - 1) & 1, a.err)) break;
                 if (a.cache.table == nullptr) {  // contiguous: the tile is one 256-position box
                     mbar_arrive_expect_tx(&sm.full[s], kIdxTileBytes);
-                    tma_load_3d(sm.b[s], &ik_map, &sm.full[s], 0, h,
+                    tma_load_3d(sm.b[s], &ik_map, &sm.full[s], 0, key_head,
                                 static_cast<int>(a.cache.starts[sm.seq] + static_cast<int64_t>(n) * kIdxCols));
                     continue;
                 }
@@ -162,7 +163,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1) prefill_index_kernel(const __g
 #pragma unroll
                 for (int qq = 0; qq < kIdxCols / kBlock; ++qq)
                     if (rows[qq] >= 0)
-                        tma_load_3d(sm.b[s] + qq * (kIdxTileBytes / (kIdxCols / kBlock)), &ik_map, &sm.full[s], 0, h,
+                        tma_load_3d(sm.b[s] + qq * (kIdxTileBytes / (kIdxCols / kBlock)), &ik_map, &sm.full[s], 0, key_head,
                                     static_cast<int>(rows[qq]));
             }
         }

@@ -46,7 +46,8 @@ __global__ void __launch_bounds__(kStagedThreads) index_scores_kernel(StagedArgs
         float s = -INFINITY;
         const int64_t row0 = ok && t <= p ? block_row(a.cache, b, t & ~int64_t{kBlock - 1}) : -1;
         if (row0 >= 0) {  // (a page outside the pool leaves -inf)
-            const uint16_t* kp = ik + ((row0 + (t & (kBlock - 1))) * a.H + h) * kIndexDim;
+            const int kh = a.ik_shared ? 1 : a.H;  // index-key heads per position
+            const uint16_t* kp = ik + ((row0 + (t & (kBlock - 1))) * kh + (a.ik_shared ? 0 : h)) * kIndexDim;
             s = 0.f;
 #pragma unroll
             for (int c = 0; c < kIndexDim / 8; ++c) {

@@ -35,7 +35,7 @@
  *       q    [total_rows, H*G, D]   bf16   q head g of KV head h is h*G+g
  *       iq   [total_rows, H, Di]    bf16
  *       k, v [cache_tokens, H, D]   bf16   token t of sequence b is row
- *       ik   [cache_tokens, H, Di]  bf16   cache_starts[b] + t
+ *       ik   [cache_tokens, H, Di]  bf16   cache_starts[b] + t  (H -> 1: shared key)
  *       out  [total_rows, H*G, D]   fp32 or bf16 (msa_problem.out_dtype)
  *       sel  [total_rows, H, top_k] int32, kept blocks ascending, -1 padded
  *       nsel [total_rows, H]        int32, number of kept blocks
@@ -114,6 +114,10 @@ typedef struct msa_problem {
     const int32_t* block_table;  /* device [B, block_table_stride] int32 page numbers, or NULL */
     int32_t block_table_stride;  /* >= ceil(max_cache_len / page_size)           */
     int32_t page_size;           /* tokens per page: a power of two >= 64 (=S x 2^k) */
+    /* Index keys per position: 0 or num_kv_heads = one per KV head (ik is
+     * [cache_tokens, H, Di]); 1 = one key shared by every KV head (ik is
+     * [cache_tokens, 1, Di]) and s_t = iq[r,h,:] . ik[t,0,:]. */
+    int32_t index_key_heads;
 } msa_problem;
 
 /* Human-readable name of a status code (static string). */

@@ -234,11 +234,11 @@ def paged_layout(w: Workload, x: dict, page_size: int, spare_pages: int = 3, see
     starts = x["cache_starts"]
     for i, name in enumerate(n for n in ("k", "v", "ik") if n in x):
         src = x[name]
-        width = src.shape[2]
+        heads, width = src.shape[1], src.shape[2]
         if name == "ik":
-            pool = int_bf16(seed, STREAM_POOL + i, (rows, w.H, width))
+            pool = int_bf16(seed, STREAM_POOL + i, (rows, heads, width))
         else:
-            pool = normal_bf16(seed, STREAM_POOL + i, (rows, w.H, width))
+            pool = normal_bf16(seed, STREAM_POOL + i, (rows, heads, width))
         for b, L in enumerate(lens):
             for pg in range(pages[b]):
                 t0, t1 = pg * page_size, min(L, (pg + 1) * page_size)
@@ -269,6 +269,9 @@ WORKLOADS = {
     # beyond the five configurations: drafted windows (several decode rows per sequence)
     "decode_4x4_65536": lambda: Workload("decode_4x4_65536", H=4, G=16, seqs=[(4, 65536)] * 4,
                                          note="drafted windows: 4 sequences x 4 rows, 65,536 cached tokens each"),
+    "decode_4x65536_shared_ik": lambda: Workload("decode_4x65536_shared_ik", H=4, G=16, seqs=[(1, 65536)] * 4,
+                                                 ik_heads=1,
+                                                 note="decode batch 4 at 65,536, one index key per position shared by the 4 KV heads"),
 }
 
 

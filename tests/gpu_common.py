@@ -36,7 +36,7 @@ def problem(w: synth.Workload, x: dict, out_dtype=torch.float32, device="cuda", 
     m = msa()
     return m.Problem(w.H, w.G, w.seqs, device, top_k=w.top_k, scale=w.softmax_scale, out_dtype=out_dtype,
                      cache_starts=[int(s) for s in x["cache_starts"]], cache_tokens=int(sum(L for _, L in w.seqs)),
-                     **kw)
+                     ik_heads=w.ik_heads, **kw)
 
 
 def run_forward(w, x, out_dtype=torch.float32, dx=None, **kw):
