@@ -205,6 +205,76 @@ __global__ void __launch_bounds__(ScanCfg<H, kShared>::kThreads, 1) decode_scan_
         const int npos0 = 2 * tig < st.n ? max(0, min(kBlock, last0)) : 0;
         const int npos1 = 2 * tig + 1 < st.n ? max(0, min(kBlock, last0 + 1)) : 0;
         if (!mbar_wait(&full[warp], (i / Cfg::kStages) & 1, a.err)) break;
+        if constexpr (kShared) {
+            // one key tile for every head: the B columns are the (row, head) pairs,
+            // column c = h * n + i, eight per pass
+            const int ncols = st.n * H;
+            for (int c0 = 0; c0 < ncols; c0 += 8) {
+                const int cb = c0 + grp;  // this lane's B column
+                uint32_t bq[4][2];
+                if (cb < ncols) {
+                    const int hb = cb / st.n, ib = cb - hb * st.n;
+                    const uint32_t* qc = reinterpret_cast<const uint32_t*>(
+                        a.iq + (static_cast<int64_t>(st.r + ib) * H + hb) * kIndexDim);
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        bq[kk][0] = __ldg(qc + kk * 8 + tig);
+                        bq[kk][1] = __ldg(qc + kk * 8 + 4 + tig);
+                    }
+                } else {
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) bq[kk][0] = bq[kk][1] = 0u;
+                }
+                float c[4][4];
+#pragma unroll
+                for (int mt = 0; mt < 4; ++mt) c[mt][0] = c[mt][1] = c[mt][2] = c[mt][3] = 0.f;
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+#pragma unroll
+                    for (int mt = 0; mt < 4; ++mt) {
+                        const int mi = lane >> 3;
+                        const int row = mt * 16 + (mi & 1) * 8 + (lane & 7);
+                        const int chunk = kk * 2 + (mi >> 1);
+                        uint32_t a0, a1, a2, a3;
+                        ldsm_x4(stage + row * 128 + ((chunk ^ (row & 7)) << 4), a0, a1, a2, a3);
+                        mma_bf16_16816(c[mt], a0, a1, a2, a3, bq[kk][0], bq[kk][1]);
+                    }
+                // accumulator columns of this lane: c0 + 2tig (e = 0) and c0 + 2tig + 1 (e = 1)
+                int npe[2], he[2], ie[2];
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int ce = c0 + 2 * tig + e;
+                    he[e] = ce / st.n;
+                    ie[e] = ce - he[e] * st.n;
+                    npe[e] = ce < ncols ? max(0, min(kBlock, st.L - st.n + ie[e] + 1 - j * kBlock)) : 0;
+                }
+                float m0 = -INFINITY, m1 = -INFINITY;
+#pragma unroll
+                for (int mt = 0; mt < 4; ++mt) {
+                    const int t0 = mt * 16 + grp, t1 = t0 + 8;
+                    if (t0 < npe[0]) m0 = fmaxf(m0, c[mt][0]);
+                    if (t1 < npe[0]) m0 = fmaxf(m0, c[mt][2]);
+                    if (t0 < npe[1]) m1 = fmaxf(m1, c[mt][1]);
+                    if (t1 < npe[1]) m1 = fmaxf(m1, c[mt][3]);
+                }
+#pragma unroll
+                for (int o = 4; o < 32; o <<= 1) {
+                    m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, o));
+                    m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, o));
+                }
+                if (grp == 0) {
+                    const float me[2] = {m0, m1};
+#pragma unroll
+                    for (int e = 0; e < 2; ++e)
+                        if (npe[e] > 0)
+                            a.pooled[((static_cast<int64_t>(b) * a.rows_per_seq + ie[e]) * H + he[e]) * a.max_blocks + j] =
+                                me[e];
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[warp]);  // stage reusable
+            continue;
+        }
 #pragma unroll 1
         for (int h = 0; h < H; ++h) {
             uint32_t bq[4][2];  // this head's index queries as B fragments (L1-resident rows)
