@@ -251,13 +251,29 @@ def measure_gpu(w, steps, warmup, dev, dist_on, flush_bytes=512 << 20, e2e_steps
         # would break their programmatic-launch overlap); a second graph with marks
         # gives the per-stage times.
         cap = torch.cuda.Stream(dev)
+        side = torch.cuda.Stream(dev)
+        try:  # mark 0 recorded by torch inside a capture needs an external event
+            mark0 = torch.cuda.Event(enable_timing=True, external=True)
+            mark0.record(stream)
+        except TypeError:
+            mark0 = None
         graphs = []
         for ev in (None, marks):
             g = torch.cuda.CUDAGraph()
             cap.wait_stream(stream)
             with torch.cuda.stream(cap):
                 with torch.cuda.graph(g, stream=cap):
-                    step(ev)
+                    if ev is not None and mark0 is not None:
+                        # stage marks: the flush in the graph, mark 0 on a branch that
+                        # waits only for it (as for the timed step), marks 1-4 in line
+                        flush_l2(0)
+                        side.wait_stream(cap)
+                        with torch.cuda.stream(side):
+                            mark0.record(side)
+                        step([None] + ev[1:])
+                        cap.wait_stream(side)
+                    else:
+                        step(ev)
             stream.wait_stream(cap)
             graphs.append(g)
         graph, graph_marked = graphs
@@ -327,13 +343,19 @@ def measure_gpu(w, steps, warmup, dev, dist_on, flush_bytes=512 << 20, e2e_steps
         td.barrier()
     assert msa.error_word(ws) == 0
     for i in range(steps):  # per-stage times, outside the timed region
-        flush_l2(i)
-        if graph_marked is not None:
-            graph_marked.replay()
+        if graph_marked is not None and mark0 is not None:
+            graph_marked.replay()  # holds its own flush
+            marks[4].synchronize()
+            first = [mark0.elapsed_time(marks[1])]
         else:
-            step(marks)
-        marks[4].synchronize()
-        stage_ms.append([marks[j].elapsed_time(marks[j + 1]) for j in range(4)])
+            flush_l2(i)
+            if graph_marked is not None:
+                graph_marked.replay()
+            else:
+                step(marks)
+            marks[4].synchronize()
+            first = [marks[0].elapsed_time(marks[1])]
+        stage_ms.append(first + [marks[j].elapsed_time(marks[j + 1]) for j in range(1, 4)])
     total_ms = max_over_ranks(float(sum(step_ms)), dev if dist_on else None)
     res = dict(ms_per_step=total_ms / steps, stage_ms=np.mean(np.array(stage_ms), axis=0).tolist(),
                wall_s=wall, clocks=clk.summary(), launches=pb.forward_launches() * steps,
