@@ -470,6 +470,8 @@ def main():
     ap.add_argument("--no-graph", action="store_true", help="launch each step directly instead of replaying a CUDA graph")
     ap.add_argument("--multirow", default="decode_4x4_65536",
                     help="decode workload with several rows per sequence measured in the same run ('none' to skip)")
+    ap.add_argument("--no-other-configs", dest="other_configs", action="store_false",
+                    help="skip the short timings of the remaining configurations")
     ap.add_argument("--shared-key", default="decode_4x65536_shared_ik",
                     help="decode workload with one index key shared by all KV heads ('none' to skip)")
     ap.add_argument("--paged-page-size", type=int, default=64,
@@ -585,6 +587,28 @@ def main():
                             "roofline": roofline_for(w3, res3, hbm, bf16, bf16_sus, peak_kind),
                             "note": w3.note}
         line["gpu_launches"] += res3["launches"]
+    if args.other_configs:
+        # the remaining configurations of the pages' workloads, a short timing each
+        others = []
+        for name in ("decode_1x4096", "decode_1x262144", "mixed_8dec_512pre"):
+            if name in (args.workload, args.secondary):
+                continue
+            w5 = synth.workload(name)
+            res5 = measure_gpu(w5, max(5, args.steps // 2), args.warmup, dev, dist_on, with_e2e=False,
+                               use_graph=not args.no_graph)
+            rf = roofline_for(w5, res5, hbm, bf16, bf16_sus, peak_kind)
+            wc5 = work_counts(w5)
+            sb = wc5["scan_bytes"] + wc5["dec_att_bytes"]
+            others.append({"workload": w5.name, "metric": _metric_for(w5),
+                           "value": round(whole_job_rate(w5.total_rows, ws, res5["ms_per_step"]), 1), "unit": "rows/s",
+                           "ms_per_step": round(res5["ms_per_step"], 5),
+                           "stage_us": {k: round(v * 1e3, 2) for k, v in zip(
+                               ("decode_scan", "decode_attend", "prefill_index", "prefill_attend"), res5["stage_ms"])},
+                           "roofline": rf,
+                           "decode_step_hbm_frac": (round(sb / (res5["ms_per_step"] * 1e-3) / 1e9 / hbm, 4)
+                                                    if wc5["pre_rows"] == 0 and sb else None)})
+            line["gpu_launches"] += res5["launches"]
+        line["other_configs"] = others
     if rank == 0 and not args.no_cpu_baseline:
         cb = cpu_baseline(w, _sample_rows(w, 4 if wc["pre_rows"] == 0 else 64), reps=3 if wc["pre_rows"] == 0 else 1)
         cb.pop("seconds")

@@ -111,8 +111,13 @@ struct PrefillIndexArgs {
     int64_t cache_tokens;
     int32_t* sel;   // [R, H, top_k]
     int32_t* nsel;  // [R, H]
+    int nsplit;         // position-range splits per (row tile, head); 1 = no merge
+    uint64_t* cand;     // nsplit > 1: [R, H, nsplit, 15] best (pooled score, block) keys of each split
+    int32_t* tickets;   // nsplit > 1: [tile bound, H] arrivals, zero on entry
     uint32_t* err;
 };
+
+constexpr int kIdxMaxSplit = 8;  // most position-range splits of the prompt-chunk indexer
 
 struct PrefillAttendArgs {
     const CUtensorMap* q_map;  // q as (D, H*G, rows)

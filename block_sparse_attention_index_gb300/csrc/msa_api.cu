@@ -110,9 +110,12 @@ msa::CacheRows cache_rows_of(const msa_problem* p) {
 }
 
 struct Layout {
-    size_t err = 0, tickets = 0, pooled = 0, partials = 0, sel = 0, nsel = 0, total = 0;
+    size_t err = 0, tickets = 0, idx_tickets = 0, pooled = 0, partials = 0, sel = 0, nsel = 0, idx_cand = 0, total = 0;
     size_t header_bytes = 0;  // error word + tickets, cleared at the start of a call
 };
+
+// Upper bound of the prompt-chunk indexer's row tiles (128 rows each).
+int64_t index_tile_bound(const msa_problem* p) { return (p->total_rows + 127) / 128 + p->num_seqs; }
 
 // Pooled-score row slots per sequence of the decode family.
 size_t decode_rows_per_seq(const msa_problem* p) {
@@ -129,6 +132,8 @@ Layout layout_of(const msa_problem* p) {
     off += 16;
     l.tickets = off;
     off += B * H * sizeof(int32_t);
+    l.idx_tickets = off;  // prompt-chunk indexer: arrivals per (row tile, head)
+    off += (static_cast<size_t>(index_tile_bound(p)) * H) * sizeof(int32_t);
     l.header_bytes = off;
     off = align256(off);
     l.pooled = off;
@@ -138,6 +143,9 @@ Layout layout_of(const msa_problem* p) {
     off = align256(off + R * H * K * sizeof(int32_t));
     l.nsel = off;
     off = align256(off + R * H * sizeof(int32_t));
+    l.idx_cand = off;  // prompt-chunk indexer: per-split top-15 lists
+    if (p->max_rows_per_seq > msa::kDecodeMaxRows && p->num_decode_seqs != p->num_seqs)
+        off = align256(off + R * H * msa::kIdxMaxSplit * 15 * sizeof(uint64_t));
     l.total = off;
     return l;
 }
@@ -566,6 +574,16 @@ msa_status msa_forward_marked(const msa_problem* p, const void* q, const void* i
         ia.cache_tokens = p->cache_tokens;
         ia.sel = sel;
         ia.nsel = nsel;
+        {  // position-range splits so that the indexer's CTAs fill the GPU
+            const int64_t pre_seqs = p->num_decode_seqs >= 0 ? p->num_seqs - p->num_decode_seqs : p->num_seqs;
+            const int64_t ctas = ((p->total_rows + 127) / 128 + pre_seqs) * p->num_kv_heads;
+            const int64_t col_tiles = (p->max_cache_len + 255) / 256;
+            int64_t ns = msa::device_sm_count() / (ctas > 0 ? ctas : 1);
+            if (ns > col_tiles / 2) ns = col_tiles / 2;  // at least two 256-position tiles a split
+            ia.nsplit = static_cast<int>(ns < 1 ? 1 : (ns > msa::kIdxMaxSplit ? msa::kIdxMaxSplit : ns));
+        }
+        ia.cand = reinterpret_cast<uint64_t*>(ws + l.idx_cand);
+        ia.tickets = reinterpret_cast<int32_t*>(ws + l.idx_tickets);
         ia.err = reinterpret_cast<uint32_t*>(ws + l.err);
         if ((e = msa::run_prefill_index(ia, st)) != cudaSuccess) return cuda_fail(e, "prefill indexer launch");
         if ((s = marks.mark(3)) != MSA_OK) return s;

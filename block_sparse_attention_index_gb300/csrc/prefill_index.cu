@@ -6,8 +6,10 @@
 // RTX PRO 6000 Blackwell (SM120)", "What this fixes": max-pool scoring and a
 // forced local block.
 //
-// One CTA = one tile of 128 query rows of one sequence and one KV head.  It
-// streams the sequence's index keys in tiles of 256 positions:
+// One CTA = one tile of 128 query rows of one sequence and one KV head (and,
+// when the tiles alone would leave SMs idle, one of up to kIdxMaxSplit
+// ranges of the positions; the last range to finish merges the ranges' lists
+// of the 15 best blocks).  It streams the index keys in tiles of 256 positions:
 //     D[128 rows, 256 positions] = iq[128, 64] . ik[256, 64]^T   (fp32, TMEM)
 // one tcgen05.mma (M=128, N=256, K=16) per 16 index dims.  The accumulator is
 // double-buffered in tensor memory (2 x 256 columns) so the MMA of tile n+1
@@ -40,6 +42,8 @@ struct __align__(1024) IndexSmem {
     uint64_t acc_empty[2];
     uint32_t tmem_base;
     int32_t seq, row0, nrows, ntiles, p0, L;
+    int32_t n0, n1;  // this split's 256-position tiles [n0, n1)
+    int32_t last;    // this CTA merges the splits' lists
 
 };
 
@@ -62,6 +66,9 @@ __device__ bool find_tile(const PrefillIndexArgs& a, int tile, int& b, int& i0, 
     }
     return false;
 }
+
+// Barrier of the four epilogue warps (threads 0-127) only.
+__device__ __forceinline__ void epilogue_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
 __device__ __forceinline__ void insert_top15(uint64_t (&best)[15], uint64_t key) {
     if (key <= best[14]) return;
@@ -101,6 +108,8 @@ __global__ void __launch_bounds__(kIdxThreads, 1) prefill_index_kernel(const __g
                 sm.p0 = L - n + i0;                              // position of the tile's first row
                 const int pmax = sm.p0 + nr - 1;
                 sm.ntiles = (pmax + kIdxCols) / kIdxCols;        // tiles covering positions 0..pmax
+                sm.n0 = static_cast<int>(static_cast<int64_t>(sm.ntiles) * blockIdx.z / a.nsplit);
+                sm.n1 = static_cast<int>(static_cast<int64_t>(sm.ntiles) * (blockIdx.z + 1) / a.nsplit);
             } else {
                 atomicOr(a.err, kErrBadMetadata);
             }
@@ -123,7 +132,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1) prefill_index_kernel(const __g
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = sm.tmem_base;
-    const int ntiles = sm.ntiles;
+    const int n0 = sm.n0, n1 = sm.n1;  // this split's tiles
 
     if (warp == 4) {
         // ---------------- TMA producer
@@ -133,9 +142,10 @@ __global__ void __launch_bounds__(kIdxThreads, 1) prefill_index_kernel(const __g
             const int key_head = a.ik_shared ? 0 : h;  // a shared index key is head 0 of ik
             mbar_arrive_expect_tx(&sm.a_full, kIdxABytes);
             tma_load_3d(sm.a, &iq_map, &sm.a_full, 0, h, sm.row0);
-            for (int n = 0; n < ntiles; ++n) {
-                const int s = n % kIdxStages;
-                if (n >= kIdxStages && !mbar_wait(&sm.empty[s], ((n / kIdxStages) - 1) & 1, a.err)) break;
+            for (int n = n0; n < n1; ++n) {
+                const int i = n - n0;  // ring position
+                const int s = i % kIdxStages;
+                if (i >= kIdxStages && !mbar_wait(&sm.empty[s], ((i / kIdxStages) - 1) & 1, a.err)) break;
                 if (a.cache.table == nullptr) {  // contiguous: the tile is one 256-position box
                     mbar_arrive_expect_tx(&sm.full[s], kIdxTileBytes);
                     tma_load_3d(sm.b[s], &ik_map, &sm.full[s], 0, key_head,
@@ -173,10 +183,11 @@ __global__ void __launch_bounds__(kIdxThreads, 1) prefill_index_kernel(const __g
             constexpr uint32_t idesc = idesc_bf16_f32(kIdxRows, kIdxCols, 0, 0);
             bool ok = mbar_wait(&sm.a_full, 0, a.err);
             const uint32_t a_addr = smem_u32(sm.a);
-            for (int n = 0; ok && n < ntiles; ++n) {
-                const int s = n % kIdxStages, acc = n & 1;
-                if (!mbar_wait(&sm.full[s], (n / kIdxStages) & 1, a.err)) break;
-                if (n >= 2 && !mbar_wait(&sm.acc_empty[acc], ((n >> 1) - 1) & 1, a.err)) break;
+            for (int n = n0; ok && n < n1; ++n) {
+                const int i = n - n0;
+                const int s = i % kIdxStages, acc = i & 1;
+                if (!mbar_wait(&sm.full[s], (i / kIdxStages) & 1, a.err)) break;
+                if (i >= 2 && !mbar_wait(&sm.acc_empty[acc], ((i >> 1) - 1) & 1, a.err)) break;
                 tc_fence_after();
                 const uint32_t b_addr = smem_u32(sm.b[s]);
 #pragma unroll
@@ -192,16 +203,16 @@ __global__ void __launch_bounds__(kIdxThreads, 1) prefill_index_kernel(const __g
     } else {
         // ---------------- epilogue: one row per thread
         const int row = tid;  // TMEM lane
-        const bool live = row < sm.nrows;
+        bool live = row < sm.nrows;
         const int p = sm.p0 + row;
         const int J = p / kBlock;
         uint64_t best[15];
 #pragma unroll
         for (int i = 0; i < 15; ++i) best[i] = 0;
         const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-        for (int n = 0; n < ntiles; ++n) {
-            const int acc = n & 1;
-            if (!mbar_wait(&sm.acc_full[acc], (n >> 1) & 1, a.err)) break;
+        for (int n = n0; n < n1; ++n) {
+            const int acc = (n - n0) & 1;
+            if (!mbar_wait(&sm.acc_full[acc], ((n - n0) >> 1) & 1, a.err)) break;
             tc_fence_after();
 #pragma unroll 1
             for (int jb = 0; jb < kIdxCols / kBlock; ++jb) {
@@ -220,6 +231,33 @@ __global__ void __launch_bounds__(kIdxThreads, 1) prefill_index_kernel(const __g
             }
             tc_fence_before();
             mbar_arrive(&sm.acc_empty[acc]);
+        }
+        if (a.nsplit > 1) {
+            // publish this split's list; the last split of the (row tile, head) to
+            // arrive merges all lists (each block lies in exactly one split's range)
+            if (live) {
+                uint64_t* mine =
+                    a.cand + ((static_cast<int64_t>(sm.row0 + row) * a.H + h) * a.nsplit + blockIdx.z) * 15;
+#pragma unroll
+                for (int i = 0; i < 15; ++i) mine[i] = best[i];
+            }
+            __threadfence();
+            epilogue_sync();
+            if (tid == 0) sm.last = atomicAdd(a.tickets + static_cast<int64_t>(blockIdx.x) * a.H + h, 1) == a.nsplit - 1;
+            epilogue_sync();
+            if (!sm.last) {
+                live = false;
+            } else {
+                __threadfence();
+                if (live) {
+                    const uint64_t* lists = a.cand + (static_cast<int64_t>(sm.row0 + row) * a.H + h) * a.nsplit * 15;
+                    for (int sp = 0; sp < a.nsplit; ++sp) {
+                        if (sp == static_cast<int>(blockIdx.z)) continue;
+#pragma unroll
+                        for (int i = 0; i < 15; ++i) insert_top15(best, __ldcg(lists + sp * 15 + i));
+                    }
+                }
+            }
         }
         if (live) {
             // kept blocks: the best min(top_k-1, J) plus J, ascending, -1 padded
@@ -261,7 +299,7 @@ cudaError_t run_prefill_index(const PrefillIndexArgs& a, cudaStream_t stream) {
     cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(prefill_index_kernel), smem);
     if (e != cudaSuccess) return e;
     const int tiles = (a.total_rows + kIdxRows - 1) / kIdxRows + a.num_seqs;  // upper bound
-    dim3 grid(tiles, a.H);
+    dim3 grid(tiles, a.H, a.nsplit);
     prefill_index_kernel<<<grid, kIdxThreads, smem, stream>>>(*a.iq_map, *a.ik_map, a);
     return cudaGetLastError();
 }
