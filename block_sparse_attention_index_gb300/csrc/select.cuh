@@ -9,10 +9,10 @@
 //
 // Each candidate j is a distinct 64-bit key (ordered score, ~j), so the
 // result does not depend on thread order:
-//   1. every thread takes the largest key among its strided candidates; the
-//      scores are read kChunk per thread at a time, all loads issued before
-//      any use, and kept in registers when J <= kChunk x NT (otherwise staged
-//      in shared memory on the way when they fit);
+//   1. every thread takes the largest key among its strided candidates; up
+//      to kRegRounds x kChunk scores per thread are loaded at once and kept
+//      in registers (otherwise rounds of kChunk, staged in shared memory on
+//      the way when they fit);
 //   2. every warp sorts its 32 per-thread maxima (bitonic, shuffles) and
 //      takes the k-th largest: that is a lower bound of the k-th largest key
 //      overall (k distinct candidates reach it); tau = the largest bound;
@@ -27,7 +27,8 @@
 namespace msa {
 
 constexpr int kCandCap = 512;
-constexpr int kChunk = 8;  // pooled scores per thread and load round
+constexpr int kChunk = 8;      // pooled scores per thread and load round
+constexpr int kRegRounds = 4;  // rounds kept in registers (J <= 4 x 8 x NT): every load issued at once
 constexpr int kSelStage = 4096;  // pooled scores staged in shared memory up to this many blocks
 
 template <int NT>
@@ -76,27 +77,51 @@ __device__ int cta_select(const float* pooled, int J, int top_k, int* sel, Selec
         __syncthreads();
         return J + 1;
     }
-    // 1. per-thread maxima; the first round's scores stay in registers
-    const bool in_regs = J <= kChunk * NT;
+    // 1. per-thread maxima
+    const bool in_regs = J <= kRegRounds * kChunk * NT;
     const bool staged = !in_regs && J <= kSelStage;
     uint64_t mine = 0;
-    float v0[kChunk];
-    for (int base = 0; base < J; base += kChunk * NT) {
-        float v[kChunk];
+    float v0[kRegRounds][kChunk];
+    const int rounds = (J + kChunk * NT - 1) / (kChunk * NT);  // used rounds (uniform branches below)
+    if (in_regs) {
 #pragma unroll
-        for (int i = 0; i < kChunk; ++i) {  // independent loads, all in flight together
-            const int j = base + i * NT + tid;
-            v[i] = j < J ? pooled[j] : 0.f;  // generic load: pooled may be shared memory
-        }
+        for (int rr = 0; rr < kRegRounds; ++rr)
+            if (rr < rounds) {
 #pragma unroll
-        for (int i = 0; i < kChunk; ++i) {
-            const int j = base + i * NT + tid;
-            if (j < J) {
-                if (staged) sm.vals[j] = v[i];
-                const uint64_t key = block_key(v[i], j);
-                mine = key > mine ? key : mine;
+                for (int i = 0; i < kChunk; ++i) {  // independent loads, all in flight together
+                    const int j = (rr * kChunk + i) * NT + tid;
+                    v0[rr][i] = j < J ? pooled[j] : 0.f;  // generic load: pooled may be shared memory
+                }
             }
-            if (base == 0) v0[i] = v[i];
+#pragma unroll
+        for (int rr = 0; rr < kRegRounds; ++rr)
+            if (rr < rounds) {
+#pragma unroll
+                for (int i = 0; i < kChunk; ++i) {
+                    const int j = (rr * kChunk + i) * NT + tid;
+                    if (j < J) {
+                        const uint64_t key = block_key(v0[rr][i], j);
+                        mine = key > mine ? key : mine;
+                    }
+                }
+            }
+    } else {
+        for (int base = 0; base < J; base += kChunk * NT) {
+            float v[kChunk];
+#pragma unroll
+            for (int i = 0; i < kChunk; ++i) {
+                const int j = base + i * NT + tid;
+                v[i] = j < J ? pooled[j] : 0.f;
+            }
+#pragma unroll
+            for (int i = 0; i < kChunk; ++i) {
+                const int j = base + i * NT + tid;
+                if (j < J) {
+                    if (staged) sm.vals[j] = v[i];
+                    const uint64_t key = block_key(v[i], j);
+                    mine = key > mine ? key : mine;
+                }
+            }
         }
     }
     // 2. per-warp bound: sort the 32 maxima descending, take the others-th;
@@ -123,14 +148,18 @@ __device__ int cta_select(const float* pooled, int J, int top_k, int* sel, Selec
     // 3. gather candidates >= tau
     if (in_regs) {
 #pragma unroll
-        for (int i = 0; i < kChunk; ++i) {
-            const int j = i * NT + tid;
-            const uint64_t key = j < J ? block_key(v0[i], j) : 0;
-            if (key >= tau) {
-                const int slot = atomicAdd(&sm.count, 1);
-                if (slot < kCandCap) sm.cand[slot] = key;
+        for (int rr = 0; rr < kRegRounds; ++rr)
+            if (rr < rounds) {
+#pragma unroll
+                for (int i = 0; i < kChunk; ++i) {
+                    const int j = (rr * kChunk + i) * NT + tid;
+                    const uint64_t key = j < J ? block_key(v0[rr][i], j) : 0;
+                    if (key >= tau) {
+                        const int slot = atomicAdd(&sm.count, 1);
+                        if (slot < kCandCap) sm.cand[slot] = key;
+                    }
+                }
             }
-        }
     } else {
         for (int j = tid; j < J; j += NT) {
             const uint64_t key = block_key(staged ? sm.vals[j] : pooled[j], j);
