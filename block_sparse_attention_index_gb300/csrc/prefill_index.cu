@@ -18,14 +18,15 @@
 // j < J into a sorted register list of the 15 best (pooled score desc, j asc).
 // Scores are never written to memory.
 //
-// Warp roles: warps 0-3 epilogue, warp 4 TMA producer, warp 5 MMA issuer and
+// Warp roles: warps 0-7 epilogue (two per TMEM lane quarter, each taking two
+// of a tile's four blocks), warp 8 TMA producer, warp 9 MMA issuer and
 // tensor-memory owner.
 #include "common.cuh"
 #include "internal.h"
 
 namespace msa {
 
-constexpr int kIdxThreads = 192;
+constexpr int kIdxThreads = 320;  // 8 epilogue warps, producer, MMA issuer
 constexpr int kIdxRows = 128;     // M
 constexpr int kIdxCols = 256;     // N, positions per tile
 constexpr int kIdxStages = 4;     // index-key tile ring
@@ -44,6 +45,7 @@ struct __align__(1024) IndexSmem {
     int32_t seq, row0, nrows, ntiles, p0, L;
     int32_t n0, n1;  // this split's 256-position tiles [n0, n1)
     int32_t last;    // this CTA merges the splits' lists
+    uint64_t half_list[kIdxRows][15];  // the second epilogue half's best blocks per row
 
 };
 
@@ -67,8 +69,8 @@ __device__ bool find_tile(const PrefillIndexArgs& a, int tile, int& b, int& i0, 
     return false;
 }
 
-// Barrier of the four epilogue warps (threads 0-127) only.
-__device__ __forceinline__ void epilogue_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+// Barrier of the eight epilogue warps (threads 0-255) only.
+__device__ __forceinline__ void epilogue_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 
 __device__ __forceinline__ void insert_top15(uint64_t (&best)[15], uint64_t key) {
     if (key <= best[14]) return;
@@ -121,20 +123,20 @@ __global__ void __launch_bounds__(kIdxThreads, 1) prefill_index_kernel(const __g
         mbar_init(&sm.a_full, 1);
         for (int s = 0; s < 2; ++s) {
             mbar_init(&sm.acc_full[s], 1);
-            mbar_init(&sm.acc_empty[s], 128);
+            mbar_init(&sm.acc_empty[s], 256);  // every epilogue thread
         }
         fence_mbar_init();
     }
     __syncthreads();
     if (sm.seq < 0) return;
-    if (warp == 5) tmem_alloc(&sm.tmem_base, 512);
+    if (warp == 9) tmem_alloc(&sm.tmem_base, 512);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = sm.tmem_base;
     const int n0 = sm.n0, n1 = sm.n1;  // this split's tiles
 
-    if (warp == 4) {
+    if (warp == 8) {
         // ---------------- TMA producer
         if (lane == 0) {
             prefetch_tmap(&iq_map);
@@ -177,7 +179,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1) prefill_index_kernel(const __g
                                     static_cast<int>(rows[qq]));
             }
         }
-    } else if (warp == 5) {
+    } else if (warp == 9) {
         // ---------------- MMA issuer
         if (lane == 0) {
             constexpr uint32_t idesc = idesc_bf16_f32(kIdxRows, kIdxCols, 0, 0);
@@ -201,21 +203,23 @@ __global__ void __launch_bounds__(kIdxThreads, 1) prefill_index_kernel(const __g
             }
         }
     } else {
-        // ---------------- epilogue: one row per thread
-        const int row = tid;  // TMEM lane
+        // ---------------- epilogue: warps w and w+4 share TMEM lane quarter w; a thread
+        // owns one row and half of each tile's blocks (blocks 2 half, 2 half + 1)
+        const int quarter = warp & 3, half = warp >> 2;
+        const int row = quarter * 32 + lane;  // TMEM lane
         bool live = row < sm.nrows;
         const int p = sm.p0 + row;
         const int J = p / kBlock;
         uint64_t best[15];
 #pragma unroll
         for (int i = 0; i < 15; ++i) best[i] = 0;
-        const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+        const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
         for (int n = n0; n < n1; ++n) {
             const int acc = (n - n0) & 1;
             if (!mbar_wait(&sm.acc_full[acc], ((n - n0) >> 1) & 1, a.err)) break;
             tc_fence_after();
 #pragma unroll 1
-            for (int jb = 0; jb < kIdxCols / kBlock; ++jb) {
+            for (int jb = half * 2; jb < half * 2 + 2; ++jb) {
                 const int j = n * (kIdxCols / kBlock) + jb;
                 uint32_t v[4][16];
 #pragma unroll
@@ -232,6 +236,17 @@ __global__ void __launch_bounds__(kIdxThreads, 1) prefill_index_kernel(const __g
             tc_fence_before();
             mbar_arrive(&sm.acc_empty[acc]);
         }
+        // the two halves' lists of a row into one (blocks are disjoint)
+        if (half == 1 && live) {
+#pragma unroll
+            for (int i = 0; i < 15; ++i) sm.half_list[row][i] = best[i];
+        }
+        epilogue_sync();
+        if (half == 0 && live) {
+#pragma unroll
+            for (int i = 0; i < 15; ++i) insert_top15(best, sm.half_list[row][i]);
+        }
+        if (half == 1) live = false;  // half 0 finishes the row
         if (a.nsplit > 1) {
             // publish this split's list; the last split of the (row tile, head) to
             // arrive merges all lists (each block lies in exactly one split's range)
@@ -288,7 +303,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1) prefill_index_kernel(const __g
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 5) {
+    if (warp == 9) {
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }
