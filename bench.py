@@ -251,7 +251,6 @@ def measure_gpu(w, steps, warmup, dev, dist_on, flush_bytes=512 << 20, e2e_steps
         # would break their programmatic-launch overlap); a second graph with marks
         # gives the per-stage times.
         cap = torch.cuda.Stream(dev)
-        side = torch.cuda.Stream(dev)
         try:  # mark 0 recorded by torch inside a capture needs an external event
             mark0 = torch.cuda.Event(enable_timing=True, external=True)
             mark0.record(stream)
@@ -264,14 +263,10 @@ def measure_gpu(w, steps, warmup, dev, dist_on, flush_bytes=512 << 20, e2e_steps
             with torch.cuda.stream(cap):
                 with torch.cuda.graph(g, stream=cap):
                     if ev is not None and mark0 is not None:
-                        # stage marks: the flush in the graph, mark 0 on a branch that
-                        # waits only for it (as for the timed step), marks 1-4 in line
+                        # stage marks: the flush in the graph, then every mark in line
                         flush_l2(0)
-                        side.wait_stream(cap)
-                        with torch.cuda.stream(side):
-                            mark0.record(side)
+                        mark0.record(cap)
                         step([None] + ev[1:])
-                        cap.wait_stream(side)
                     else:
                         step(ev)
             stream.wait_stream(cap)
@@ -292,21 +287,17 @@ def measure_gpu(w, steps, warmup, dev, dist_on, flush_bytes=512 << 20, e2e_steps
                 ev.record(stream)
             torch.cuda.synchronize(dev)
             g = torch.cuda.CUDAGraph()
-            side = torch.cuda.Stream(dev)
             cap.wait_stream(stream)
             with torch.cuda.stream(cap):
                 with torch.cuda.graph(g, stream=cap):
                     flush_l2(0)
-                    # the begin mark on a branch of its own that waits only for the
-                    # flush: it fires when the step's inputs are ready, while the
-                    # step's first kernel launches (a mark node in line with the step
-                    # would add a node-to-node dependency delay to the step)
-                    side.wait_stream(cap)
-                    with torch.cuda.stream(side):
-                        tmarks[0].record(side)
+                    # marks in line with the step: an event node on a branch of its
+                    # own can fire after the next node of the main branch has run,
+                    # so it could start the clock late; in line it can only start it
+                    # early (a node-to-node delay before the first kernel)
+                    tmarks[0].record(cap)
                     step()
                     tmarks[1].record(cap)
-                    cap.wait_stream(side)
             stream.wait_stream(cap)
             torch.cuda.synchronize(dev)
             for _ in range(warmup):
@@ -545,8 +536,8 @@ def main():
             "config": {"workload": w.name, "note": w.note, "H": w.H, "G": w.G, "head_dim": w.D, "index_dim": w.Di,
                        "block": w.S, "top_k": w.top_k, "rows_per_gpu": rows,
                        "cache_tokens_per_gpu": w.cache_tokens, "l2": "flushed before every step (512 MiB write, then 256 MiB read)",
-                       "launch": ("CUDA graph: L2 flush; then one msa_forward and the end mark, with the begin mark on a "
-                                   "branch that waits only for the flush" if res.get("flush_in_graph")
+                       "launch": ("CUDA graph: L2 flush, begin mark, one msa_forward, end mark (marks in line)"
+                                  if res.get("flush_in_graph")
                                   else "CUDA graph replay of one msa_forward" if res["graph"] else "direct msa_forward calls"),
                        "parallelism": f"replicas x{ws}"},
             "stage_us": {"decode_scan": round(res["stage_ms"][0] * 1e3, 2),
