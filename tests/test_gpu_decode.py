@@ -112,3 +112,39 @@ def test_decode_workloads_full_size(name):
     ref = oracle_forward(w, x)
     assert_selection_equal(sel, nsel, ref)
     assert_out_close(out, ref["out"], torch.float32)
+
+
+def test_decode_max_cache_len():
+    """The largest supported cache (2^21 tokens, 32,768 blocks): the selection
+    reads its pooled scores in rounds from memory (beyond the register and
+    shared-memory paths)."""
+    w = synth.Workload("dec_max_len", H=1, G=16, seqs=[(1, 1 << 21), (1, 70000)], seed=31)
+    x = synth.make_inputs(w)
+    out, sel, nsel = run_forward(w, x)
+    ref = oracle_forward(w, x)
+    assert_selection_equal(sel, nsel, ref)
+    assert_out_close(out, ref["out"], torch.float32)
+
+
+def test_decode_max_num_seqs():
+    """4,096 decode sequences (the supported maximum) with ragged short caches:
+    the scan's prefix sum over sequences runs in several chunks and the
+    attention grid is 4,096 deep."""
+    lens = synth.ragged_lengths(5, 4096, 1, 400)
+    w = synth.Workload("dec_many", H=2, G=4, seqs=[(1, L) for L in lens], seed=32)
+    x = synth.make_inputs(w)
+    out, sel, nsel = run_forward(w, x)
+    ref = oracle_forward(w, x)
+    assert_selection_equal(sel, nsel, ref)
+    assert_out_close(out, ref["out"], torch.float32)
+
+
+def test_decode_family_max_rows_many_sequences():
+    """4,096 sequences of 8 drafted rows each: 32,768 attention grid rows."""
+    lens = synth.ragged_lengths(6, 4096, 8, 200)
+    w = synth.Workload("dec_many_rows", H=1, G=2, seqs=[(8, L) for L in lens], seed=33)
+    x = synth.make_inputs(w)
+    out, sel, nsel = run_forward(w, x)
+    ref = oracle_forward(w, x)
+    assert_selection_equal(sel, nsel, ref)
+    assert_out_close(out, ref["out"], torch.float32)

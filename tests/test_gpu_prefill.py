@@ -102,3 +102,15 @@ def test_prefill_workloads_full_size(name):
     ref = oracle_forward(w, x)
     assert_selection_equal(sel, nsel, ref)
     assert_out_close(out, ref["out"], torch.float32)
+
+
+def test_prefill_long_prefix():
+    """A 256-row chunk after a 131,072-token prefix: the indexer splits each
+    (row tile, head) over position ranges and merges their lists; selections
+    reach back over 2,000+ blocks."""
+    w = synth.Workload("pre_long", H=4, G=16, seqs=[(256, 131072 + 256)], seed=34)
+    x = synth.make_inputs(w)
+    out, sel, nsel = run_forward(w, x)
+    ref = oracle_forward(w, x)
+    assert_selection_equal(sel, nsel, ref)
+    assert_out_close(out, ref["out"], torch.float32)
