@@ -11,8 +11,8 @@
 // result does not depend on thread order:
 //   1. every thread takes the largest key among its strided candidates; up
 //      to kRegRounds x kChunk scores per thread are loaded at once and kept
-//      in registers (otherwise rounds of kChunk, staged in shared memory on
-//      the way when they fit);
+//      in registers (longer lists are read in rounds of kChunk, and read
+//      again for the gather);
 //   2. every warp sorts its 32 per-thread maxima (bitonic, shuffles) and
 //      takes the k-th largest: that is a lower bound of the k-th largest key
 //      overall (k distinct candidates reach it); tau = the largest bound;
@@ -29,11 +29,9 @@ namespace msa {
 constexpr int kCandCap = 512;
 constexpr int kChunk = 8;      // pooled scores per thread and load round
 constexpr int kRegRounds = 4;  // rounds kept in registers (J <= 4 x 8 x NT): every load issued at once
-constexpr int kSelStage = 4096;  // pooled scores staged in shared memory up to this many blocks
 
 template <int NT>
 struct SelectSmem {
-    float vals[kSelStage];
     uint64_t warp_tau[NT / 32];
     uint64_t cand[kCandCap];
     uint64_t red[NT / 32];
@@ -79,7 +77,6 @@ __device__ int cta_select(const float* pooled, int J, int top_k, int* sel, Selec
     }
     // 1. per-thread maxima
     const bool in_regs = J <= kRegRounds * kChunk * NT;
-    const bool staged = !in_regs && J <= kSelStage;
     uint64_t mine = 0;
     float v0[kRegRounds][kChunk];
     const int rounds = (J + kChunk * NT - 1) / (kChunk * NT);  // used rounds (uniform branches below)
@@ -117,7 +114,6 @@ __device__ int cta_select(const float* pooled, int J, int top_k, int* sel, Selec
             for (int i = 0; i < kChunk; ++i) {
                 const int j = base + i * NT + tid;
                 if (j < J) {
-                    if (staged) sm.vals[j] = v[i];
                     const uint64_t key = block_key(v[i], j);
                     mine = key > mine ? key : mine;
                 }
@@ -162,7 +158,7 @@ __device__ int cta_select(const float* pooled, int J, int top_k, int* sel, Selec
             }
     } else {
         for (int j = tid; j < J; j += NT) {
-            const uint64_t key = block_key(staged ? sm.vals[j] : pooled[j], j);
+            const uint64_t key = block_key(pooled[j], j);
             if (key >= tau) {
                 const int slot = atomicAdd(&sm.count, 1);
                 if (slot < kCandCap) sm.cand[slot] = key;
