@@ -14,8 +14,11 @@
 // one tcgen05.mma (M=128, N=256, K=16) per 16 index dims.  The accumulator is
 // double-buffered in tensor memory (2 x 256 columns) so the MMA of tile n+1
 // overlaps the epilogue of tile n.  Epilogue: thread i owns row i (TMEM lane
-// i), max-pools each 64-column block over positions <= p, and inserts blocks
-// j < J into a sorted register list of the 15 best (pooled score desc, j asc).
+// i) and max-pools each 64-column block with one reduction load from tensor
+// memory (tcgen05.ld.red .max: the block's maximum arrives with its values,
+// no per-column compares), then inserts blocks j < J into a sorted register
+// list of the 15 best (pooled score desc, j asc).  Blocks j < J lie wholly
+// at positions <= p; the local block J is forced and needs no score.
 // Scores are never written to memory.
 //
 // Warp roles: warps 0-7 epilogue (two per TMEM lane quarter, each taking two
@@ -221,16 +224,10 @@ __global__ void __launch_bounds__(kIdxThreads, 1) prefill_index_kernel(const __g
 #pragma unroll 1
             for (int jb = half * 2; jb < half * 2 + 2; ++jb) {
                 const int j = n * (kIdxCols / kBlock) + jb;
-                uint32_t v[4][16];
-#pragma unroll
-                for (int c = 0; c < 4; ++c) tmem_ld16(lane_addr + acc * kIdxCols + jb * kBlock + c * 16, v[c]);
+                float m;  // the block's pooled score: the maximum of its 64 columns, taken by the TMEM load
+                tmem_ld_max64(lane_addr + acc * kIdxCols + jb * kBlock, m);
                 tmem_ld_wait();
                 if (!live || j >= J) continue;  // the local block is forced; later blocks are in the future
-                float m = __uint_as_float(v[0][0]);
-#pragma unroll
-                for (int c = 0; c < 4; ++c)
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) m = fmaxf(m, __uint_as_float(v[c][e]));
                 insert_top15(best, block_key(m, j));
             }
             tc_fence_before();
