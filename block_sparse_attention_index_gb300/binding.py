@@ -23,7 +23,7 @@ ERR_WAIT_TIMEOUT, ERR_BAD_METADATA, ERR_TMEM_ALLOC = 1, 2, 4
 EXPORTED = [
     "msa_status_string", "msa_last_error", "msa_workspace_size", "msa_index_scores", "msa_select_blocks",
     "msa_attend_decode", "msa_attend_prefill", "msa_forward", "msa_forward_marked", "msa_forward_launches",
-    "msa_attend_decode_noalloc",
+    "msa_attend_decode_noalloc", "msa_check_wait_timeout",
 ]
 
 
@@ -70,9 +70,10 @@ def _load():
     lib.msa_forward_marked.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, C.c_size_t, vp,
                                        C.POINTER(vp), i32]
     lib.msa_forward_launches.argtypes = [P]
+    lib.msa_check_wait_timeout.argtypes = [vp, C.c_size_t, C.c_uint32, vp]
     lib.msa_forward_launches.restype = i32
     for name in ["msa_workspace_size", "msa_index_scores", "msa_select_blocks", "msa_attend_decode",
-                 "msa_attend_decode_noalloc",
+                 "msa_attend_decode_noalloc", "msa_check_wait_timeout",
                  "msa_attend_prefill", "msa_forward", "msa_forward_marked"]:
         getattr(lib, name).restype = C.c_int
     return lib
@@ -294,11 +295,18 @@ def forward(pb: Problem, q, iq, k, v, ik, out=None, sel=None, nsel=None, workspa
     return out, sel, nsel
 
 
+def check_wait_timeout(workspace, limit_us: int = 20000):
+    """msa_check_wait_timeout: one bounded wait of the library runs out on purpose
+    and sets the timeout bit (ERR_WAIT_TIMEOUT) of the workspace's error word."""
+    _need(workspace, "workspace", torch.uint8, workspace.device)
+    _check(_lib.msa_check_wait_timeout(_ptr(workspace), workspace.numel(), int(limit_us), _stream(workspace.device)))
+
+
 def error_word(workspace) -> int:
     """The device error word at the start of a workspace (synchronises)."""
     return int(workspace[:4].view(torch.int32).item())
 
 
 __all__ = ["Problem", "MsaProblem", "MsaError", "index_scores", "select_blocks", "attend_decode", "attend_prefill",
-           "attend_decode_noalloc",
+           "attend_decode_noalloc", "check_wait_timeout",
            "forward", "error_word", "lib", "LIB_PATH", "EXPORTED"]

@@ -116,12 +116,13 @@ __device__ __forceinline__ bool mbar_try_wait_hint(uint64_t* bar, uint32_t parit
 
 // Wait for phase `parity` of `bar` to complete, giving up after kWaitLimitNs.
 // On time-out sets kErrWaitTimeout in *err (if given) and returns false.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* err) {
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* err,
+                                          uint64_t limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     while (true) {
         if (mbar_try_wait_hint(bar, parity, 1000000u)) return true;
-        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        if (globaltimer_ns() - t0 > limit_ns) {
             if (err) atomicOr(err, kErrWaitTimeout);
             return false;
         }
@@ -197,6 +198,7 @@ __device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
                  : "r"(taddr));
 }
 
+#pragma nv_diag_suppress 550  // the reduction load's 64 value registers are written, never read
 // 32 lanes x 32 bits, 64 consecutive columns per thread, reduced to their
 // maximum as they are read (tcgen05.ld.red, an sm_103a instruction): the
 // values themselves are dropped.  Read `m` only after tmem_ld_wait().
@@ -209,6 +211,7 @@ __device__ __forceinline__ void tmem_ld_max64(uint32_t taddr, float& m) {
           "=f"(m)
         : "r"(taddr));
 }
+#pragma nv_diag_default 550
 
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 

@@ -139,7 +139,10 @@ __global__ void __launch_bounds__(kAttThreads) decode_attend_kernel(const __grid
     }
     __syncthreads();
     const bool ok = mbar_wait(&sm.bar, 0, a.err);
-    if (!ok) return;  // the copy never landed; the error word says so
+    if (!ok) {  // the copy never landed (the error word says so): wait once more, bounded, so
+        mbar_wait(&sm.bar, 0, nullptr);  // that no copy is left in flight when the CTA ends
+        return;
+    }
 
     // ---- S = Q K^T for keys [16*warp, 16*warp + 16)
     const int grp = lane >> 2, tig = lane & 3;

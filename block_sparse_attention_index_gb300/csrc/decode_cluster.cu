@@ -180,7 +180,11 @@ __global__ void __launch_bounds__(kClThreads) decode_cluster_kernel(const __grid
         }
     }
     __syncthreads();  // q visible to every warp
-    if (nmy > 0 && !__syncthreads_and(mbar_wait(&sm.bar, 0, a.err))) nmy = 0;  // copy never landed: no keys
+    bool kv_in_flight = false;  // a copy that did not land in time: waited for again before the CTA ends
+    if (nmy > 0 && !__syncthreads_and(mbar_wait(&sm.bar, 0, a.err))) {
+        nmy = 0;  // copy never landed: no keys
+        kv_in_flight = true;
+    }
 
 
     // ---- S = Q K^T: warp w owns keys [32w, 32w+32) of this CTA's 128 (block w/2)
@@ -334,6 +338,7 @@ __global__ void __launch_bounds__(kClThreads) decode_cluster_kernel(const __grid
         else
             *reinterpret_cast<float2*>(reinterpret_cast<float*>(a.out) + oi) = make_float2(ox * inv, oy * inv);
     }
+    if (kv_in_flight && tid == 0) mbar_wait(&sm.bar, 0, nullptr);
 }
 
 cudaError_t run_decode_cluster(const DecodeAttendArgs& a, bool after_scan, cudaStream_t stream) {

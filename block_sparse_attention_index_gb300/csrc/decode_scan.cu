@@ -153,6 +153,7 @@ __global__ void __launch_bounds__(ScanCfg<H, kShared>::kThreads, 1) decode_scan_
             prefetch_tmap(&ik_map);
             int b = b0;
             ScanSeqState st;
+            int armed = 0;  // stages armed so far (ring positions 0 .. armed-1)
             for (int i = 0; i < n; ++i) {
                 const int64_t u = u0 + i;
                 scan_locate(a, prefix, u, b, st);
@@ -176,7 +177,12 @@ __global__ void __launch_bounds__(ScanCfg<H, kShared>::kThreads, 1) decode_scan_
                 } else {
                     mbar_arrive_expect_tx(&full[s], 0);
                 }
+                armed = i + 1;
             }
+            // no copy of this lane may still be in flight when the CTA ends (after a timed-out
+            // wait of a consumer, too): wait, bounded, for the last phase armed on every stage
+            for (int s = 0; s < Cfg::kStages && s < armed; ++s)
+                mbar_wait(&full[s], ((s + Cfg::kStages * ((armed - 1 - s) / Cfg::kStages)) / Cfg::kStages) & 1, a.err);
         }
         return;
     }
@@ -275,6 +281,7 @@ __global__ void __launch_bounds__(ScanCfg<H, kShared>::kThreads, 1) decode_scan_
             if (lane == 0) mbar_arrive(&empty[warp]);  // stage reusable
             continue;
         }
+        if constexpr (!kShared) {  // one key tile per head
 #pragma unroll 1
         for (int h = 0; h < H; ++h) {
             uint32_t bq[4][2];  // this head's index queries as B fragments (L1-resident rows)
@@ -294,7 +301,7 @@ __global__ void __launch_bounds__(ScanCfg<H, kShared>::kThreads, 1) decode_scan_
                     const int row = mt * 16 + (mi & 1) * 8 + (lane & 7);
                     const int chunk = kk * 2 + (mi >> 1);
                     uint32_t a0, a1, a2, a3;
-                    ldsm_x4(stage + (kShared ? 0 : h) * Cfg::kHeadBytes + row * 128 + ((chunk ^ (row & 7)) << 4), a0,
+                    ldsm_x4(stage + h * Cfg::kHeadBytes + row * 128 + ((chunk ^ (row & 7)) << 4), a0,
                             a1, a2, a3);
                     mma_bf16_16816(c[mt], a0, a1, a2, a3, bq[kk][0], bq[kk][1]);
                 }
@@ -319,6 +326,7 @@ __global__ void __launch_bounds__(ScanCfg<H, kShared>::kThreads, 1) decode_scan_
                 if (npos0 > 0) pooled[(2 * tig) * row_stride] = m0;
                 if (npos1 > 0) pooled[(2 * tig + 1) * row_stride] = m1;
             }
+        }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[warp]);  // stage reusable

@@ -153,6 +153,7 @@ cudaError_t run_select_blocks(const StagedArgs& a, const float* scores, int64_t 
                               cudaStream_t stream);
 cudaError_t run_prefill_index(const PrefillIndexArgs& a, cudaStream_t stream);
 cudaError_t run_prefill_attend(const PrefillAttendArgs& a, cudaStream_t stream);
+cudaError_t run_wait_timeout_check(uint32_t* err, uint64_t limit_ns, cudaStream_t stream);
 
 int device_sm_count();
 

@@ -597,6 +597,17 @@ msa_status msa_forward_marked(const msa_problem* p, const void* q, const void* i
     return MSA_OK;
 }
 
+msa_status msa_check_wait_timeout(void* workspace, size_t workspace_bytes, uint32_t limit_us, void* stream) {
+    g_last_error.clear();
+    msa_status s;
+    if ((s = check_ptr(workspace, "workspace")) != MSA_OK) return s;
+    if (workspace_bytes < sizeof(uint32_t)) return fail(MSA_ERR_WORKSPACE, "workspace smaller than the error word");
+    if (limit_us < 1 || limit_us > 2000000) return fail(MSA_ERR_INVALID_ARG, "limit_us outside [1, 2000000]");
+    cudaError_t e = msa::run_wait_timeout_check(static_cast<uint32_t*>(workspace), 1000ull * limit_us,
+                                                static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? MSA_OK : cuda_fail(e, "wait check launch");
+}
+
 msa_status msa_forward(const msa_problem* p, const void* q, const void* iq, const void* k_cache,
                        const void* v_cache, const void* ik_cache, void* out, int32_t* sel_out, int32_t* nsel_out,
                        void* workspace, size_t workspace_bytes, void* stream) {

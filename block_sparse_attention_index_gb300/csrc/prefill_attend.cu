@@ -82,6 +82,7 @@ struct __align__(1024) AttendSmem {
     uint64_t o_empty[2];
     uint64_t rs_full[2];
     uint64_t rs_empty[2];
+    uint64_t drain[2];  // S and PV issuers: their last MMAs done before the CTA frees tensor memory
     uint64_t info_full[kInfoSlots];
     uint64_t info_empty[kInfoSlots];
     ItemInfo info[kInfoSlots];
@@ -182,6 +183,7 @@ __global__ void __launch_bounds__(kPaThreads, 1) prefill_attend_kernel(const __g
             mbar_init(&sm.rs_full[s], 8);
             mbar_init(&sm.rs_empty[s], 4);
         }
+        for (int s = 0; s < 2; ++s) mbar_init(&sm.drain[s], 1);
         for (int s = 0; s < kInfoSlots; ++s) {
             mbar_init(&sm.info_full[s], 1);
             mbar_init(&sm.info_empty[s], kInfoReaders);
@@ -200,7 +202,7 @@ __global__ void __launch_bounds__(kPaThreads, 1) prefill_attend_kernel(const __g
         if (lane == 0) {
             prefetch_tmap(&q_map);
             prefetch_tmap(&k_map);
-            uint32_t g = 0, n = 0;
+            uint32_t g = 0, n = 0, q_armed = 0;
             bool alive = true;
             for (int item = blockIdx.x; alive && item < n_items; item += gridDim.x) {
                 Item x;
@@ -226,6 +228,7 @@ __global__ void __launch_bounds__(kPaThreads, 1) prefill_attend_kernel(const __g
                 const int qb = n & 1;
                 if (n >= 2 && !mbar_wait(&sm.q_empty[qb], ((n >> 1) - 1) & 1, a.err)) break;
                 mbar_arrive_expect_tx(&sm.q_full[qb], kQBytes);
+                ++q_armed;
                 const int hq0 = x.h * a.G;
                 tma_load_3d(sm.q[qb], &q_map, &sm.q_full[qb], 0, hq0, x.r);
                 tma_load_3d(sm.q[qb] + kQBytes / 2, &q_map, &sm.q_full[qb], 64, hq0, x.r);
@@ -252,6 +255,13 @@ __global__ void __launch_bounds__(kPaThreads, 1) prefill_attend_kernel(const __g
                 sm.info[slot].end = 1;
                 mbar_arrive(&sm.info_full[slot]);
             }
+            // no copy of this thread may still be in flight when the CTA ends (after a
+            // timed-out wait elsewhere, too): wait, bounded, for the last phase armed on
+            // every slot
+            for (uint32_t s = 0; s < kKStages; ++s)
+                if (g > s) mbar_wait(&sm.kfull[s], ((s + kKStages * ((g - 1 - s) / kKStages)) / kKStages) & 1, a.err);
+            for (uint32_t b = 0; b < 2; ++b)
+                if (q_armed > b) mbar_wait(&sm.q_full[b], ((b + 2 * ((q_armed - 1 - b) / 2)) >> 1) & 1, a.err);
         }
     } else if (warp == 13) {
         // ---------------- V producer: the V pairs of PV(i), in item order
@@ -282,6 +292,8 @@ __global__ void __launch_bounds__(kPaThreads, 1) prefill_attend_kernel(const __g
                 mbar_arrive(&sm.info_empty[slot]);
                 if (!alive) break;
             }
+            for (uint32_t s = 0; s < kPvStages; ++s)  // as for K: no copy left in flight
+                if (g > s) mbar_wait(&sm.pv_full[s], ((s + kPvStages * ((g - 1 - s) / kPvStages)) / kPvStages) & 1, a.err);
         }
     } else if (warp == 14) {
         // ---------------- S issuer (tensor-memory owner): S^T(i) = K_pair . Q^T per pair
@@ -295,6 +307,7 @@ __global__ void __launch_bounds__(kPaThreads, 1) prefill_attend_kernel(const __g
 #pragma unroll
             for (int i = 0; i < 2; ++i) qdesc[i] = smem_desc_sw128(smem_u32(sm.q[i]), 16, 1024);
             uint32_t g = 0;
+            bool issued = false;
             for (uint32_t n = 0;; ++n) {
                 const int slot = n % kInfoSlots;
                 if (!mbar_wait(&sm.info_full[slot], (n / kInfoSlots) & 1, a.err)) break;
@@ -319,11 +332,16 @@ __global__ void __launch_bounds__(kPaThreads, 1) prefill_attend_kernel(const __g
                         tc_mma_ss(d_tmem, kb + static_cast<uint64_t>(koff >> 4), qb_desc + static_cast<uint64_t>(qoff >> 4),
                                   idesc_s, kk > 0);
                     }
+                    issued = true;
                     tc_commit(&sm.kempty[s]);
                 }
                 if (!alive) break;
                 tc_commit(&sm.q_empty[qb]);
                 tc_commit(&sm.s_full[sb]);
+            }
+            if (issued) {  // this thread's MMAs are done before tensor memory is freed
+                tc_commit(&sm.drain[0]);
+                mbar_wait(&sm.drain[0], 0, a.err);
             }
         }
     } else if (warp == 15) {
@@ -339,6 +357,7 @@ __global__ void __launch_bounds__(kPaThreads, 1) prefill_attend_kernel(const __g
                 pdesc[i] = smem_desc_sw64(smem_u32(sm.p[i]), 8192, 512);
             }
             uint32_t g = 0;
+            bool issued = false;
             for (uint32_t n = 0;; ++n) {
                 const int slot = n % kInfoSlots;
                 if (!mbar_wait(&sm.info_full[slot], (n / kInfoSlots) & 1, a.err)) break;
@@ -358,10 +377,15 @@ __global__ void __launch_bounds__(kPaThreads, 1) prefill_attend_kernel(const __g
                     for (int kk = 0; kk < 8; ++kk)  // 16 keys per step: V rows +2 KB, P rows +1 KB
                         tc_mma_ss(d_tmem, vb + static_cast<uint64_t>(kk * 2048 >> 4), pb + static_cast<uint64_t>(kk * 1024 >> 4),
                                   idesc_o, (q > 0 || kk > 0) ? 1u : 0u);
+                    issued = true;
                     tc_commit(&sm.pv_empty[s]);
                 }
                 if (!alive) break;
                 tc_commit(&sm.o_full[ob]);
+            }
+            if (issued) {
+                tc_commit(&sm.drain[1]);
+                mbar_wait(&sm.drain[1], 0, a.err);
             }
         }
     } else if (warp < 8) {

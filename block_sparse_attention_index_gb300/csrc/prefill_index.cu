@@ -42,6 +42,7 @@ struct __align__(1024) IndexSmem {
     uint64_t full[kIdxStages];
     uint64_t empty[kIdxStages];
     uint64_t a_full;
+    uint64_t drain;  // the MMA issuer's last MMAs done before tensor memory is freed
     uint64_t acc_full[2];
     uint64_t acc_empty[2];
     uint32_t tmem_base;
@@ -128,6 +129,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1) prefill_index_kernel(const __g
             mbar_init(&sm.acc_full[s], 1);
             mbar_init(&sm.acc_empty[s], 256);  // every epilogue thread
         }
+        mbar_init(&sm.drain, 1);
         fence_mbar_init();
     }
     __syncthreads();
@@ -147,10 +149,12 @@ __global__ void __launch_bounds__(kIdxThreads, 1) prefill_index_kernel(const __g
             const int key_head = a.ik_shared ? 0 : h;  // a shared index key is head 0 of ik
             mbar_arrive_expect_tx(&sm.a_full, kIdxABytes);
             tma_load_3d(sm.a, &iq_map, &sm.a_full, 0, h, sm.row0);
+            int armed = 0;  // ring positions armed so far
             for (int n = n0; n < n1; ++n) {
                 const int i = n - n0;  // ring position
                 const int s = i % kIdxStages;
                 if (i >= kIdxStages && !mbar_wait(&sm.empty[s], ((i / kIdxStages) - 1) & 1, a.err)) break;
+                armed = i + 1;
                 if (a.cache.table == nullptr) {  // contiguous: the tile is one 256-position box
                     mbar_arrive_expect_tx(&sm.full[s], kIdxTileBytes);
                     tma_load_3d(sm.b[s], &ik_map, &sm.full[s], 0, key_head,
@@ -181,12 +185,18 @@ __global__ void __launch_bounds__(kIdxThreads, 1) prefill_index_kernel(const __g
                         tma_load_3d(sm.b[s] + qq * (kIdxTileBytes / (kIdxCols / kBlock)), &ik_map, &sm.full[s], 0, key_head,
                                     static_cast<int>(rows[qq]));
             }
+            // no copy of this lane may still be in flight when the CTA ends (after a timed-out
+            // wait elsewhere, too): wait, bounded, for the last phase armed on every slot
+            mbar_wait(&sm.a_full, 0, a.err);
+            for (int s = 0; s < kIdxStages && s < armed; ++s)
+                mbar_wait(&sm.full[s], ((s + kIdxStages * ((armed - 1 - s) / kIdxStages)) / kIdxStages) & 1, a.err);
         }
     } else if (warp == 9) {
         // ---------------- MMA issuer
         if (lane == 0) {
             constexpr uint32_t idesc = idesc_bf16_f32(kIdxRows, kIdxCols, 0, 0);
             bool ok = mbar_wait(&sm.a_full, 0, a.err);
+            bool issued = false;
             const uint32_t a_addr = smem_u32(sm.a);
             for (int n = n0; ok && n < n1; ++n) {
                 const int i = n - n0;
@@ -201,8 +211,13 @@ __global__ void __launch_bounds__(kIdxThreads, 1) prefill_index_kernel(const __g
                     const uint64_t bd = smem_desc_sw128(b_addr + k * 32, 16, 1024);
                     tc_mma_ss(tmem + acc * kIdxCols, ad, bd, idesc, k > 0);
                 }
+                issued = true;
                 tc_commit(&sm.empty[s]);
                 tc_commit(&sm.acc_full[acc]);
+            }
+            if (issued) {  // this thread's MMAs are done before tensor memory is freed
+                tc_commit(&sm.drain);
+                mbar_wait(&sm.drain, 0, a.err);
             }
         }
     } else {

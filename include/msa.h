@@ -222,6 +222,18 @@ msa_status msa_forward_marked(const msa_problem* p, const void* q, const void* i
 /* Number of kernels msa_forward launches for p (host only). */
 int32_t msa_forward_launches(const msa_problem* p);
 
+/* Diagnostics of the failure path.  Every barrier wait in the library's
+ * kernels gives up after a time limit, sets bit 1 of the device error word
+ * and lets the kernel finish (after waiting, again with a limit, for its own
+ * copies in flight), so a lost arrival ends a call with an error instead of
+ * a hung GPU.  This call makes one such wait run out on purpose: one thread
+ * waits on a barrier that nothing arrives on, gives up after limit_us
+ * microseconds (1 .. 2,000,000) and ORs 1 into the 32-bit word at the start
+ * of `workspace` (device memory, >= 4 bytes, owned by the caller; the word
+ * is not cleared first).  Asynchronous on `stream`; argument errors return
+ * MSA_ERR_INVALID_ARG or MSA_ERR_WORKSPACE without launching. */
+msa_status msa_check_wait_timeout(void* workspace, size_t workspace_bytes, uint32_t limit_us, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

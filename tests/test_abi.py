@@ -98,6 +98,11 @@ def test_workspace_size_and_pointer_checks():
     pb2 = _problem(max_rows_per_seq=1, total_rows=2, num_seqs=2, num_decode_seqs=2)
     assert L.msa_attend_decode(C.byref(pb2), fake, fake, fake, None, fake, fake, ws, 1 << 30, None) == 1
     assert L.msa_index_scores(C.byref(pb), fake, fake, fake, 100, None) == 1  # ld < max_cache_len
+    # the wait check: null workspace, no room for the error word, a limit outside [1 us, 2 s]
+    assert L.msa_check_wait_timeout(None, 256, 1000, None) == 1
+    assert L.msa_check_wait_timeout(ws, 2, 1000, None) == 3
+    assert L.msa_check_wait_timeout(ws, 256, 0, None) == 1
+    assert L.msa_check_wait_timeout(ws, 256, 2000001, None) == 1
     assert L.msa_forward_launches(C.byref(pb)) == 2
     assert L.msa_forward_launches(C.byref(_problem(max_rows_per_seq=12, total_rows=12, num_decode_seqs=0))) == 2
     assert L.msa_forward_launches(C.byref(_problem(num_seqs=2, max_rows_per_seq=9, total_rows=10,

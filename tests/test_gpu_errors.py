@@ -68,3 +68,19 @@ def test_given_selection_outside_causal_range_flagged(kind):
     fn(pb, dx["q"], dx["k"], dx["v"], sel, nsel, workspace=ws)
     torch.cuda.synchronize()
     assert m.error_word(ws) & BAD_METADATA
+
+
+def test_bounded_wait_runs_out_and_the_context_stays_usable():
+    """A barrier wait that nothing completes gives up after its limit, sets the
+    timeout bit of the error word and returns; the next call is exact."""
+    m = msa()
+    ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    m.check_wait_timeout(ws, limit_us=20000)
+    torch.cuda.synchronize()
+    assert m.error_word(ws) & m.ERR_WAIT_TIMEOUT
+    w = synth.Workload("after_timeout", H=2, G=16, seqs=[(1, 3000), (40, 900)], seed=81)
+    x = synth.make_inputs(w)
+    out, sel, nsel = run_forward(w, x)
+    ref = oracle_forward(w, x)
+    assert_selection_equal(sel, nsel, ref)
+    assert_out_close(out, ref["out"], torch.float32)
