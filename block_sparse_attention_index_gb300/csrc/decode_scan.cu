@@ -88,16 +88,21 @@ __global__ void __launch_bounds__(ScanCfg<H, kShared>::kThreads, 1) decode_scan_
     __shared__ int warp_tot[Cfg::kThreads / 32];
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    // The attention kernel that follows uses these words; clear them here.
-    if (blockIdx.x == 0)
-        for (int i = tid; i < a.n_clear; i += Cfg::kThreads) a.clear_words[i] = 0;
     if (tid == 0) {
         for (int s = 0; s < Cfg::kStages; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
         fence_mbar_init();
+        prefetch_tmap(&ik_map);
     }
+    // Launched as a programmatic dependent of whatever kernel precedes it on the
+    // stream: only the set-up above may overlap that kernel; every input read and
+    // every write comes after it has completed and its memory is visible.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    // The attention kernel that follows uses these words; clear them here.
+    if (blockIdx.x == 0)
+        for (int i = tid; i < a.n_clear; i += Cfg::kThreads) a.clear_words[i] = 0;
     // Units per sequence: ceil(L/64) for decode sequences, 0 otherwise
     // (block-wide exclusive scan in chunks of kThreads).
     int carry = 0;
@@ -150,7 +155,6 @@ __global__ void __launch_bounds__(ScanCfg<H, kShared>::kThreads, 1) decode_scan_
     if (warp == Cfg::kConsumers) {
         // ---------------- producer: one lane streams units into the ring
         if (lane == 0) {
-            prefetch_tmap(&ik_map);
             int b = b0;
             ScanSeqState st;
             int armed = 0;  // stages armed so far (ring positions 0 .. armed-1)
@@ -342,7 +346,18 @@ static cudaError_t launch_scan(const ScanArgs& a, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     int64_t grid = device_sm_count();
     if (a.unit_bound < grid) grid = a.unit_bound > 0 ? a.unit_bound : 1;
-    decode_scan_kernel<H, kShared><<<static_cast<unsigned>(grid), Cfg::kThreads, smem, stream>>>(*a.ik_map, a);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+    cfg.blockDim = dim3(Cfg::kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;  // set-up overlaps the previous kernel's tail
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, decode_scan_kernel<H, kShared>, *a.ik_map, a);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
