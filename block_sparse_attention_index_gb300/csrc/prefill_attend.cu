@@ -37,14 +37,16 @@
 //
 // Warp roles: 0-7 softmax (warps w and w+4 share TMEM lane quarter w and
 // take heads 0-7 and 8-15), 8-11 epilogue, 12 K producer, 13 V producer,
-// 14 S issuer and tensor-memory owner, 15 PV issuer.  Items are strided over
-// a grid of one CTA per SM.
+// 14 S issuer and tensor-memory owner, 15 PV issuer, 16 item decoder (the
+// whole warp reads a row's selection and resolves its cache rows, up to six
+// items ahead, so the producers never wait on metadata loads).  Items are
+// strided over a grid of one CTA per SM.
 #include "common.cuh"
 #include "internal.h"
 
 namespace msa {
 
-constexpr int kPaThreads = 512;
+constexpr int kPaThreads = 544;
 constexpr int kKStages = 3;                       // K pairs ring (its own producer warp)
 constexpr int kPvStages = 3;                      // V pairs + P pairs ring: slot i holds both operands of one PV pair
 constexpr int kPairBytes = 2 * 2 * 64 * 64 * 2;  // [dim half][2 blocks x 64 keys][64 dims] bf16 = 32 KB
@@ -54,10 +56,10 @@ constexpr int kTmemCols = 512;
 constexpr int kSCol = 0;                         // S^T buffers: columns [0,128) and [128,256)
 constexpr int kOCol = 256;                       // O^T buffers: columns [256,288) and [288,320)
 constexpr int kInfoSlots = 6;                    // decoded items published by the K producer
-constexpr int kInfoReaders = 1 + 2 + 8 + 4;      // V producer, S and PV issuers, softmax warps, epilogue warps
+constexpr int kInfoReaders = 2 + 2 + 8 + 4;      // K and V producers, S and PV issuers, softmax warps, epilogue warps
 
-// One decoded work item, shared through shared memory so that only one
-// thread per CTA walks the sequence metadata and reads the selection.
+// One decoded work item, shared through shared memory so that only the
+// decoder warp walks the sequence metadata and reads the selection.
 struct ItemInfo {
     int32_t r, h, p, nsel, end;
     int32_t b;                // sequence
@@ -93,15 +95,20 @@ struct __align__(1024) AttendSmem {
 
 static_assert(sizeof(AttendSmem) + 1024 <= 227 * 1024, "prompt-chunk attention exceeds 227 KB of shared memory");
 
-struct Item {
+// One work item as decoded by a warp: the row, KV head, position, number of
+// kept blocks and sequence (the same in every lane), and kept block `lane`
+// with its first cache row (lanes < nsel).
+struct WarpItem {
     int r, h, p, nsel, b;
-    int blk[kMaxTopK];
-    int row[kMaxTopK];
+    int blk, row;
 };
 
-// Decodes work item `it`; false when the item is skipped (a row of a
-// decode-family sequence on the fused path, or inconsistent metadata / selection).
-__device__ bool load_item(const PrefillAttendArgs& a, int it, Item& x, bool& bad) {
+// Decodes work item `it` with all 32 lanes (lane i reads kept block i and
+// resolves its cache row, so the loads of a row's blocks go out together).
+// False when the item is skipped: a row of a decode-family sequence on the
+// fused path, or (with `bad` set in every lane) inconsistent metadata or
+// selection.  Every branch depends only on values that all lanes share.
+__device__ bool decode_item_warp(const PrefillAttendArgs& a, int it, int lane, WarpItem& x, bool& bad) {
     bad = false;
     x.r = it / a.H;
     x.h = it - x.r * a.H;
@@ -111,12 +118,13 @@ __device__ bool load_item(const PrefillAttendArgs& a, int it, Item& x, bool& bad
         if (a.cu_rows[mid] <= x.r) lo = mid; else hi = mid;
     }
     const int b = lo;
-    const int n = a.cu_rows[b + 1] - a.cu_rows[b];
+    const int c0 = a.cu_rows[b], c1 = a.cu_rows[b + 1];
+    const int n = c1 - c0;
     if (a.only_multi_row && n <= kDecodeMaxRows) return false;  // taken by the decode kernels
     const int L = a.cache_lens[b];
     x.b = b;
-    x.p = L - n + (x.r - a.cu_rows[b]);
-    if (x.r < a.cu_rows[b] || x.r >= a.cu_rows[b + 1] || L < 1 || L > a.max_cache_len || x.p < 0 ||
+    x.p = L - n + (x.r - c0);
+    if (x.r < c0 || x.r >= c1 || L < 1 || L > a.max_cache_len || x.p < 0 ||
         !seq_rows_ok(a.cache, b, L, a.cache_tokens)) {
         bad = true;
         return false;
@@ -127,23 +135,19 @@ __device__ bool load_item(const PrefillAttendArgs& a, int it, Item& x, bool& bad
         bad = true;
         return false;
     }
-    const int32_t* s = a.sel + (static_cast<int64_t>(x.r) * a.H + x.h) * a.top_k;
-    for (int i = 0; i < kMaxTopK; ++i) {
-        x.blk[i] = i < x.nsel ? s[i] : 0;
-        if (i < x.nsel && (x.blk[i] < 0 || x.blk[i] > J)) {
-            bad = true;
-            return false;
-        }
+    const bool mine = lane < x.nsel;  // nsel <= top_k <= kMaxTopK <= 32
+    x.blk = mine ? a.sel[(static_cast<int64_t>(x.r) * a.H + x.h) * a.top_k + lane] : 0;
+    bool lane_bad = mine && (x.blk < 0 || x.blk > J);
+    int64_t row = 0;
+    if (mine && !lane_bad) {
+        const int64_t t = static_cast<int64_t>(x.blk) * kBlock;
+        row = a.cache.table == nullptr ? a.cache.starts[b] + t : block_row(a.cache, b, t);
+        lane_bad = row < 0;  // page outside the pool
     }
-    const int64_t start = a.cache.table == nullptr ? a.cache.starts[b] : 0;
-    for (int i = 0; i < kMaxTopK; ++i) {  // cache rows of the kept blocks (independent loads when paged)
-        const int64_t t = static_cast<int64_t>(x.blk[i]) * kBlock;
-        const int64_t row = i >= x.nsel ? 0 : (a.cache.table == nullptr ? start + t : block_row(a.cache, b, t));
-        if (row < 0) {  // page outside the pool
-            bad = true;
-            return false;
-        }
-        x.row[i] = static_cast<int>(row);
+    x.row = static_cast<int>(row);
+    if (__any_sync(0xffffffffu, lane_bad)) {
+        bad = true;
+        return false;
     }
     return true;
 }
@@ -185,7 +189,7 @@ __global__ void __launch_bounds__(kPaThreads, 1) prefill_attend_kernel(const __g
         }
         for (int s = 0; s < 2; ++s) mbar_init(&sm.drain[s], 1);
         for (int s = 0; s < kInfoSlots; ++s) {
-            mbar_init(&sm.info_full[s], 1);
+            mbar_init(&sm.info_full[s], 32);  // every lane of the decoder warp (each releases its own writes)
             mbar_init(&sm.info_empty[s], kInfoReaders);
         }
         fence_mbar_init();
@@ -196,43 +200,70 @@ __global__ void __launch_bounds__(kPaThreads, 1) prefill_attend_kernel(const __g
     tc_fence_after();
     const uint32_t tmem = sm.tmem_base;
 
-    if (warp == 12) {
-        // ---------------- K producer: decodes the items, publishes them, loads Q(i)
-        // and the K pairs of S(i)
-        if (lane == 0) {
-            prefetch_tmap(&q_map);
-            prefetch_tmap(&k_map);
-            uint32_t g = 0, n = 0, q_armed = 0;
-            bool alive = true;
-            for (int item = blockIdx.x; alive && item < n_items; item += gridDim.x) {
-                Item x;
-                bool bad;
-                if (!load_item(a, item, x, bad)) {
-                    if (bad) atomicOr(a.err, kErrBadMetadata);
-                    continue;
-                }
-                const int slot = n % kInfoSlots;
-                if (n >= kInfoSlots && !mbar_wait(&sm.info_empty[slot], ((n / kInfoSlots) - 1) & 1, a.err)) break;
-                ItemInfo& inf = sm.info[slot];
+    if (warp == 16) {
+        // ---------------- item decoder: decodes this CTA's items with the whole warp and
+        // publishes them in the info ring, up to kInfoSlots items ahead of the producers
+        uint32_t n = 0;
+        bool alive = true;
+        for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+            WarpItem x;
+            bool bad;
+            if (!decode_item_warp(a, item, lane, x, bad)) {
+                if (bad && lane == 0) atomicOr(a.err, kErrBadMetadata);
+                continue;
+            }
+            const int slot = n % kInfoSlots;
+            int free_slot = 1;
+            if (lane == 0 && n >= kInfoSlots) free_slot = mbar_wait(&sm.info_empty[slot], ((n / kInfoSlots) - 1) & 1, a.err);
+            if (!__shfl_sync(0xffffffffu, free_slot, 0)) {
+                alive = false;
+                break;
+            }
+            ItemInfo& inf = sm.info[slot];
+            if (lane == 0) {
                 inf.r = x.r;
                 inf.h = x.h;
                 inf.p = x.p;
                 inf.nsel = x.nsel;
                 inf.b = x.b;
                 inf.end = 0;
-                for (int i = 0; i < kMaxTopK; ++i) {
-                    inf.blk[i] = x.blk[i];
-                    inf.row[i] = x.row[i];
-                }
-                mbar_arrive(&sm.info_full[slot]);  // release: the fields above are visible
+            }
+            if (lane < kMaxTopK) {
+                inf.blk[lane] = x.blk;
+                inf.row[lane] = x.row;
+            }
+            mbar_arrive(&sm.info_full[slot]);  // every lane: release of its own fields
+            ++n;
+        }
+        // end marker (also after an abandoned loop, so that every reader stops)
+        const int slot = n % kInfoSlots;
+        int free_slot = alive ? 1 : 0;
+        if (lane == 0 && alive && n >= kInfoSlots)
+            free_slot = mbar_wait(&sm.info_empty[slot], ((n / kInfoSlots) - 1) & 1, a.err);
+        if (__shfl_sync(0xffffffffu, free_slot, 0)) {
+            if (lane == 0) sm.info[slot].end = 1;
+            mbar_arrive(&sm.info_full[slot]);
+        }
+    } else if (warp == 12) {
+        // ---------------- K producer: Q(i) and the K pairs of S(i), in item order
+        if (lane == 0) {
+            prefetch_tmap(&q_map);
+            prefetch_tmap(&k_map);
+            uint32_t g = 0, q_armed = 0;
+            bool alive = true;
+            for (uint32_t n = 0; alive; ++n) {
+                const int slot = n % kInfoSlots;
+                if (!mbar_wait(&sm.info_full[slot], (n / kInfoSlots) & 1, a.err)) break;
+                const ItemInfo& inf = sm.info[slot];
+                if (inf.end) break;
                 const int qb = n & 1;
                 if (n >= 2 && !mbar_wait(&sm.q_empty[qb], ((n >> 1) - 1) & 1, a.err)) break;
                 mbar_arrive_expect_tx(&sm.q_full[qb], kQBytes);
                 ++q_armed;
-                const int hq0 = x.h * a.G;
-                tma_load_3d(sm.q[qb], &q_map, &sm.q_full[qb], 0, hq0, x.r);
-                tma_load_3d(sm.q[qb] + kQBytes / 2, &q_map, &sm.q_full[qb], 64, hq0, x.r);
-                const int npairs = (x.nsel + 1) >> 1;
+                const int hq0 = inf.h * a.G;
+                tma_load_3d(sm.q[qb], &q_map, &sm.q_full[qb], 0, hq0, inf.r);
+                tma_load_3d(sm.q[qb] + kQBytes / 2, &q_map, &sm.q_full[qb], 64, hq0, inf.r);
+                const int nsel = inf.nsel, npairs = (nsel + 1) >> 1;
                 for (int q = 0; q < npairs; ++q, ++g) {
                     const int s = g % kKStages;
                     if (g >= static_cast<uint32_t>(kKStages) &&
@@ -242,18 +273,12 @@ __global__ void __launch_bounds__(kPaThreads, 1) prefill_attend_kernel(const __g
                     }
                     mbar_arrive_expect_tx(&sm.kfull[s], kPairBytes);
                     for (int half = 0; half < 2; ++half) {
-                        const int tok = x.row[min(2 * q + half, x.nsel - 1)];
-                        tma_load_3d(sm.kst[s] + half * 8192, &k_map, &sm.kfull[s], 0, x.h, tok);
-                        tma_load_3d(sm.kst[s] + half * 8192 + 16384, &k_map, &sm.kfull[s], 64, x.h, tok);
+                        const int tok = inf.row[min(2 * q + half, nsel - 1)];
+                        tma_load_3d(sm.kst[s] + half * 8192, &k_map, &sm.kfull[s], 0, inf.h, tok);
+                        tma_load_3d(sm.kst[s] + half * 8192 + 16384, &k_map, &sm.kfull[s], 64, inf.h, tok);
                     }
                 }
-                ++n;
-            }
-            // end marker (also after an abandoned loop, so that every reader stops)
-            const int slot = n % kInfoSlots;
-            if (n < kInfoSlots || mbar_wait(&sm.info_empty[slot], ((n / kInfoSlots) - 1) & 1, a.err)) {
-                sm.info[slot].end = 1;
-                mbar_arrive(&sm.info_full[slot]);
+                mbar_arrive(&sm.info_empty[slot]);
             }
             // no copy of this thread may still be in flight when the CTA ends (after a
             // timed-out wait elsewhere, too): wait, bounded, for the last phase armed on
