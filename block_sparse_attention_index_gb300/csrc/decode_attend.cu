@@ -1,9 +1,10 @@
 // Decode stage 2b+3: block selection, attention over the kept blocks as split
 // partials, and the log-sum-exp combine.
 //
-// PR #1388 "minimax_m3: a CUDA backend for MiniMax-M3.1-Flash ...", commit
-// text of the native Metal family: decode attention runs over the kept
-// blocks in partials.  Here one CTA = one (sequence, KV head, kept block):
+// PR #1388 "minimax_m3: a CUDA backend for MiniMax-M3.1-Flash ...", native
+// Metal family commit: a decode row attends to its chosen blocks in partial
+// results that are merged afterwards.  Here one CTA = one (sequence, KV head,
+// kept block):
 //   - it selects the kept blocks from the pooled index scores (every split
 //     of a (sequence, head) computes the same selection; the pooled scores
 //     are a few KB in L2), or reads a given selection;

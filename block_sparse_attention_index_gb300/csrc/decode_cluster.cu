@@ -1,9 +1,10 @@
 // Decode stage 2b+3 as one thread-block cluster per (query row, KV head) of
 // the decode family (sequences with up to kDecodeMaxRows rows).
 //
-// PR #1388 "minimax_m3: a CUDA backend for MiniMax-M3.1-Flash ...", commit
-// text of the native Metal family: decode attention runs over the kept
-// blocks in partials.  Here the partials never leave the chip:
+// PR #1388 "minimax_m3: a CUDA backend for MiniMax-M3.1-Flash ...", native
+// Metal family commit: a decode row attends to its chosen blocks in partial
+// results that are merged afterwards.  Here the partials never leave the
+// chip:
 //   - the 8 CTAs of a cluster each take two of the (up to 16) kept blocks,
 //     stage their K and V by TMA (128-byte swizzle) and compute S = Q K^T
 //     and O = P V for the group's 16 query heads on mma.sync (P split into

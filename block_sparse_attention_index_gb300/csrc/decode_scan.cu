@@ -1,11 +1,12 @@
 // Decode stage 1+2a: lightning-indexer scan with the block max-pool fused in.
 //
-// For every sequence with exactly one query row (a decode row at p = L-1)
-// and every KV head h, computes the pooled index score of every block j:
+// For every sequence of the decode family (1 to 8 query rows, row i of n at
+// p = L - n + i) and every KV head h, computes the pooled index score of
+// every block j for each row:
 //     m_j = max_{t in block j, t <= p}  iq[r,h,:] . ik[t,h,:]
 // ("MiniMax-M3 on 4x RTX PRO 6000 Blackwell (SM120)", "What this fixes":
-// max-pool scoring; PR #1388 "minimax_m3: a CUDA backend ...": the index
-// scores per row and key head).  Only the pooled scores (4 bytes per block
+// blocks are scored by their largest index score; PR #1388 "minimax_m3: a
+// CUDA backend ...": index scores are taken per row and key head).  Only the pooled scores (4 bytes per block
 // and head) leave the kernel; the per-position scores live in registers.
 //
 // The scan is HBM-bound: each cached position carries H x 64 bf16 index-key

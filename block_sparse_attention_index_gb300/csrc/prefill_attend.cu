@@ -2,10 +2,10 @@
 // head over the row's kept blocks, with tensor-memory accumulators.
 //
 // PR #1388 "minimax_m3: a CUDA backend for MiniMax-M3.1-Flash ...", prompt-
-// tile commit: a tile holds the 16 query heads of one key head; the heads
-// share their row's block selection, so each key/value block is read once
-// for all of them.  The row's selection is used as it stands (a tile never
-// attends to a block the row did not keep).
+// tile commit: the 16 query heads of a key head use the same chosen blocks,
+// so one read of a key or value block serves them all.  Each row keeps its
+// own selection here: a work item never touches a block its row did not
+// choose.
 //
 // Work item = (query row, KV head), up to 16 kept blocks = 8 pairs of 64
 // keys.  The MMAs are transposed so that the 16 heads are the N dimension and

@@ -2,9 +2,10 @@
 // core GEMM with the block max-pool and a running top-k in its epilogue.
 //
 // PR #1388 "minimax_m3: a CUDA backend for MiniMax-M3.1-Flash ...": index
-// scores and top-16 block selection per row and key head; "MiniMax-M3 on 4x
-// RTX PRO 6000 Blackwell (SM120)", "What this fixes": max-pool scoring and a
-// forced local block.
+// scores and the top-16 block selection are made per row and key head;
+// "MiniMax-M3 on 4x RTX PRO 6000 Blackwell (SM120)", "What this fixes": blocks
+// are ranked by their largest index score and the current position's block
+// is always kept.
 //
 // One CTA = one tile of 128 query rows of one sequence and one KV head (and,
 // when the tiles alone would leave SMs idle, one of up to kIdxMaxSplit

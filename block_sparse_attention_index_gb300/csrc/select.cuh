@@ -1,9 +1,10 @@
 // CTA-wide top-k block selection with the forced local block.
 //
 // Rule ("MiniMax-M3 on 4x RTX PRO 6000 Blackwell (SM120)", "What this fixes":
-// per-GQA-group top-16 block selection, max-pool scoring, forced local
-// block; PR #1388 "minimax_m3: a CUDA backend ...": top-16 selection per row
-// and key head): keep the local block J plus the (top_k - 1) best blocks
+// each GQA group keeps 16 blocks ranked by their maximum index score, the
+// current position's block always among them; PR #1388 "minimax_m3: a CUDA
+// backend ...": the selection is made per row and key head): keep the local
+// block J plus the (top_k - 1) best blocks
 // j < J under (pooled score descending, block index ascending); keep every
 // block 0..J when J < top_k; list the kept blocks ascending.
 //

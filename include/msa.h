@@ -3,16 +3,18 @@
  *
  * The method (MiniMax-M3 sparse attention, as the pages describe it):
  *   "MiniMax-M3 on 4x RTX PRO 6000 Blackwell (SM120)", section "What this
- *   fixes": the MSA model does per-GQA-group top-16 block selection with
- *   max-pool scoring and a forced local block.
+ *   fixes": for each GQA group the model keeps the 16 key blocks with the
+ *   largest block maxima of the index scores, always including the block
+ *   that holds the current position.
  *   "minimax_m3: a CUDA backend for MiniMax-M3.1-Flash at TP over GB10s"
- *   (PR #1388), commit text of the native Metal family: lightning-indexer
- *   index scores and top-16 block selection per row and key head; decode
- *   attention over the kept blocks in partials; prompt chunks on the tensor
- *   units over each tile's kept blocks.  Same PR, prompt-tile commit: a tile
- *   holds the 16 query heads of one key head, which share their rows'
- *   selection, so each key/value block is read once for all of them.  Same
- *   PR, cache commit: keys, values and index keys are cached as bf16.
+ *   (PR #1388), native Metal family commit: the lightning indexer scores
+ *   keys and 16 blocks are chosen for each row and key head; a decode row
+ *   attends to its chosen blocks in partial results merged afterwards, and
+ *   prompt chunks run their attention on the matrix units, each tile over
+ *   its chosen blocks.  Same PR, prompt-tile commit: the 16 query heads of a
+ *   key head use the same chosen blocks, so one read of a key or value block
+ *   serves them all.  Same PR, cache commit: the key, value and index-key
+ *   caches hold bf16.
  *
  * For every query row r (absolute position p) and KV head h:
  *   s_t  = iq[r,h,:] . ik[t,h,:]                     t = 0..p        (indexer)
@@ -30,7 +32,7 @@
  *     default stream) and launch only the library's own kernels.  No call
  *     synchronises the device or reads device memory on the host, so every
  *     call can be enqueued back to back.
- *   - bf16 is IEEE-754 binary16 "brain float" bits (uint16_t); fp32 is float.
+ *   - bf16 is bfloat16: the upper 16 bits of an IEEE-754 binary32 (uint16_t); fp32 is float.
  *   - Layouts are contiguous, row-major:
  *       q    [total_rows, H*G, D]   bf16   q head g of KV head h is h*G+g
  *       iq   [total_rows, H, Di]    bf16

@@ -16,24 +16,26 @@
  *     The pages name the indexer but print no formula; the plain reading is
  *     the dot product of the index query with the index key, no activation,
  *     weight or scale.
- *  2. Max-pool scoring (MiniMax-M3 on 4x RTX PRO 6000 Blackwell (SM120),
- *     "What this fixes": "max-pool scoring"):
+ *  2. Block max-pool (MiniMax-M3 on 4x RTX PRO 6000 Blackwell (SM120),
+ *     section What this fixes: a block is scored by the largest index score
+ *     among its positions):
  *         m_j = max { s_t : t in [jS, jS+S-1], t <= p }   for j = 0 .. J,
  *     J = floor(p / S) the block holding the current position.
  *  3. Top-k block selection per row and GQA group with the forced local
- *     block (same passage: "per-GQA-group top-16 block selection ... forced
- *     local block"): the kept set is {J} plus the (top_k - 1) best blocks
+ *     block (same section: each GQA group keeps 16 blocks, one of them always
+ *     the block of the current position): the kept set is {J} plus the
+ *     (top_k - 1) best blocks
  *     j < J under the order (m_j descending, j ascending).  When J < top_k
  *     every causal block is kept.  The set is returned sorted ascending.
  *  4. Attention of each query head g of group h over the kept keys
- *     (PR #1388: "decode attention over the kept blocks"; the same
- *     per-row result for prompt chunks, whose tiles share the selection of
- *     their rows):
+ *     (PR #1388: decode rows attend over their kept blocks only; prompt
+ *     chunks give the same per-row result, their tiles sharing the rows'
+ *     selection):
  *         x_t = scale * (q[r, h*G+g] . k[t, h])  for t in kept blocks, t <= p
  *         o   = sum_t exp(x_t - max x) v[t, h] / sum_t exp(x_t - max x)
- *     Keys, values and index keys are bf16 (PR #1388, commit removing the
- *     int8 cache: "keys, values and index keys are cached as bf16"); they
- *     are widened exactly to double here.
+ *     Keys, values and index keys are bf16 (PR #1388, the commit that
+ *     removes the int8 cache keeps all three caches in bf16); they are
+ *     widened exactly to double here.
  *
  * Layouts (contiguous): q [R, H*G, D], iq [R, H, Di], k/v [T, H, D],
  * ik [T, H, Di]; token t of sequence b is cache row cache_starts[b] + t.
