@@ -36,3 +36,42 @@ def test_work_counts_by_hand():
     kept = sum(15 * 64 + (p % 64) + 1 for p in range(8192, 12288))
     assert wc3["att_flops"] == 4 * 128 * kept * 4 * 16
     assert wc3["idx_flops"] == sum(2 * 64 * (p + 1) * 4 for p in range(8192, 12288))
+
+
+def test_rotation_sets_clear_the_l2():
+    """Back-to-back timing rotates enough input copies that the other copies'
+    bytes between two uses of one copy exceed twice the L2; tiny workloads
+    fall back to the flush."""
+    for name in synth.WORKLOADS:
+        w = synth.workload(name)
+        n = bench.rotation_sets(w)
+        t = bench.step_touched_bytes(w)
+        if n:
+            assert 3 <= n <= 8
+            assert (n - 1) * t > 2 * bench.L2_BYTES, (name, n, t)
+        else:
+            assert 7 * t <= 2 * bench.L2_BYTES, (name, t)
+    assert bench.rotation_sets(synth.workload("decode_1x4096")) == 0
+    assert bench.rotation_sets(synth.workload("decode_4x65536")) == 3
+
+
+def test_step_touched_bytes_by_hand():
+    w = synth.workload("prefill_4096_at_8192")
+    # q in (bf16) and out (fp32) of 4,096 rows x 64 heads x 128 dims, iq, and the causal caches (ik 64 + k, v 128 dims)
+    want = 4096 * 64 * 128 * 6 + 4096 * 4 * 64 * 2 + 12288 * (4 * 64 + 2 * 4 * 128) * 2
+    assert bench.step_touched_bytes(w) == want
+    w2 = synth.workload("decode_4x65536")
+    wc = bench.work_counts(w2)
+    assert bench.step_touched_bytes(w2) == wc["scan_bytes"] + wc["dec_att_bytes"]
+
+
+def test_timing_fields_pick_back_to_back_when_measured():
+    res = {"ms_per_step": 0.040, "b2b_ms_per_step": 0.034, "b2b_sets": 3}
+    assert bench.step_ms(res) == 0.034
+    assert "rotating" in bench.timing_note(res)
+    lat = bench.flushed_latency(res, rows=4, ws=1)
+    assert lat["ms_per_step"] == 0.04 and abs(lat["value"] - 100000.0) < 1e-6
+    flushed_only = {"ms_per_step": 0.017}
+    assert bench.step_ms(flushed_only) == 0.017
+    assert bench.flushed_latency(flushed_only, rows=1, ws=1) is None
+    assert "flushed" in bench.timing_note(flushed_only)
