@@ -65,8 +65,8 @@ msa_status check_problem(const msa_problem* p) {
     if (p->max_rows_per_seq <= msa::kDecodeMaxRows && p->num_decode_seqs != -1 && p->num_decode_seqs != p->num_seqs)
         return fail(MSA_ERR_INVALID_ARG, "max_rows_per_seq <= 8 implies num_decode_seqs == num_seqs");
     if (!p->cu_rows || !p->cache_lens) return fail(MSA_ERR_INVALID_ARG, "device metadata is null");
-    if (!aligned16(p->cu_rows) && (reinterpret_cast<uintptr_t>(p->cu_rows) & 3u))
-        return fail(MSA_ERR_INVALID_ARG, "cu_rows misaligned");
+    if ((reinterpret_cast<uintptr_t>(p->cu_rows) & 3u) || (reinterpret_cast<uintptr_t>(p->cache_lens) & 3u))
+        return fail(MSA_ERR_INVALID_ARG, "cu_rows or cache_lens is not 4-byte aligned");
     if (p->index_key_heads != 0 && p->index_key_heads != 1 && p->index_key_heads != H)
         return fail(MSA_ERR_INVALID_ARG, "index_key_heads must be 0, 1 or num_kv_heads (got %d)", p->index_key_heads);
     if (p->block_table == nullptr) {

@@ -60,7 +60,8 @@ def _problem(**over):
     (dict(num_seqs=0), 1), (dict(softmax_scale=float("nan")), 1), (dict(softmax_scale=-1.0), 1),
     (dict(out_dtype=7), 1), (dict(total_rows=0), 1), (dict(max_rows_per_seq=2), 1),
     (dict(max_cache_len=(1 << 21) + 1), 2), (dict(cache_tokens=0), 1), (dict(num_decode_seqs=2), 1),
-    (dict(cu_rows=None), 1), (dict(cache_starts=260), 1), (dict(cache_starts=None), 1),
+    (dict(cu_rows=None), 1), (dict(cu_rows=258), 1), (dict(cache_lens=258), 1), (dict(cache_starts=260), 1),
+    (dict(cache_starts=None), 1),
     (dict(num_seqs=2, max_rows_per_seq=8, total_rows=9, num_decode_seqs=1), 1),  # <= 8 rows: all decode family
     # paged caches: page size a power of two >= 64, pool a whole number of pages,
     # table wide enough for max_cache_len, table aligned
