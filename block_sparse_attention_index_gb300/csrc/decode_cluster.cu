@@ -168,22 +168,27 @@ __global__ void __launch_bounds__(kClThreads) decode_cluster_kernel(const __grid
             blk[i] = J;
         }
     }
-    if (tid == 0 && nmy > 0) {
-        mbar_arrive_expect_tx(&sm.bar, nmy * 4 * 64 * 64 * 2);
-        for (int i = 0; i < nmy; ++i) {
-            int64_t row = block_row(a.cache, b, static_cast<int64_t>(blk[i]) * kBlock);
-            if (row < 0) {  // page outside the pool
-                atomicOr(a.err, kErrBadMetadata);
-                row = 0;
-            }
-            const int tok = static_cast<int>(row);
+    if (tid == 0 && nmy > 0) mbar_arrive_expect_tx(&sm.bar, nmy * 4 * 64 * 64 * 2);
+    __syncthreads();  // the expected bytes are registered before any copy lands; q visible to every warp
+    // Warp w issues the copies of block w / 2, K (w even) or V (w odd): one thread issues TMA boxes
+    // at a bounded rate, so four issuers land the 64 KB sooner than one.
+    if (lane == 0 && warp < 2 * nmy) {
+        const int i = warp >> 1;
+        const int bi = i == 0 ? blk[0] : blk[1];  // no dynamic index into blk: it stays in registers
+        int64_t row = block_row(a.cache, b, static_cast<int64_t>(bi) * kBlock);
+        if (row < 0) {  // page outside the pool
+            atomicOr(a.err, kErrBadMetadata);
+            row = 0;
+        }
+        const int tok = static_cast<int>(row);
+        if ((warp & 1) == 0) {
             tma_load_3d(sm.k[i][0], &k_map, &sm.bar, 0, h, tok);
             tma_load_3d(sm.k[i][1], &k_map, &sm.bar, 64, h, tok);
+        } else {
             tma_load_3d(sm.v[i][0], &v_map, &sm.bar, 0, h, tok);
             tma_load_3d(sm.v[i][1], &v_map, &sm.bar, 64, h, tok);
         }
     }
-    __syncthreads();  // q visible to every warp
     bool kv_in_flight = false;  // a copy that did not land in time: waited for again before the CTA ends
     if (nmy > 0 && !__syncthreads_and(mbar_wait(&sm.bar, 0, a.err))) {
         nmy = 0;  // copy never landed: no keys
