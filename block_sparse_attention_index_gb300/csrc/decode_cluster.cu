@@ -108,9 +108,6 @@ __global__ void __launch_bounds__(kClThreads) decode_cluster_kernel(const __grid
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int H = a.H, G = a.G;
 
-    // a kernel launched after this one as a programmatic dependent may start its own
-    // set-up now; it waits for this grid to finish before it reads or writes anything
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     // ---- prologue: only inputs that no earlier kernel of the step writes
     const int nrows = a.cu_rows[b + 1] - a.cu_rows[b];
     // not a decode-family sequence, or no such row (the whole cluster returns)
@@ -138,6 +135,10 @@ __global__ void __launch_bounds__(kClThreads) decode_cluster_kernel(const __grid
         }
     }
     pdl_wait();  // the index scan (pooled scores, error word) is complete and visible
+    // A kernel launched after this one as a programmatic dependent may start now.  The
+    // scan's header clears (tickets of the prompt indexer) have landed by this point;
+    // a dependent that reads anything this grid writes waits for it to finish first.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (!meta_ok) {
         if (tid == 0 && rank == 0) atomicOr(a.err, kErrBadMetadata);
         return;  // the whole cluster returns: before any cluster barrier

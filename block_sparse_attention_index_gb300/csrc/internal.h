@@ -151,7 +151,7 @@ cudaError_t run_index_scores(const StagedArgs& a, const uint16_t* iq, const uint
                              int64_t ld, cudaStream_t stream);
 cudaError_t run_select_blocks(const StagedArgs& a, const float* scores, int64_t ld, int32_t* sel, int32_t* nsel,
                               cudaStream_t stream);
-cudaError_t run_prefill_index(const PrefillIndexArgs& a, cudaStream_t stream);
+cudaError_t run_prefill_index(const PrefillIndexArgs& a, bool after_decode, cudaStream_t stream);
 cudaError_t run_prefill_attend(const PrefillAttendArgs& a, cudaStream_t stream);
 cudaError_t run_wait_timeout_check(uint32_t* err, uint64_t limit_ns, cudaStream_t stream);
 

@@ -585,7 +585,9 @@ msa_status msa_forward_marked(const msa_problem* p, const void* q, const void* i
         ia.cand = reinterpret_cast<uint64_t*>(ws + l.idx_cand);
         ia.tickets = reinterpret_cast<int32_t*>(ws + l.idx_tickets);
         ia.err = reinterpret_cast<uint32_t*>(ws + l.err);
-        if ((e = msa::run_prefill_index(ia, st)) != cudaSuccess) return cuda_fail(e, "prefill indexer launch");
+        // behind the decode attention (no mark in between) the indexer overlaps its tail
+        const bool pdl = dec && (events == nullptr || n_events < 3 || events[2] == nullptr);
+        if ((e = msa::run_prefill_index(ia, pdl, st)) != cudaSuccess) return cuda_fail(e, "prefill indexer launch");
         if ((s = marks.mark(3)) != MSA_OK) return s;
         msa::PrefillAttendArgs pa = prefill_attend_args(p, &qm, &km, &vm, sel, nsel, out, ws, l);
         pa.only_multi_row = 1;

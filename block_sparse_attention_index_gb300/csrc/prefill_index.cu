@@ -90,6 +90,12 @@ __device__ __forceinline__ void insert_top15(uint64_t (&best)[15], uint64_t key)
     }
 }
 
+// Launched as a programmatic dependent of the decode attention (mixed batches), this
+// kernel reads nothing that grid writes, so it starts at once; but no CTA exits before
+// that grid has finished, so that work queued after this kernel on the stream also
+// comes after the decode attention.  A no-op in an ordinary launch.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __global__ void __launch_bounds__(kIdxThreads, 1) prefill_index_kernel(const __grid_constant__ CUtensorMap iq_map,
                                                                        const __grid_constant__ CUtensorMap ik_map,
                                                                        const PrefillIndexArgs a) {
@@ -134,7 +140,10 @@ __global__ void __launch_bounds__(kIdxThreads, 1) prefill_index_kernel(const __g
         fence_mbar_init();
     }
     __syncthreads();
-    if (sm.seq < 0) return;
+    if (sm.seq < 0) {
+        grid_dependency_wait();
+        return;
+    }
     if (warp == 9) tmem_alloc(&sm.tmem_base, 512);
     tc_fence_before();
     __syncthreads();
@@ -320,15 +329,28 @@ __global__ void __launch_bounds__(kIdxThreads, 1) prefill_index_kernel(const __g
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }
+    grid_dependency_wait();
 }
 
-cudaError_t run_prefill_index(const PrefillIndexArgs& a, cudaStream_t stream) {
+cudaError_t run_prefill_index(const PrefillIndexArgs& a, bool after_decode, cudaStream_t stream) {
     const size_t smem = sizeof(IndexSmem) + 1024;
     cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(prefill_index_kernel), smem);
     if (e != cudaSuccess) return e;
     const int tiles = (a.total_rows + kIdxRows - 1) / kIdxRows + a.num_seqs;  // upper bound
-    dim3 grid(tiles, a.H, a.nsplit);
-    prefill_index_kernel<<<grid, kIdxThreads, smem, stream>>>(*a.iq_map, *a.ik_map, a);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(tiles, a.H, a.nsplit);
+    cfg.blockDim = dim3(kIdxThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    // only behind the decode attention, whose outputs this kernel does not read; as the
+    // first kernel of a call it would overlap whatever the caller wrote iq or ik with
+    cfg.numAttrs = after_decode ? 1 : 0;
+    e = cudaLaunchKernelEx(&cfg, prefill_index_kernel, *a.iq_map, *a.ik_map, a);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
