@@ -50,7 +50,7 @@ struct __align__(1024) IndexSmem {
     int32_t seq, row0, nrows, ntiles, p0, L;
     int32_t n0, n1;  // this split's 256-position tiles [n0, n1)
     int32_t last;    // this CTA merges the splits' lists
-    uint64_t half_list[kIdxRows][15];  // the second epilogue half's best blocks per row
+    uint64_t half_list[kIdxRows][16];  // the second epilogue half's best blocks per row
 
 };
 
@@ -77,7 +77,11 @@ __device__ bool find_tile(const PrefillIndexArgs& a, int tile, int& b, int& i0, 
 // Barrier of the eight epilogue warps (threads 0-255) only.
 __device__ __forceinline__ void epilogue_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 
-__device__ __forceinline__ void insert_top15(uint64_t (&best)[15], uint64_t key) {
+// A thread's running list of its row's best blocks: key inserted into a sorted list
+// (descending; key 0 = none, every block's key is larger).  One insertion is a chain
+// of dependent compare-and-swaps; in the tile loop two warps a scheduler interleave
+// theirs, which sorting networks (more instructions) would not beat.
+__device__ __forceinline__ void insert_top(uint64_t (&best)[16], uint64_t key) {
     if (key <= best[14]) return;
     best[14] = key;
 #pragma unroll
@@ -90,10 +94,56 @@ __device__ __forceinline__ void insert_top15(uint64_t (&best)[15], uint64_t key)
     }
 }
 
+// Merging whole lists, at the end of a row, uses bitonic networks instead: an
+// insertion per key would chain 15 x 14 dependent steps with nothing else to run,
+// while each stage of a network has eight independent compare-and-swaps.  All
+// indices are compile-time constants, so the lists stay in registers.
+
+// Compare-and-swap: the larger key to a.
+__device__ __forceinline__ void cas_desc(uint64_t& a, uint64_t& b) {
+    const uint64_t hi = a > b ? a : b;
+    b = a > b ? b : a;
+    a = hi;
+}
+
+// best := the 16 largest keys of best and b, descending (both given descending;
+// best[15] and b[15] may be 0).  The elementwise maximum of best and b reversed
+// is a bitonic sequence holding them; the bitonic merge (four stages) sorts it.
+__device__ __forceinline__ void merge16_desc(uint64_t (&best)[16], const uint64_t (&b)[16]) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) best[i] = best[i] > b[15 - i] ? best[i] : b[15 - i];
+#pragma unroll
+    for (int stride = 8; stride > 0; stride >>= 1)
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const int l = i ^ stride;
+            if (l > i) cas_desc(best[i], best[l]);
+        }
+}
+
+// Bitonic sort of 16 block indices into ascending order.
+__device__ __forceinline__ void sort16_asc(int (&v)[16]) {
+#pragma unroll
+    for (int size = 2; size <= 16; size <<= 1)
+#pragma unroll
+        for (int stride = size >> 1; stride > 0; stride >>= 1)
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const int l = i ^ stride;
+                if (l > i) {
+                    const bool up = (i & size) == 0;  // ascending run
+                    const int lo = min(v[i], v[l]), hi = max(v[i], v[l]);
+                    v[i] = up ? lo : hi;
+                    v[l] = up ? hi : lo;
+                }
+            }
+}
+
 // Launched as a programmatic dependent of the decode attention (mixed batches), this
-// kernel reads nothing that grid writes, so it starts at once; but no CTA exits before
-// that grid has finished, so that work queued after this kernel on the stream also
-// comes after the decode attention.  A no-op in an ordinary launch.
+// kernel reads nothing that grid writes, so it starts at once; but every working CTA
+// (and CTA 0 in any case) waits for that grid to finish before it exits, so this grid
+// cannot finish first and work queued after it on the stream also comes after the
+// decode attention.  A no-op in an ordinary launch.
 __device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 __global__ void __launch_bounds__(kIdxThreads, 1) prefill_index_kernel(const __grid_constant__ CUtensorMap iq_map,
@@ -140,8 +190,8 @@ __global__ void __launch_bounds__(kIdxThreads, 1) prefill_index_kernel(const __g
         fence_mbar_init();
     }
     __syncthreads();
-    if (sm.seq < 0) {
-        grid_dependency_wait();
+    if (sm.seq < 0) {  // no tile here: leave the SM to working CTAs, but CTA 0 always waits
+        if (blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0) grid_dependency_wait();
         return;
     }
     if (warp == 9) tmem_alloc(&sm.tmem_base, 512);
@@ -238,9 +288,11 @@ __global__ void __launch_bounds__(kIdxThreads, 1) prefill_index_kernel(const __g
         bool live = row < sm.nrows;
         const int p = sm.p0 + row;
         const int J = p / kBlock;
-        uint64_t best[15];
+        // best[0..14]: the 15 best keys so far, descending; best[15] stays 0 (a slot for the
+        // merges below)
+        uint64_t best[16];
 #pragma unroll
-        for (int i = 0; i < 15; ++i) best[i] = 0;
+        for (int i = 0; i < 16; ++i) best[i] = 0;
         const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
         for (int n = n0; n < n1; ++n) {
             const int acc = (n - n0) & 1;
@@ -253,7 +305,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1) prefill_index_kernel(const __g
                 tmem_ld_max64(lane_addr + acc * kIdxCols + jb * kBlock, m);
                 tmem_ld_wait();
                 if (!live || j >= J) continue;  // the local block is forced; later blocks are in the future
-                insert_top15(best, block_key(m, j));
+                insert_top(best, block_key(m, j));
             }
             tc_fence_before();
             mbar_arrive(&sm.acc_empty[acc]);
@@ -261,12 +313,14 @@ __global__ void __launch_bounds__(kIdxThreads, 1) prefill_index_kernel(const __g
         // the two halves' lists of a row into one (blocks are disjoint)
         if (half == 1 && live) {
 #pragma unroll
-            for (int i = 0; i < 15; ++i) sm.half_list[row][i] = best[i];
+            for (int i = 0; i < 16; ++i) sm.half_list[row][i] = best[i];
         }
         epilogue_sync();
         if (half == 0 && live) {
+            uint64_t other[16];
 #pragma unroll
-            for (int i = 0; i < 15; ++i) insert_top15(best, sm.half_list[row][i]);
+            for (int i = 0; i < 16; ++i) other[i] = sm.half_list[row][i];
+            merge16_desc(best, other);
         }
         if (half == 1) live = false;  // half 0 finishes the row
         if (a.nsplit > 1) {
@@ -287,11 +341,28 @@ __global__ void __launch_bounds__(kIdxThreads, 1) prefill_index_kernel(const __g
             } else {
                 __threadfence();
                 if (live) {
+                    // the other splits' lists (15 keys each, descending), the next one loading
+                    // while the current one is merged
                     const uint64_t* lists = a.cand + (static_cast<int64_t>(sm.row0 + row) * a.H + h) * a.nsplit * 15;
-                    for (int sp = 0; sp < a.nsplit; ++sp) {
-                        if (sp == static_cast<int>(blockIdx.z)) continue;
+                    const int me = static_cast<int>(blockIdx.z);
+                    int sp = me == 0 ? 1 : 0;  // the first other split (nsplit >= 2)
+                    uint64_t cur[16], nxt[16];
+                    cur[15] = nxt[15] = 0;
 #pragma unroll
-                        for (int i = 0; i < 15; ++i) insert_top15(best, __ldcg(lists + sp * 15 + i));
+                    for (int i = 0; i < 15; ++i) cur[i] = __ldcg(lists + sp * 15 + i);
+                    while (true) {
+                        int sn = sp + 1;
+                        if (sn == me) ++sn;
+                        const bool more = sn < a.nsplit;
+                        if (more) {
+#pragma unroll
+                            for (int i = 0; i < 15; ++i) nxt[i] = __ldcg(lists + sn * 15 + i);
+                        }
+                        merge16_desc(best, cur);
+                        if (!more) break;
+#pragma unroll
+                        for (int i = 0; i < 15; ++i) cur[i] = nxt[i];
+                        sp = sn;
                     }
                 }
             }
@@ -308,18 +379,12 @@ __global__ void __launch_bounds__(kIdxThreads, 1) prefill_index_kernel(const __g
                 for (int i = 0; i < 16; ++i)
                     if (i == others) v[i] = J;
             }
-#pragma unroll
-            for (int i = 0; i < 16; ++i)
-#pragma unroll
-                for (int k = 0; k < 15 - i; ++k)
-                    if (v[k] > v[k + 1]) {
-                        const int t = v[k];
-                        v[k] = v[k + 1];
-                        v[k + 1] = t;
-                    }
+            sort16_asc(v);
             const int r = sm.row0 + row;
             int32_t* out = a.sel + (static_cast<int64_t>(r) * a.H + h) * a.top_k;
-            for (int i = 0; i < a.top_k; ++i) out[i] = v[i] == 0x7fffffff ? -1 : v[i];
+#pragma unroll
+            for (int i = 0; i < kMaxTopK; ++i)  // unrolled: v stays in registers
+                if (i < a.top_k) out[i] = v[i] == 0x7fffffff ? -1 : v[i];
             a.nsel[static_cast<int64_t>(r) * a.H + h] = others + 1;
         }
     }
