@@ -114,3 +114,24 @@ def test_prefill_long_prefix():
     ref = oracle_forward(w, x)
     assert_selection_equal(sel, nsel, ref)
     assert_out_close(out, ref["out"], torch.float32)
+
+
+@pytest.mark.parametrize("H,seqs,ties", [
+    (2, [(2200, 6000)], False),              # 4 position ranges per (row tile, head) on 152 SMs
+    (2, [(900, 2000), (33, 2100)], True),    # 4 ranges, every index score equal
+    (4, [(700, 3333)], False),               # 5 ranges, ragged row tile and position tail
+    (1, [(20, 40000)], False),               # 8 ranges over 157 position tiles
+])
+def test_prefill_position_splits(H, seqs, ties):
+    """The indexer's position ranges: each range keeps its own list of the best
+    blocks and the last range to finish merges them all.  With every score
+    equal, each range holds its lowest blocks and the merge must still keep
+    the lowest overall (ties to the lower block)."""
+    w = synth.Workload("pre_splits", H=H, G=16, seqs=seqs, seed=61 + H + len(seqs))
+    x = synth.make_inputs(w)
+    if ties:
+        x["ik"][:] = x["ik"][0, 0, :]
+    out, sel, nsel = run_forward(w, x)
+    ref = oracle_forward(w, x)
+    assert_selection_equal(sel, nsel, ref)
+    assert_out_close(out, ref["out"], torch.float32)
