@@ -77,27 +77,26 @@ __device__ bool find_tile(const PrefillIndexArgs& a, int tile, int& b, int& i0, 
 // Barrier of the eight epilogue warps (threads 0-255) only.
 __device__ __forceinline__ void epilogue_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 
-// A thread's running list of its row's best blocks: key inserted into a sorted list
-// (descending; key 0 = none, every block's key is larger).  One insertion is a chain
-// of dependent compare-and-swaps; in the tile loop two warps a scheduler interleave
-// theirs, which sorting networks (more instructions) would not beat.
+// A thread's running list of its row's best blocks: key inserted into best[0..14]
+// (descending; key 0 = none, every block's key is larger; keys are distinct).  As the
+// list is sorted, "key goes above slot i" is one comparison per slot, all independent,
+// and each slot's new value is a select on the old list: slot i keeps its key, takes
+// the new one (the first slot it beats) or takes its upper neighbour's.  Depth ~4
+// instead of a chain of 14 dependent compare-and-swaps, for about as many instructions.
 __device__ __forceinline__ void insert_top(uint64_t (&best)[16], uint64_t key) {
     if (key <= best[14]) return;
-    best[14] = key;
+    bool above[15];
 #pragma unroll
-    for (int i = 14; i > 0; --i) {
-        if (best[i] > best[i - 1]) {
-            const uint64_t t = best[i];
-            best[i] = best[i - 1];
-            best[i - 1] = t;
-        }
-    }
+    for (int i = 0; i < 15; ++i) above[i] = key > best[i];
+#pragma unroll
+    for (int i = 14; i > 0; --i) best[i] = above[i] ? (above[i - 1] ? best[i - 1] : key) : best[i];
+    best[0] = above[0] ? key : best[0];
 }
 
-// Merging whole lists, at the end of a row, uses bitonic networks instead: an
-// insertion per key would chain 15 x 14 dependent steps with nothing else to run,
-// while each stage of a network has eight independent compare-and-swaps.  All
-// indices are compile-time constants, so the lists stay in registers.
+// Merging whole lists, at the end of a row, uses bitonic networks instead of 15
+// insertions one after another: 16 maxima and four stages of eight independent
+// compare-and-swaps.  All indices are compile-time constants, so the lists stay in
+// registers.
 
 // Compare-and-swap: the larger key to a.
 __device__ __forceinline__ void cas_desc(uint64_t& a, uint64_t& b) {
