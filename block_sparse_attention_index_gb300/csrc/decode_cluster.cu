@@ -114,7 +114,8 @@ __global__ void __launch_bounds__(kClThreads) decode_cluster_kernel(const __grid
     if (nrows < 1 || nrows > kDecodeMaxRows || row_in_seq >= nrows) return;
     const int r = a.cu_rows[b] + row_in_seq;
     const int L = a.cache_lens[b];
-    const bool meta_ok = !(r < 0 || r >= a.total_rows || L < nrows || L > a.max_cache_len) &&
+    // nrows > rows_per_seq: more rows than the grid and the pooled scores have slots for
+    const bool meta_ok = !(r < 0 || r >= a.total_rows || L < nrows || L > a.max_cache_len || nrows > a.rows_per_seq) &&
                          seq_rows_ok(a.cache, b, L, a.cache_tokens);
     if (tid == 0) {
         mbar_init(&sm.bar, 1);

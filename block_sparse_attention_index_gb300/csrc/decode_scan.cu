@@ -68,8 +68,11 @@ __device__ __forceinline__ bool scan_locate(const ScanArgs& a, const int32_t* pr
         const int r = a.cu_rows[b];
         const int nr = min(max(a.cu_rows[b + 1] - r, 1), kDecodeMaxRows);
         const int L = min(max(a.cache_lens[b], 0), a.max_cache_len);
-        const bool ok = r >= 0 && r + nr <= a.total_rows && L >= nr && seq_rows_ok(a.cache, b, L, a.cache_tokens);
-        st.L = ok ? L : 0;  // inconsistent metadata: the sequence is skipped
+        // more rows than the pooled-score slots of a sequence (max_rows_per_seq understated) would
+        // write into the next sequence's slots or past the buffer: inconsistent, like the rest
+        const bool ok = r >= 0 && r + nr <= a.total_rows && L >= nr && nr <= a.rows_per_seq &&
+                        seq_rows_ok(a.cache, b, L, a.cache_tokens);
+        st.L = ok ? L : 0;  // inconsistent metadata: the sequence is skipped (the attention sets the error word)
         st.n = ok ? nr : 1;
         st.r = ok ? r : 0;
         return true;

@@ -133,8 +133,10 @@ const char* msa_last_error(void);
  * 256-byte aligned; its contents need no initialisation and are clobbered.
  * Its first 4 bytes are the device error word of the last call that used
  * it: 0, or a bitwise OR of 1 (a bounded wait gave up), 2 (device metadata
- * outside the host-side bounds), 4 (tensor memory could not be allocated);
- * valid once that call has completed on the stream. */
+ * outside the host-side bounds, e.g. a sequence with more rows than
+ * max_rows_per_seq; such a sequence is skipped, nothing is written outside
+ * the buffers), 4 (tensor memory could not be allocated); valid once that
+ * call has completed on the stream. */
 msa_status msa_workspace_size(const msa_problem* p, size_t* bytes);
 
 /* Stage 1 alone: the lightning-indexer scores

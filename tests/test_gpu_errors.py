@@ -70,6 +70,26 @@ def test_given_selection_outside_causal_range_flagged(kind):
     assert m.error_word(ws) & BAD_METADATA
 
 
+@pytest.mark.parametrize("seqs,claimed", [([(1, 3000), (3, 2000)], 1), ([(1, 3000), (3, 2000), (1, 1500)], 2)])
+def test_rows_beyond_max_rows_per_seq_flagged(seqs, claimed):
+    """max_rows_per_seq understated: a decode-family sequence has more rows than
+    the pooled scores give each sequence slots for (min(max_rows_per_seq, 8)).
+    The scan skips that sequence (no write into the next sequence's slots or
+    past the buffer) and the attention sets the error word; a clean call
+    afterwards is exact."""
+    w = synth.Workload("err_rows", H=2, G=16, seqs=seqs, seed=84)
+    x = synth.make_inputs(w)
+
+    def mutate(pb):
+        pb.c.max_rows_per_seq = claimed
+
+    assert forward_with(w, x, mutate) & BAD_METADATA
+    out, sel, nsel = run_forward(w, x)
+    ref = oracle_forward(w, x)
+    assert_selection_equal(sel, nsel, ref)
+    assert_out_close(out, ref["out"], torch.float32)
+
+
 def test_bounded_wait_runs_out_and_the_context_stays_usable():
     """A barrier wait that nothing completes gives up after its limit, sets the
     timeout bit of the error word and returns; the next call is exact."""
