@@ -169,7 +169,7 @@ msa_status msa_attend_decode(const msa_problem* p, const void* q, const void* k_
                              void* out, void* workspace, size_t workspace_bytes, void* stream);
 
 /* Stage 3, decode form, for callers that cannot allocate device memory.
- * The paper has no counterpart: this is a deployment variant of
+ * The pages describe no counterpart: this is a deployment variant of
  * msa_attend_decode.  Some callers cannot call cudaMalloc at all -- code
  * enqueued while a framework captures a CUDA graph and forbids allocation
  * inside the capture, hosts whose device memory is carved out once at
