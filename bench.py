@@ -84,7 +84,29 @@ def work_counts(w: synth.Workload):
             idx_flops += 2 * Di * (p + 1) * H
             att_flops += 4 * D * _kept_keys(p, w.top_k) * H * G
     return dict(scan_bytes=scan_bytes, dec_att_bytes=att_bytes, idx_flops=idx_flops, att_flops=att_flops,
-                dec_rows=sum(n for n, _ in dec), pre_rows=sum(n for n, _ in pre))
+                att_exec_flops=prefill_executed_flops(w), dec_rows=sum(n for n, _ in dec),
+                pre_rows=sum(n for n, _ in pre))
+
+
+# Tensor-core FLOPs the prompt-chunk attention issues for one pair of kept
+# blocks (128 keys) of one (row, KV head): S^T = K_pair . Q^T (M = 128 keys,
+# N = 16 head columns, K = 128 dims) and O^T += V_pair^T . [P_hi; P_lo]^T
+# (M = 128 dims, N = 32, K = 128 keys).  Masked keys (past p, the duplicate of
+# an odd last block) and the head columns past G are issued too.
+EXEC_FLOPS_PER_PAIR = 2 * 128 * 16 * 128 + 2 * 128 * 32 * 128
+
+
+def prefill_executed_flops(w: synth.Workload):
+    """FLOPs the prompt-chunk attention kernel issues on the tensor cores (the
+    kept-block FLOPs of work_counts, plus padding and the second P part)."""
+    total = 0
+    for n, L in w.seqs:
+        if n <= DECODE_MAX_ROWS:
+            continue
+        for i in range(n):
+            nsel = min(w.top_k, (L - n + i) // w.S + 1)
+            total += (nsel + 1) // 2 * EXEC_FLOPS_PER_PAIR * w.H
+    return total
 
 
 L2_BYTES = 129 << 20
@@ -575,6 +597,36 @@ def flushed_latency(res, rows, ws):
             "note": "one step per graph replay after an L2 flush, begin and end marks in line"}
 
 
+def _traffic_source(summary_name, traffic):
+    """Where roofline.traffic comes from: a committed ncu capture of the same
+    kernel source (not measured in this run), or nothing."""
+    if traffic is None:
+        return None
+    return f"committed ncu capture profiles/{summary_name} (kernel source hash matches); not measured in this run"
+
+
+def part_work(w, res, hbm, bf16):
+    """Each stage's algorithmic work and, where its marked stage time exists,
+    its fraction of the measured peak (mixed batches report every part)."""
+    wc = work_counts(w)
+    st = res["stage_ms"]
+    out = {}
+    if wc["dec_rows"]:
+        out["decode_scan"] = {"bytes": wc["scan_bytes"], "us": round(st[0] * 1e3, 2),
+                              "hbm_frac": round(wc["scan_bytes"] / (st[0] * 1e-3) / 1e9 / hbm, 4) if st[0] > 0 else None}
+        out["decode_attend"] = {"bytes": wc["dec_att_bytes"], "us": round(st[1] * 1e3, 2),
+                                "hbm_frac": round(wc["dec_att_bytes"] / (st[1] * 1e-3) / 1e9 / hbm, 4) if st[1] > 0 else None}
+    if wc["pre_rows"]:
+        out["prefill_index"] = {"flops": wc["idx_flops"], "us": round(st[2] * 1e3, 2),
+                                "bf16_frac": round(wc["idx_flops"] / (st[2] * 1e-3) / 1e12 / bf16, 4) if st[2] > 0 else None}
+        out["prefill_attend"] = {"flops": wc["att_flops"], "executed_flops": wc["att_exec_flops"],
+                                 "us": round(st[3] * 1e3, 2),
+                                 "bf16_frac": round(wc["att_flops"] / (st[3] * 1e-3) / 1e12 / bf16, 4) if st[3] > 0 else None,
+                                 "executed_bf16_frac": (round(wc["att_exec_flops"] / (st[3] * 1e-3) / 1e12 / bf16, 4)
+                                                        if st[3] > 0 else None)}
+    return out
+
+
 def roofline_for(w, res, hbm, bf16, bf16_sus, peak_kind):
     wc = work_counts(w)
     stage = res["stage_ms"]  # [decode scan, decode attention, prefill index, prefill attention]
@@ -583,17 +635,38 @@ def roofline_for(w, res, hbm, bf16, bf16_sus, peak_kind):
         traffic = ncu_traffic("decode_scan_4x65536.md", ["decode_scan.cu", "common.cuh"]) if w.name == "decode_4x65536" else None
         return {"kernel": "decode_scan_kernel", "bound": "hbm", "achieved": round(achieved, 1), "peak": hbm,
                 "unit": "GB/s", "frac": round(achieved / hbm, 4), "traffic": traffic,
+                "traffic_source": _traffic_source("decode_scan_4x65536.md", traffic),
                 "algorithmic_bytes": wc["scan_bytes"], "kernel_us": round(stage[0] * 1e3, 2),
                 "peak_source": f"{peak_kind} hbm_gbs (copy)"}
     if stage[3] > 0:
         achieved = wc["att_flops"] / (stage[3] * 1e-3) / 1e12
         traffic = (ncu_traffic("prefill_attend_4096_at_8192.md", ["prefill_attend.cu", "common.cuh"])
                    if w.name == "prefill_4096_at_8192" else None)
+        executed = wc["att_exec_flops"] / (stage[3] * 1e-3) / 1e12
         return {"kernel": "prefill_attend_kernel", "bound": "tensor", "achieved": round(achieved, 1), "peak": bf16,
                 "unit": "TFLOP/s", "frac": round(achieved / bf16, 4), "traffic": traffic,
-                "algorithmic_flops": wc["att_flops"], "kernel_us": round(stage[3] * 1e3, 2),
-                "peak_source": f"{peak_kind} bf16_tflops (burst)"}
+                "traffic_source": _traffic_source("prefill_attend_4096_at_8192.md", traffic),
+                "algorithmic_flops": wc["att_flops"], "executed_flops": wc["att_exec_flops"],
+                "executed_tflops": round(executed, 1), "executed_frac": round(executed / bf16, 4),
+                "kernel_us": round(stage[3] * 1e3, 2), "peak_source": f"{peak_kind} bf16_tflops (burst)"}
     return None
+
+
+def l2_note(w, use_graph=True):
+    """How the L2 is kept out of the timing for workload w (the rule this
+    bench applies to it; the same words in both arms' config)."""
+    sets = rotation_sets(w)
+    if sets > 1 and use_graph:
+        return (f"inputs larger than L2: {sets} rotating copies of the inputs, steps back to back in one CUDA graph "
+                "(an L2 flush, begin mark, K msa_forward calls, end mark)")
+    return "flushed before every step (512 MiB write, then 256 MiB read)"
+
+
+def config_for(w, world_size, use_graph=True):
+    """The workload description printed by both arms (identical dicts)."""
+    return {"workload": w.name, "note": w.note, "H": w.H, "G": w.G, "head_dim": w.D, "index_dim": w.Di,
+            "block": w.S, "top_k": w.top_k, "rows_per_gpu": w.total_rows, "cache_tokens_per_gpu": w.cache_tokens,
+            "l2": l2_note(w, use_graph), "parallelism": f"replicas x{world_size}"}
 
 
 def main():
@@ -638,10 +711,9 @@ def main():
                 "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
                 "ms_per_step": 1e3 * t_total / steps_done, "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-                "config": {"workload": w.name, "note": w.note, "H": w.H, "G": w.G, "rows": w.total_rows,
-                           "sample_rows": len(rows)},
+                "config": config_for(w, ws, use_graph=not args.no_graph),
                 "cpu_baseline": {"kind": "oracle", "cores": r["cores"], "sample": r["sample"], "value": value,
-                                 "unit": "rows/s"},
+                                 "unit": "rows/s", "sample_rows": len(rows)},
                 "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
         print(json.dumps(line))
         return
@@ -661,15 +733,13 @@ def main():
     line = {"metric": _metric_for(w), "value": round(value, 1), "unit": "rows/s", "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(step_ms(res), 5), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": w.name, "note": w.note, "H": w.H, "G": w.G, "head_dim": w.D, "index_dim": w.Di,
-                       "block": w.S, "top_k": w.top_k, "rows_per_gpu": rows,
-                       "cache_tokens_per_gpu": w.cache_tokens, "l2": timing_note(res),
-                       "launch": ("CUDA graph: L2 flush, begin mark, one msa_forward, end mark (marks in line)"
-                                  if res.get("flush_in_graph") and "b2b_ms_per_step" not in res
-                                  else "CUDA graph: L2 flush, begin mark, K msa_forward calls, end mark"
-                                  if "b2b_ms_per_step" in res
-                                  else "CUDA graph replay of one msa_forward" if res["graph"] else "direct msa_forward calls"),
-                       "parallelism": f"replicas x{ws}"},
+            "config": config_for(w, ws, use_graph=not args.no_graph),
+            "l2": timing_note(res),
+            "launch": ("CUDA graph: L2 flush, begin mark, one msa_forward, end mark (marks in line)"
+                       if res.get("flush_in_graph") and "b2b_ms_per_step" not in res
+                       else "CUDA graph: L2 flush, begin mark, K msa_forward calls, end mark"
+                       if "b2b_ms_per_step" in res
+                       else "CUDA graph replay of one msa_forward" if res["graph"] else "direct msa_forward calls"),
             "stage_us": {"decode_scan": round(res["stage_ms"][0] * 1e3, 2),
                          "decode_attend": round(res["stage_ms"][1] * 1e3, 2),
                          "prefill_index": round(res["stage_ms"][2] * 1e3, 2),
@@ -707,7 +777,7 @@ def main():
                              "stage_us": {"prefill_index": round(res2["stage_ms"][2] * 1e3, 2),
                                           "prefill_attend": round(res2["stage_ms"][3] * 1e3, 2)},
                              "roofline": roofline_for(w2, res2, hbm, bf16, bf16_sus, peak_kind),
-                             "gpu_launches": res2["launches"]}
+                             "parts": part_work(w2, res2, hbm, bf16), "gpu_launches": res2["launches"]}
         line["gpu_launches"] += res2["launches"]
     if args.paged_page_size > 0:
         resp = measure_gpu(w, args.steps, args.warmup, dev, dist_on, with_e2e=False, use_graph=not args.no_graph,
@@ -763,7 +833,7 @@ def main():
                            "latency_flushed": flushed_latency(res5, w5.total_rows, ws),
                            "stage_us": {k: round(v * 1e3, 2) for k, v in zip(
                                ("decode_scan", "decode_attend", "prefill_index", "prefill_attend"), res5["stage_ms"])},
-                           "roofline": rf,
+                           "roofline": rf, "parts": part_work(w5, res5, hbm, bf16),
                            "decode_step_hbm_frac": (round(sb / (step_ms(res5) * 1e-3) / 1e9 / hbm, 4)
                                                     if wc5["pre_rows"] == 0 and sb else None)})
             line["gpu_launches"] += res5["launches"]

@@ -17,6 +17,8 @@
 //   - it writes (m, l, O) for its block; the last split to finish (atomic
 //     ticket) combines the partials:  M = max_s m_s,  L = sum_s l_s 2^(m_s-M),
 //     out = sum_s O_s 2^(m_s-M) / L.
+#include <cudaTypedefs.h>
+
 #include <mutex>
 
 #include "common.cuh"
@@ -79,7 +81,10 @@ __global__ void __launch_bounds__(kAttThreads) decode_attend_kernel(const __grid
     const int H = a.H, G = a.G;
 
     const int r = a.cu_rows[b];
-    if (a.cu_rows[b + 1] - r != 1) return;  // not a decode sequence
+    if (a.cu_rows[b + 1] - r != 1) {  // not a one-row sequence: the host bound said every one is
+        if (tid == 0 && split == 0) atomicOr(a.err, kErrBadMetadata);
+        return;
+    }
     const int L = a.cache_lens[b];
     if (r < 0 || r >= a.total_rows || L < 1 || L > a.max_cache_len || !seq_rows_ok(a.cache, b, L, a.cache_tokens)) {
         if (tid == 0 && split == 0) atomicOr(a.err, kErrBadMetadata);
@@ -94,8 +99,24 @@ __global__ void __launch_bounds__(kAttThreads) decode_attend_kernel(const __grid
     }
     // ---- selection
     if constexpr (kSelGiven) {
+        const int nraw = a.nsel_in[static_cast<int64_t>(r) * H + h];  // the same in every thread
+        if (nraw < 1 || nraw > a.top_k) {
+            if (tid == 0 && split == 0) atomicOr(a.err, kErrBadMetadata);
+            if (nraw < 1) {  // no kept block: the softmax is empty; split 0 writes zeros
+                if (split == 0) {
+                    const int64_t o0 = (static_cast<int64_t>(r) * H * G + static_cast<int64_t>(h) * G) * kHeadDim;
+                    for (int i = tid; i < G * kHeadDim; i += kAttThreads) {
+                        if (a.out_bf16)
+                            reinterpret_cast<__nv_bfloat16*>(a.out)[o0 + i] = __float2bfloat16_rn(0.f);
+                        else
+                            reinterpret_cast<float*>(a.out)[o0 + i] = 0.f;
+                    }
+                }
+                return;
+            }
+        }
         if (tid < kMaxTopK) sm.sel[tid] = tid < a.top_k ? a.sel_in[(static_cast<int64_t>(r) * H + h) * a.top_k + tid] : -1;
-        if (tid == 0) sm.nsel = min(max(a.nsel_in[static_cast<int64_t>(r) * H + h], 0), a.top_k);
+        if (tid == 0) sm.nsel = min(nraw, a.top_k);
         __syncthreads();
     } else {
         const float* pooled = a.pooled + (static_cast<int64_t>(b) * H + h) * a.max_blocks;
@@ -358,24 +379,68 @@ static_assert(kNoAllocMaxPairs * sizeof(int32_t) + 16 <= kNoAllocHeader, "ticket
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocBytes];
 
+// The array's device address, cached per CUDA context.  A context has its own
+// copy of the module and so its own address; after cudaDeviceReset (or a
+// release and re-creation of the primary context) the device gets a new
+// context whose ID differs, so a stale address is never reused.
+struct NoAllocEntry {
+    unsigned long long ctx_id;
+    void* base;
+};
 std::mutex g_noalloc_mutex;
-void* g_noalloc_base[64] = {nullptr};  // device address of the array, per device
+NoAllocEntry g_noalloc_cache[64];
+int g_noalloc_used = 0;
+int g_noalloc_next = 0;  // slot replaced when the cache is full (round robin)
 
-// Device address of the array on the current device.  Looked up once per
-// device (host code may not use the symbol itself as a device pointer).
+PFN_cuCtxGetCurrent_v4000 g_ctx_current = nullptr;
+PFN_cuCtxGetId_v12000 g_ctx_id = nullptr;
+
+// ID of the calling thread's current context (0 if there is none yet).
+cudaError_t current_context_id(unsigned long long* id) {
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_ctx_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(fn);
+        fn = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_ctx_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(fn);
+    });
+    if (g_ctx_current == nullptr || g_ctx_id == nullptr) return cudaErrorNotSupported;
+    CUcontext ctx = nullptr;
+    if (g_ctx_current(&ctx) != CUDA_SUCCESS) return cudaErrorUnknown;
+    *id = 0;
+    if (ctx == nullptr) return cudaSuccess;
+    return g_ctx_id(ctx, id) == CUDA_SUCCESS ? cudaSuccess : cudaErrorUnknown;
+}
+
+// Device address of the array in the current context (host code may not use
+// the symbol itself as a device pointer).  The first call in a context looks
+// it up with cudaGetSymbolAddress (which also makes the runtime set up the
+// device's primary context if nothing has yet); later calls reuse it.
 cudaError_t noalloc_base(void** out) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    unsigned long long id = 0;
+    cudaError_t e = current_context_id(&id);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     std::lock_guard<std::mutex> lock(g_noalloc_mutex);
-    if (g_noalloc_base[dev] == nullptr) {
-        void* ptr = nullptr;
-        e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
-        if (e != cudaSuccess) return e;
-        g_noalloc_base[dev] = ptr;
+    if (id != 0)
+        for (int i = 0; i < g_noalloc_used; ++i)
+            if (g_noalloc_cache[i].ctx_id == id) {
+                *out = g_noalloc_cache[i].base;
+                return cudaSuccess;
+            }
+    void* ptr = nullptr;
+    e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+    if (e != cudaSuccess) return e;
+    if (id == 0 && (e = current_context_id(&id)) != cudaSuccess) return e;  // the lookup created the context
+    if (id != 0) {
+        const int slot = g_noalloc_used < 64 ? g_noalloc_used++ : (g_noalloc_next++ & 63);
+        g_noalloc_cache[slot] = NoAllocEntry{id, ptr};
     }
-    *out = g_noalloc_base[dev];
+    *out = ptr;
     return cudaSuccess;
 }
 

@@ -135,6 +135,8 @@ __global__ void __launch_bounds__(kClThreads) decode_cluster_kernel(const __grid
             if (tid == 0) sm.nsel = min(max(a.nsel_in[static_cast<int64_t>(r) * H + h], 0), a.top_k);
         }
     }
+    // a given count of kept blocks (the same in every thread of the cluster)
+    const int nsel_given = kSelGiven && meta_ok ? a.nsel_in[static_cast<int64_t>(r) * H + h] : 1;
     pdl_wait();  // the index scan (pooled scores, error word) is complete and visible
     // A kernel launched after this one as a programmatic dependent may start now.  The
     // scan's header clears (tickets of the prompt indexer) have landed by this point;
@@ -143,6 +145,20 @@ __global__ void __launch_bounds__(kClThreads) decode_cluster_kernel(const __grid
     if (!meta_ok) {
         if (tid == 0 && rank == 0) atomicOr(a.err, kErrBadMetadata);
         return;  // the whole cluster returns: before any cluster barrier
+    }
+    if (nsel_given < 1 || nsel_given > a.top_k) {
+        if (tid == 0 && rank == 0) atomicOr(a.err, kErrBadMetadata);
+        if (nsel_given < 1) {  // no kept block: the softmax is empty; the outputs are zeros
+            const int g = 2 * rank + (tid >> 6), d = (tid & 63) * 2;  // CTA `rank` owns heads 2 rank, 2 rank + 1
+            if (g < G) {
+                const int64_t oi = (static_cast<int64_t>(r) * H * G + static_cast<int64_t>(h) * G + g) * kHeadDim + d;
+                if (a.out_bf16)
+                    *reinterpret_cast<uint32_t*>(reinterpret_cast<__nv_bfloat16*>(a.out) + oi) = pack_bf16x2(0.f, 0.f);
+                else
+                    *reinterpret_cast<float2*>(reinterpret_cast<float*>(a.out) + oi) = make_float2(0.f, 0.f);
+            }
+            return;  // every CTA of the cluster takes this branch, before any cluster barrier
+        }
     }
     cluster_arrive_relaxed();  // matched by cluster_wait() before the first remote store
     const int p = L - nrows + row_in_seq;  // this row's position

@@ -57,8 +57,11 @@
  *     1 <= G <= 16, H in {1, 2, 4, 8}, max_cache_len <= 2^21,
  *     num_seqs <= 4096; other values return MSA_ERR_UNSUPPORTED.
  *   - Thread safety: calls from several host threads are safe; the only
- *     library state is a per-device set-up flag and the thread-local error
- *     message.  Two calls sharing one workspace must be ordered on the GPU.
+ *     library state is per-device set-up (kernel shared-memory limits, the
+ *     SM count), the thread-local error message and, for
+ *     msa_attend_decode_noalloc alone, its scratch array and the per-context
+ *     cache of that array's address.  Two calls sharing one workspace must
+ *     be ordered on the GPU.
  */
 #ifndef MSA_H_
 #define MSA_H_
@@ -122,14 +125,17 @@ typedef struct msa_problem {
     int32_t index_key_heads;
 } msa_problem;
 
-/* Human-readable name of a status code (static string). */
+/* Human-readable name of a status code (static string).  Library mechanics:
+ * the pages define no interface for the method. */
 const char* msa_status_string(msa_status status);
 
-/* Message describing the calling thread's most recent failure ("" if none). */
+/* Message describing the calling thread's most recent failure ("" if none).
+ * Library mechanics (no counterpart in the pages). */
 const char* msa_last_error(void);
 
 /* Bytes of scratch that msa_forward, msa_attend_decode and msa_attend_prefill
- * need for problem p (host only; enqueues nothing).  The workspace must be
+ * need for problem p (host only; enqueues nothing).  Library mechanics (no
+ * counterpart in the pages).  The workspace must be
  * 256-byte aligned; its contents need no initialisation and are clobbered.
  * Its first 4 bytes are the device error word of the last call that used
  * it: 0, or a bitwise OR of 1 (a bounded wait gave up), 2 (device metadata
@@ -139,7 +145,12 @@ const char* msa_last_error(void);
  * call has completed on the stream. */
 msa_status msa_workspace_size(const msa_problem* p, size_t* bytes);
 
-/* Stage 1 alone: the lightning-indexer scores
+/* Stage 1 alone: the lightning-indexer scores.  PR #1388, native Metal family
+ * commit: the indexer scores the cached keys for each row and key head;
+ * "MiniMax-M3 on 4x RTX PRO 6000 Blackwell (SM120)", section "Alternative:
+ * NVFP4 (SGLang)": the model's sparse layers carry this lightning indexer.
+ * The pages give no formula; the score taken here is the plain dot product
+ * of the row's index query with the position's index key:
  *   scores[r, h, t] = iq[r,h,:] . ik[t,h,:]   (fp32)   for t <= p,
  *   scores[r, h, t] = -inf                             for p < t < ld.
  * scores is [total_rows, H, ld] fp32 with ld >= max_cache_len.  fp32
@@ -150,19 +161,29 @@ msa_status msa_workspace_size(const msa_problem* p, size_t* bytes);
 msa_status msa_index_scores(const msa_problem* p, const void* iq, const void* ik_cache,
                             float* scores, int64_t ld, void* stream);
 
-/* Stage 2 alone: block max-pool of `scores` (as written by msa_index_scores,
- * entries past p ignored) and top-k selection with the forced local block,
- * ties to the lower block index.  Writes sel and nsel. */
+/* Stage 2 alone.  "MiniMax-M3 on 4x RTX PRO 6000 Blackwell (SM120)", section
+ * "What this fixes": blocks are scored by the maximum of their index scores,
+ * 16 blocks are kept per GQA group and the block holding the current
+ * position is always among them; PR #1388, native Metal family commit: the
+ * selection is made per row and key head.  Block max-pool of `scores` (as
+ * written by msa_index_scores, entries past p ignored), then the local block
+ * J plus the top_k-1 best blocks j < J, ties to the lower block index (every
+ * block 0..J when J < top_k), listed ascending.  Writes sel and nsel. */
 msa_status msa_select_blocks(const msa_problem* p, const float* scores, int64_t ld,
                              int32_t* sel, int32_t* nsel, void* stream);
 
-/* Stage 3, decode form: every sequence has 1 to 8 rows
+/* Stage 3, decode form.  PR #1388, native Metal family commit: a decode row
+ * attends to its kept blocks in partial results (32 keys each there) that
+ * are merged afterwards.  Every sequence has 1 to 8 rows
  * (max_rows_per_seq <= 8), e.g. one decode row or a drafted window.  The
  * kept blocks of one (row, KV head) are
  * split over a cluster of 8 CTAs (two blocks each); their partial softmax
  * states (running max, sum, unnormalised output) are combined by
  * log-sum-exp on chip, through distributed shared memory.  sel/nsel as msa_select_blocks
- * writes them (entries must be causal blocks <= J, ascending, distinct).
+ * writes them (entries must be causal blocks <= J, ascending, distinct;
+ * 1 <= nsel <= top_k).  A count nsel < 1 or > top_k sets the bad-metadata
+ * bit of the error word; with nsel < 1 (no kept block, an empty softmax)
+ * the G outputs of that (row, KV head) are written as zeros.
  * Needs msa_workspace_size bytes of workspace. */
 msa_status msa_attend_decode(const msa_problem* p, const void* q, const void* k_cache,
                              const void* v_cache, const int32_t* sel, const int32_t* nsel,
@@ -170,18 +191,22 @@ msa_status msa_attend_decode(const msa_problem* p, const void* q, const void* k_
 
 /* Stage 3, decode form, for callers that cannot allocate device memory.
  * The pages describe no counterpart: this is a deployment variant of
- * msa_attend_decode.  Some callers cannot call cudaMalloc at all -- code
+ * msa_attend_decode for one decode row per sequence.  Some callers cannot call cudaMalloc at all -- code
  * enqueued while a framework captures a CUDA graph and forbids allocation
  * inside the capture, hosts whose device memory is carved out once at
  * start-up, plug-ins that do not own the process's allocator -- so this
  * entry point takes no workspace and allocates nothing: its scratch (split
  * partials, tickets, error word) is a fixed device array inside the library,
  * about 4 MiB, which every GPU that loads the library holds until the
- * process exits.  Limit: num_seqs * num_kv_heads <= 32; larger problems are
- * rejected with MSA_ERR_UNSUPPORTED.  Arguments and results are those of
- * msa_attend_decode.  The first call on each device looks up the array's
+ * process exits.  Limits: num_seqs * num_kv_heads <= 32 (larger problems
+ * are rejected with MSA_ERR_UNSUPPORTED) and exactly one row per sequence
+ * (max_rows_per_seq == 1, else MSA_ERR_INVALID_ARG; msa_attend_decode takes
+ * up to 8).  Within those limits the arguments and results are those of
+ * msa_attend_decode, including the zero output for nsel < 1.  The first call
+ * in each CUDA context (normally once per device) looks up the array's
  * device address (a host-side query, made with that device current); make
- * that first call before any stream capture.  Every call shares the one
+ * that first call before any stream capture.  After cudaDeviceReset the
+ * device has a new context and the next call looks the address up again.  Every call shares the one
  * array: calls that overlap on the GPU (several streams or host threads)
  * race and give wrong results, so order them on one stream.  Device-side
  * errors are recorded only in the library's own scratch and are not
@@ -190,15 +215,21 @@ msa_status msa_attend_decode_noalloc(const msa_problem* p, const void* q, const 
                                      const void* v_cache, const int32_t* sel, const int32_t* nsel,
                                      void* out, void* stream);
 
-/* Stage 3, prompt-chunk form (any rows per sequence): tcgen05 tensor-core
- * tiles in which the G query heads of one KV head share each key/value block
- * read; accumulators live in tensor memory.  Same arguments as the decode
- * form. */
+/* Stage 3, prompt-chunk form (any rows per sequence).  PR #1388, native
+ * Metal family commit: prompt chunks run their attention on the matrix units,
+ * each tile over its kept blocks; same PR, prompt-tile commit: the 16 query
+ * heads of a key head share the rows' selection, so one read of a key or
+ * value block serves them all.  Here: tcgen05 tensor-core tiles of one
+ * (row, KV head) whose G query heads share each key/value block read;
+ * accumulators live in tensor memory.  Same arguments as the decode form. */
 msa_status msa_attend_prefill(const msa_problem* p, const void* q, const void* k_cache,
                               const void* v_cache, const int32_t* sel, const int32_t* nsel,
                               void* out, void* workspace, size_t workspace_bytes, void* stream);
 
-/* The fused hot path: all three stages for every row of the batch.
+/* The fused hot path: all three stages for every row of the batch (the
+ * passages cited at msa_index_scores, msa_select_blocks, msa_attend_decode
+ * and msa_attend_prefill; the key, value and index-key caches hold bf16 as in
+ * PR #1388, bf16-cache commit).
  * Sequences with 1 to 8 rows (the decode family: decode rows, drafted
  * windows) take the decode kernels (index-key scan with the block max-pool
  * fused in, one pass over the index keys for all of a sequence's rows, then
@@ -211,8 +242,9 @@ msa_status msa_forward(const msa_problem* p, const void* q, const void* iq, cons
                        const void* v_cache, const void* ik_cache, void* out, int32_t* sel_out,
                        int32_t* nsel_out, void* workspace, size_t workspace_bytes, void* stream);
 
-/* msa_forward with timing marks: events[i] (cudaEvent_t, created by the
- * caller, may be NULL) is recorded on `stream` at mark i:
+/* msa_forward with timing marks (library mechanics, no counterpart in the
+ * pages): events[i] (cudaEvent_t, created by the caller, may be NULL) is
+ * recorded on `stream` at mark i:
  *   0 before the first kernel, 1 after the decode index scan, 2 after decode
  *   attention, 3 after the prompt-chunk indexer, 4 after prompt-chunk
  *   attention.  Marks of a path with no rows are recorded back to back.
@@ -223,10 +255,12 @@ msa_status msa_forward_marked(const msa_problem* p, const void* q, const void* i
                               size_t workspace_bytes, void* stream, void* const* events,
                               int32_t n_events);
 
-/* Number of kernels msa_forward launches for p (host only). */
+/* Number of kernels msa_forward launches for p (host only; library
+ * mechanics, no counterpart in the pages). */
 int32_t msa_forward_launches(const msa_problem* p);
 
-/* Diagnostics of the failure path.  Every barrier wait in the library's
+/* Diagnostics of the failure path (library mechanics, no counterpart in the
+ * pages).  Every barrier wait in the library's
  * kernels gives up after a time limit, sets bit 1 of the device error word
  * and lets the kernel finish (after waiting, again with a limit, for its own
  * copies in flight), so a lost arrival ends a call with an error instead of
