@@ -25,7 +25,7 @@ class _Problem(C.Structure):
         ("num_seqs", C.c_int32), ("H", C.c_int32), ("G", C.c_int32), ("D", C.c_int32),
         ("Di", C.c_int32), ("S", C.c_int32), ("top_k", C.c_int32), ("scale", C.c_double),
         ("cu_rows", C.c_void_p), ("cache_lens", C.c_void_p), ("cache_starts", C.c_void_p),
-        ("ik_heads", C.c_int32),
+        ("ik_heads", C.c_int32), ("kv_int8", C.c_int32), ("k_scale", C.c_void_p), ("v_scale", C.c_void_p),
     ]
 
 
@@ -59,20 +59,28 @@ class Problem:
     """Shape and metadata of one MSA problem (arrays are kept alive here)."""
 
     def __init__(self, H, G, cu_rows, cache_lens, cache_starts, D=128, Di=64, S=64, top_k=16, scale=None,
-                 ik_heads=None):
+                 ik_heads=None, k_scale=None, v_scale=None):
         self.cu_rows = np.ascontiguousarray(cu_rows, dtype=np.int32)
         self.cache_lens = np.ascontiguousarray(cache_lens, dtype=np.int32)
         self.cache_starts = np.ascontiguousarray(cache_starts, dtype=np.int64)
         self.H, self.G, self.D, self.Di, self.S, self.top_k = H, G, D, Di, S, top_k
         self.scale = scale if scale is not None else 1.0 / np.sqrt(D)
         self.ik_heads = H if ik_heads is None else ik_heads  # 1: one index key shared by all KV heads
+        # int8 key/value cache: one float scale per (cache row, KV head) for each of k and v
+        self.kv_int8 = k_scale is not None
+        if self.kv_int8 != (v_scale is not None):
+            raise ValueError("k_scale and v_scale go together")
+        self.k_scale = None if k_scale is None else np.ascontiguousarray(k_scale, dtype=np.float32)
+        self.v_scale = None if v_scale is None else np.ascontiguousarray(v_scale, dtype=np.float32)
         self.c = _Problem(len(self.cache_lens), H, G, D, Di, S, top_k, self.scale,
-                          _ptr(self.cu_rows), _ptr(self.cache_lens), _ptr(self.cache_starts), self.ik_heads)
+                          _ptr(self.cu_rows), _ptr(self.cache_lens), _ptr(self.cache_starts), self.ik_heads,
+                          int(self.kv_int8), _ptr(self.k_scale), _ptr(self.v_scale))
 
     @classmethod
     def from_workload(cls, w, x):
         return cls(w.H, w.G, x["cu_rows"], x["cache_lens"], x["cache_starts"], D=w.D, Di=w.Di,
-                   S=w.S, top_k=w.top_k, scale=w.softmax_scale, ik_heads=int(x["ik"].shape[1]))
+                   S=w.S, top_k=w.top_k, scale=w.softmax_scale, ik_heads=int(x["ik"].shape[1]),
+                   k_scale=x.get("k_scale"), v_scale=x.get("v_scale"))
 
     @property
     def total_rows(self):
@@ -89,6 +97,18 @@ class Problem:
 
 def _u16(a):
     return None if a is None else np.ascontiguousarray(a, dtype=np.uint16)
+
+
+def _kv(pr: Problem, a):
+    """A key or value cache as the oracle reads it: int8 values when the
+    problem has scales, bf16 bit patterns otherwise."""
+    if a is None:
+        return None
+    if pr.kv_int8:
+        if a.dtype != np.int8:
+            raise ValueError("an int8 key/value cache needs int8 values")
+        return np.ascontiguousarray(a)
+    return _u16(a)
 
 
 def index_scores(pr: Problem, iq, ik, r: int, h: int, lib_path=None) -> np.ndarray:
@@ -124,7 +144,7 @@ def attend(pr: Problem, q, k, v, r: int, h: int, sel, lib_path=None) -> np.ndarr
     listed blocks (entries < 0 ignored)."""
     sel = np.ascontiguousarray([s for s in np.asarray(sel).ravel() if s >= 0], dtype=np.int32)
     out = np.empty((pr.G, pr.D), dtype=np.float64)
-    q, k, v = _u16(q), _u16(k), _u16(v)
+    q, k, v = _u16(q), _kv(pr, k), _kv(pr, v)
     nk = lib(lib_path).oracle_attend(C.byref(pr.c), _ptr(q), _ptr(k), _ptr(v), r, h, _ptr(sel), len(sel), _ptr(out))
     assert nk >= 0
     return out
@@ -145,7 +165,7 @@ def forward(pr: Problem, x: dict, rows=None, threads: int = 0, with_out: bool = 
     mb = pr.max_blocks()
     pooled = np.empty((n, H, mb), dtype=np.float64) if with_pooled else None
     q, iq, ik = _u16(x["q"]), _u16(x["iq"]), _u16(x["ik"])
-    k, v = _u16(x.get("k")), _u16(x.get("v"))
+    k, v = _kv(pr, x.get("k")), _kv(pr, x.get("v"))
     if with_out and (k is None or v is None):
         raise ValueError("k and v are needed for the attention output")
     rc = lib(lib_path).oracle_forward(C.byref(pr.c), _ptr(q), _ptr(iq), _ptr(k), _ptr(v), _ptr(ik), _ptr(rows_arr), n,

@@ -48,6 +48,15 @@
  * reading of one key per position for all heads.
  * Rows of sequence b are cu_rows[b] .. cu_rows[b+1]-1; with n rows and cache
  * length L, row i sits at p = L - n + i.
+ *
+ * int8 key/value cache (kv_int8 = 1): MiniMax-M3 PR #1388, native Metal
+ * family commit, caches keys and values as int8 with one scale per position
+ * and head (a later commit of the same PR goes back to bf16).  The pages
+ * give no formula; the plain reading is dequantisation by that scale:
+ *     k[t, h, d] = k_scale[t, h] * k8[t, h, d],  v likewise with v_scale,
+ * both factors widened exactly to double (their product is exact), then
+ * step 4 unchanged.  k8/v8 are [T, H, D] int8, the scales [T, H] float,
+ * indexed by the same cache row as the values.  Index keys stay bf16.
  */
 #include <math.h>
 #include <stdint.h>
@@ -70,6 +79,9 @@ typedef struct oracle_problem {
     const int32_t* cache_lens;   /* [num_seqs] */
     const int64_t* cache_starts; /* [num_seqs] */
     int32_t ik_heads;            /* index keys per position: H, or 1 (shared); 0 means H */
+    int32_t kv_int8;             /* 0: k, v bf16; 1: int8 with a scale per (cache row, head) */
+    const float* k_scale;        /* [T, H] when kv_int8 */
+    const float* v_scale;        /* [T, H] when kv_int8 */
 } oracle_problem;
 
 static double widen_bf16(uint16_t b) {
@@ -77,6 +89,16 @@ static double widen_bf16(uint16_t b) {
     float f;
     memcpy(&f, &u, sizeof f);
     return (double)f;
+}
+
+/* Element d of the key or value row of cache row `row`, KV head h: a bf16
+ * value widened to double, or (kv_int8) the int8 value times its row's scale. */
+static double kv_value(const oracle_problem* pr, const void* base, const float* scale, int64_t row, int32_t h,
+                       int32_t d) {
+    const int64_t i = (row * pr->H + h) * (int64_t)pr->D + d;
+    if (pr->kv_int8)
+        return (double)scale[row * pr->H + h] * (double)((const int8_t*)base)[i];
+    return widen_bf16(((const uint16_t*)base)[i]);
 }
 
 /* Sequence index of query row r, and its absolute position p. */
@@ -159,7 +181,7 @@ int oracle_select(const double* m, int32_t nblocks, int32_t top_k, int32_t* sel)
 
 /* Step 4: out[g, d] for the G query heads of KV head h at row r, attending
  * over the keys of the listed blocks that are <= p. */
-int oracle_attend(const oracle_problem* pr, const uint16_t* q, const uint16_t* k, const uint16_t* v,
+int oracle_attend(const oracle_problem* pr, const uint16_t* q, const void* k, const void* v,
                   int64_t r, int32_t h, const int32_t* sel, int32_t nsel, double* out) {
     int64_t p;
     int b = locate_row(pr, r, &p);
@@ -178,9 +200,9 @@ int oracle_attend(const oracle_problem* pr, const uint16_t* q, const uint16_t* k
         double* o = out + (int64_t)g * D;
         double mx = -INFINITY;
         for (int64_t i = 0; i < nk; ++i) {
-            const uint16_t* kt = k + ((pr->cache_starts[b] + keys[i]) * H + h) * (int64_t)D;
+            const int64_t row = pr->cache_starts[b] + keys[i];
             double acc = 0.0;
-            for (int d = 0; d < D; ++d) acc += widen_bf16(qg[d]) * widen_bf16(kt[d]);
+            for (int d = 0; d < D; ++d) acc += widen_bf16(qg[d]) * kv_value(pr, k, pr->k_scale, row, h, d);
             x[i] = pr->scale * acc;
             if (x[i] > mx) mx = x[i];
         }
@@ -189,8 +211,8 @@ int oracle_attend(const oracle_problem* pr, const uint16_t* q, const uint16_t* k
         for (int64_t i = 0; i < nk; ++i) {
             double w = exp(x[i] - mx);
             den += w;
-            const uint16_t* vt = v + ((pr->cache_starts[b] + keys[i]) * H + h) * (int64_t)D;
-            for (int d = 0; d < D; ++d) o[d] += w * widen_bf16(vt[d]);
+            const int64_t row = pr->cache_starts[b] + keys[i];
+            for (int d = 0; d < D; ++d) o[d] += w * kv_value(pr, v, pr->v_scale, row, h, d);
         }
         for (int d = 0; d < D; ++d) o[d] = nk > 0 ? o[d] / den : 0.0;
     }
@@ -203,7 +225,7 @@ int oracle_attend(const oracle_problem* pr, const uint16_t* q, const uint16_t* k
  * holds row rows[i]: sel [n, H, top_k], nsel [n, H], pooled (optional)
  * [n, H, max_blocks], out [n, H*G, D].  Returns 0, or -1 on a bad row. */
 int oracle_forward(const oracle_problem* pr, const uint16_t* q, const uint16_t* iq,
-                   const uint16_t* k, const uint16_t* v, const uint16_t* ik,
+                   const void* k, const void* v, const uint16_t* ik,
                    const int64_t* rows, int64_t nrows, int32_t* sel, int32_t* nsel,
                    double* out, double* pooled, int64_t max_blocks, int32_t nthreads) {
     const int H = pr->H;

@@ -12,13 +12,17 @@ seed x is mix64(key(x, s) + (i + 1) * 0x9E3779B97F4A7C15).  Uniform doubles
 take the top 53 bits.  Normals use the Box-Muller transform on consecutive
 pairs of uniforms and are rounded double -> float -> bf16, each step
 round-to-nearest-even.  Index q/k are uniform integers in [-8, 8], stored
-as bf16 (exact), so fp32 index scores are exact.
+as bf16 (exact), so fp32 index scores are exact.  An int8 key/value cache
+(kv_dtype "int8") holds uniform integers in [-127, 127] with one float32
+scale per (cache row, KV head) drawn uniformly from [0.5/64, 1.5/64], so the
+dequantised values have about the spread of the bf16 N(0,1) cache.
 
 Layouts (all row-major, bf16 carried as uint16 bit patterns):
   q   [total_rows, H*G, D]     query row r, q head h*G+g
   iq  [total_rows, H, Di]      index query
   k,v [cache_tokens, H, D]     sequence b occupies rows cache_starts[b] .. +L_b
   ik  [cache_tokens, H, Di]    index keys, same token rows as k/v
+  k_scale, v_scale [cache_tokens, H] float32 (int8 caches only)
 Row i of a sequence with n rows and cache length L sits at position L-n+i.
 """
 from __future__ import annotations
@@ -32,7 +36,7 @@ import numpy as np
 
 __all__ = [
     "Workload", "make_inputs", "WORKLOADS", "workload", "bf16_to_f32",
-    "uniform", "normal_bf16", "int_bf16", "ragged_lengths",
+    "uniform", "normal_bf16", "int_bf16", "int8_values", "uniform_f32", "ragged_lengths",
 ]
 
 _MASK = (1 << 64) - 1
@@ -43,6 +47,7 @@ _CHUNK = 1 << 20
 
 # stream ids, one per drawn tensor
 STREAM_Q, STREAM_IQ, STREAM_K, STREAM_V, STREAM_IK, STREAM_LENS = 1, 2, 3, 4, 5, 6
+STREAM_KSCALE, STREAM_VSCALE = 7, 8
 
 
 def _mix_int(z: int) -> int:
@@ -138,6 +143,29 @@ def int_bf16(seed: int, stream: int, shape, lo: int = -8, hi: int = 8) -> np.nda
     return out.reshape(shape)
 
 
+def int8_values(seed: int, stream: int, shape, lo: int = -127, hi: int = 127) -> np.ndarray:
+    """Uniform integers in [lo, hi] as int8."""
+    n = int(np.prod(shape, dtype=np.int64))
+    out = np.empty(n, dtype=np.int8)
+    key = _key(seed, stream)
+    span = hi - lo + 1
+
+    def one(s0):
+        m = min(_CHUNK, n - s0)
+        u = _u53(_bits(key, s0, m))
+        out[s0:s0 + m] = (np.floor(u * span) + lo).astype(np.int8)
+
+    _parallel(one, n, _CHUNK)
+    return out.reshape(shape)
+
+
+def uniform_f32(seed: int, stream: int, shape, lo: float, hi: float) -> np.ndarray:
+    """Uniform draws in [lo, hi) rounded to float32."""
+    n = int(np.prod(shape, dtype=np.int64))
+    u = uniform(seed, stream, n)
+    return (lo + (hi - lo) * u).astype(np.float32).reshape(shape)
+
+
 def ragged_lengths(seed: int, n: int, lo: int, hi: int) -> list[int]:
     """n lengths drawn log-uniformly from [lo, hi)."""
     u = uniform(seed, STREAM_LENS, n)
@@ -165,6 +193,7 @@ class Workload:
     note: str = ""
     extra: dict = field(default_factory=dict)
     ik_heads: int = 0  # index keys per position: 0 = one per KV head, 1 = one shared by all heads
+    kv_dtype: str = "bf16"  # "int8": int8 key/value cache with a float32 scale per (cache row, KV head)
 
     @property
     def softmax_scale(self) -> float:
@@ -203,7 +232,12 @@ def make_inputs(w: Workload, with_kv: bool = True) -> dict:
         iq=int_bf16(w.seed, STREAM_IQ, (R, w.H, w.Di)),
         ik=int_bf16(w.seed, STREAM_IK, (T, 1 if w.ik_heads == 1 else w.H, w.Di)),
     )
-    if with_kv:
+    if with_kv and w.kv_dtype == "int8":
+        out["k"] = int8_values(w.seed, STREAM_K, (T, w.H, w.D))
+        out["v"] = int8_values(w.seed, STREAM_V, (T, w.H, w.D))
+        out["k_scale"] = uniform_f32(w.seed, STREAM_KSCALE, (T, w.H), 0.5 / 64, 1.5 / 64)
+        out["v_scale"] = uniform_f32(w.seed, STREAM_VSCALE, (T, w.H), 0.5 / 64, 1.5 / 64)
+    elif with_kv:
         out["k"] = normal_bf16(w.seed, STREAM_K, (T, w.H, w.D))
         out["v"] = normal_bf16(w.seed, STREAM_V, (T, w.H, w.D))
     return out
@@ -232,13 +266,16 @@ def paged_layout(w: Workload, x: dict, page_size: int, spare_pages: int = 3, see
     rows = num_pages * page_size
     out = dict(table=table, num_pages=num_pages, page_size=page_size)
     starts = x["cache_starts"]
-    for i, name in enumerate(n for n in ("k", "v", "ik") if n in x):
+    for i, name in enumerate(n for n in ("k", "v", "ik", "k_scale", "v_scale") if n in x):
         src = x[name]
-        heads, width = src.shape[1], src.shape[2]
         if name == "ik":
-            pool = int_bf16(seed, STREAM_POOL + i, (rows, heads, width))
+            pool = int_bf16(seed, STREAM_POOL + i, (rows,) + src.shape[1:])
+        elif src.dtype == np.int8:
+            pool = int8_values(seed, STREAM_POOL + i, (rows,) + src.shape[1:])
+        elif src.dtype == np.float32:
+            pool = uniform_f32(seed, STREAM_POOL + i, (rows,) + src.shape[1:], 0.5 / 64, 1.5 / 64)
         else:
-            pool = normal_bf16(seed, STREAM_POOL + i, (rows, heads, width))
+            pool = normal_bf16(seed, STREAM_POOL + i, (rows,) + src.shape[1:])
         for b, L in enumerate(lens):
             for pg in range(pages[b]):
                 t0, t1 = pg * page_size, min(L, (pg + 1) * page_size)
@@ -272,6 +309,14 @@ WORKLOADS = {
     "decode_4x65536_shared_ik": lambda: Workload("decode_4x65536_shared_ik", H=4, G=16, seqs=[(1, 65536)] * 4,
                                                  ik_heads=1,
                                                  note="decode batch 4 at 65,536, one index key per position shared by the 4 KV heads"),
+    "decode_4x65536_int8": lambda: Workload("decode_4x65536_int8", H=4, G=16, seqs=[(1, 65536)] * 4,
+                                            kv_dtype="int8",
+                                            note="decode batch 4 at 65,536 with an int8 key/value cache "
+                                                 "(a float32 scale per position and KV head)"),
+    "prefill_4096_at_8192_int8": lambda: Workload("prefill_4096_at_8192_int8", H=4, G=16,
+                                                  seqs=[(4096, 8192 + 4096)], kv_dtype="int8",
+                                                  note="prefill chunk of 4,096 rows after an 8,192-token prefix, "
+                                                       "int8 key/value cache"),
 }
 
 

@@ -315,10 +315,113 @@ def check_future_blocks_never_selected(lib_path=None):
         assert max(sel) == J and sel == exp, (i, p, sel, exp)
 
 
+# --------------------------------------------------------------------------
+# int8 key/value cache (PR #1388, native Metal family commit: int8 values with
+# one scale per position and head; read as value = scale * int8)
+# --------------------------------------------------------------------------
+
+def _int8_workload(name, seed, scale=None):
+    w = synth.Workload(name, H=2, G=4, seqs=[(1, 700), (9, 1300), (1, 64)], seed=seed, kv_dtype="int8",
+                       scale=scale)
+    return w, synth.make_inputs(w)
+
+
+def _as_bf16_cache(a8):
+    """The same integers stored as bf16 (exact for |v| <= 256)."""
+    return bf16_bits(a8.astype(np.float32))
+
+
+def check_int8_unit_scales_equal_bf16_integers(lib_path=None):
+    """All scales 1: the int8 cache reads the same values as a bf16 cache
+    holding the same integers, so the outputs are identical."""
+    w, x = _int8_workload("int8_unit", 31)
+    ones = np.ones_like(x["k_scale"])
+    x8 = dict(x, k_scale=ones, v_scale=ones)
+    xb = {k: v for k, v in x.items() if k not in ("k_scale", "v_scale")}
+    xb["k"], xb["v"] = _as_bf16_cache(x["k"]), _as_bf16_cache(x["v"])
+    r8 = oracle.forward(oracle.Problem.from_workload(w, x8), x8, lib_path=lib_path)
+    rb = oracle.forward(oracle.Problem.from_workload(w, xb), xb, lib_path=lib_path)
+    assert np.array_equal(r8["sel"], rb["sel"])
+    assert np.array_equal(r8["out"], rb["out"])
+
+
+def check_int8_key_scale_is_softmax_scale(lib_path=None):
+    """Every key scale 1/4 (a power of two, so every product is exact) and
+    value scales 1: the same as a bf16 cache of the integers with the softmax
+    scale divided by 4."""
+    w, x = _int8_workload("int8_kscale", 37)
+    x8 = dict(x, k_scale=np.full_like(x["k_scale"], 0.25), v_scale=np.ones_like(x["v_scale"]))
+    wb = synth.Workload(w.name, H=w.H, G=w.G, seqs=w.seqs, seed=w.seed, scale=w.softmax_scale * 0.25)
+    xb = {k: v for k, v in x.items() if k not in ("k_scale", "v_scale")}
+    xb["k"], xb["v"] = _as_bf16_cache(x["k"]), _as_bf16_cache(x["v"])
+    r8 = oracle.forward(oracle.Problem.from_workload(w, x8), x8, lib_path=lib_path)
+    rb = oracle.forward(oracle.Problem.from_workload(wb, xb), xb, lib_path=lib_path)
+    assert np.max(np.abs(r8["out"] - rb["out"])) < 1e-13
+
+
+def check_int8_value_scales_closed_form(lib_path=None):
+    """Two keys with zero key vectors (equal scores): the output is the mean
+    of the two dequantised values, each with its own position's and head's
+    scale: (vs_0 * v8_0 + vs_1 * v8_1) / 2."""
+    cu, lens, starts = np.array([0, 1]), np.array([2]), np.array([0])
+    vs = np.array([[0.5, 3.0], [0.125, 7.0]], dtype=np.float32)  # [position, head]
+    pr = oracle.Problem(2, 1, cu, lens, starts, D=2, Di=2, S=2, top_k=16, scale=1.0,
+                        k_scale=np.ones((2, 2), dtype=np.float32), v_scale=vs)
+    q = bf16_bits([[[1.0, 2.0], [3.0, -1.0]]])
+    k = np.zeros((2, 2, 2), dtype=np.int8)
+    v = np.array([[[10, -3], [4, 5]], [[-8, 100], [-127, 1]]], dtype=np.int8)
+    for h in range(2):
+        got = oracle.attend(pr, q, k, v, 0, h, [0], lib_path=lib_path)
+        exp = (float(vs[0, h]) * v[0, h].astype(np.float64) + float(vs[1, h]) * v[1, h].astype(np.float64)) / 2
+        assert np.max(np.abs(got[0] - exp)) < 1e-15, (h, got, exp)
+
+
+def check_int8_key_scales_closed_form(lib_path=None):
+    """Two keys with the same int8 vector but different scales: scores
+    scale * ks_t * (q . k8), so the weights are exp(ks_0 c) and exp(ks_1 c)
+    with c = q . k8 = 3; the output weighs the two values by them."""
+    cu, lens, starts = np.array([0, 1]), np.array([2]), np.array([0])
+    ks = np.array([[0.25], [0.5]], dtype=np.float32)
+    pr = oracle.Problem(1, 1, cu, lens, starts, D=2, Di=2, S=2, top_k=16, scale=1.0,
+                        k_scale=ks, v_scale=np.ones((2, 1), dtype=np.float32))
+    q = bf16_bits([[[1.0, 1.0]]])
+    k = np.array([[[1, 2]], [[1, 2]]], dtype=np.int8)
+    v = np.array([[[1, 0]], [[0, 1]]], dtype=np.int8)
+    got = oracle.attend(pr, q, k, v, 0, 0, [0], lib_path=lib_path)
+    w0, w1 = math.exp(0.25 * 3), math.exp(0.5 * 3)
+    exp = np.array([w0, w1]) / (w0 + w1)
+    assert np.max(np.abs(got[0] - exp)) < 1e-14, (got, exp)
+
+
+def check_int8_dense_special_case(lib_path=None):
+    """Every causal block kept: the int8 cache's MSA output is dense causal
+    attention (torch float64 SDPA) over the dequantised keys and values."""
+    w, x = _int8_workload("int8_dense", 41)
+    pr = oracle.Problem.from_workload(w, x)
+    rows = [0, 1, 5, 9, 10]
+    res = oracle.forward(pr, x, rows=rows, lib_path=lib_path)
+    for i, r in enumerate(rows):
+        b, p = pr.position(r)
+        if p // 64 + 1 > w.top_k:
+            continue
+        s0 = int(x["cache_starts"][b])
+        for h in range(w.H):
+            kd = x["k"][s0:s0 + p + 1, h, :].astype(np.float64) * x["k_scale"][s0:s0 + p + 1, h, None]
+            vd = x["v"][s0:s0 + p + 1, h, :].astype(np.float64) * x["v_scale"][s0:s0 + p + 1, h, None]
+            qg = torch.from_numpy(to_f64(x["q"][r, h * w.G:(h + 1) * w.G, :]))[None, :, None, :]
+            kk = torch.from_numpy(kd)[None, None].expand(1, w.G, -1, -1)
+            vv = torch.from_numpy(vd)[None, None].expand(1, w.G, -1, -1)
+            ref = torch.nn.functional.scaled_dot_product_attention(qg, kk, vv, scale=w.softmax_scale)[0, :, 0, :]
+            got = res["out"][i, h * w.G:(h + 1) * w.G]
+            assert np.max(np.abs(got - ref.numpy())) < 1e-12, (r, h)
+
+
 ALL_CHECKS = [
     check_select_golden, check_select_golden_through_forward, check_pool_golden, check_scores_unit_query,
     check_scores_integer_matmul, check_dense_special_case, check_explicit_selection, check_two_key_closed_form,
     check_constant_values, check_single_key, check_zero_scale_is_mean, check_select_bruteforce,
     check_select_invariants, check_future_blocks_never_selected, check_shared_key_integer_matmul,
-    check_shared_key_equals_replicated,
+    check_shared_key_equals_replicated, check_int8_unit_scales_equal_bf16_integers,
+    check_int8_key_scale_is_softmax_scale, check_int8_value_scales_closed_form, check_int8_key_scales_closed_form,
+    check_int8_dense_special_case,
 ]

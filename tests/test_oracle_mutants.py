@@ -23,7 +23,11 @@ MUTANTS = {
     "wrong_index_key_head": [("* kh + (kh == 1 ? 0 : h))", "* kh + 0)")],
     "unnormalised_output": [("o[d] = nk > 0 ? o[d] / den : 0.0;", "o[d] = nk > 0 ? o[d] : 0.0;")],
     "last_not_max_pool": [("if (s[t] > best) best = s[t];", "best = s[t];")],
-    "values_from_keys": [("const uint16_t* vt = v + ", "const uint16_t* vt = k + ")],
+    "values_from_keys": [("kv_value(pr, v, pr->v_scale", "kv_value(pr, k, pr->v_scale")],
+    "int8_scale_ignored": [("return (double)scale[row * pr->H + h] * (double)((const int8_t*)base)[i];",
+                            "return (double)((const int8_t*)base)[i];")],
+    "int8_key_scale_for_values": [("kv_value(pr, v, pr->v_scale", "kv_value(pr, v, pr->k_scale")],
+    "int8_scale_of_head_0": [("scale[row * pr->H + h]", "scale[row * pr->H]")],
     "block_end_off_by_one": [("t < (int64_t)(sel[i] + 1) * S;", "t < (int64_t)(sel[i] + 1) * S - 1;")],
     "drops_current_position": [("if (t >= 0 && t <= p) keys[nk++] = t;", "if (t >= 0 && t < p) keys[nk++] = t;")],
     "min_not_max_selection": [("if (x->m > y->m) return -1;\n    if (x->m < y->m) return 1;",
