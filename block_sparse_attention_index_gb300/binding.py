@@ -18,6 +18,7 @@ LIB_PATH = os.path.join(_HERE, "_lib", "libmsa_gb300.so")
 
 MSA_OK, MSA_ERR_INVALID_ARG, MSA_ERR_UNSUPPORTED, MSA_ERR_WORKSPACE, MSA_ERR_CUDA, MSA_ERR_INTERNAL = range(6)
 MSA_OUT_F32, MSA_OUT_BF16 = 0, 1
+MSA_KV_BF16, MSA_KV_INT8 = 0, 1
 ERR_WAIT_TIMEOUT, ERR_BAD_METADATA, ERR_TMEM_ALLOC = 1, 2, 4
 
 EXPORTED = [
@@ -39,7 +40,8 @@ class MsaProblem(C.Structure):
         ("max_rows_per_seq", C.c_int32), ("max_cache_len", C.c_int32), ("cache_tokens", C.c_int64),
         ("num_decode_seqs", C.c_int32), ("cu_rows", C.c_void_p), ("cache_lens", C.c_void_p),
         ("cache_starts", C.c_void_p), ("block_table", C.c_void_p), ("block_table_stride", C.c_int32),
-        ("page_size", C.c_int32), ("index_key_heads", C.c_int32),
+        ("page_size", C.c_int32), ("index_key_heads", C.c_int32), ("kv_dtype", C.c_int32),
+        ("k_scale", C.c_void_p), ("v_scale", C.c_void_p),
     ]
 
 
@@ -123,11 +125,13 @@ class Problem:
     block_table ([B, stride] int32 page numbers, tensor or nested list) and
     page_size, with cache_tokens = rows of the page pool.  ik_heads=1: one
     index key per position shared by every KV head (ik is [T, 1, Di]).
+    k_scale, v_scale (float32 [cache_tokens, H] device tensors): the key and
+    value caches are int8 with these per-(cache row, head) scales.
     """
 
     def __init__(self, H, G, seqs_host, device, top_k=16, scale=None, out_dtype=torch.float32,
                  cache_starts=None, cache_tokens=None, D=128, Di=64, S=64, num_decode_seqs="auto",
-                 block_table=None, page_size=0, ik_heads=0):
+                 block_table=None, page_size=0, ik_heads=0, k_scale=None, v_scale=None):
         self.H, self.G, self.D, self.Di, self.S, self.top_k = H, G, D, Di, S, top_k
         self.device = torch.device(device)
         if self.device.type == "cuda" and self.device.index is None:
@@ -170,6 +174,18 @@ class Problem:
             None if self.block_table is None else self.block_table.data_ptr(),
             0 if self.block_table is None else int(self.block_table.shape[1]), int(page_size), int(ik_heads))
         self.KH = 1 if (ik_heads == 1 or H == 1) else H  # index-key heads per position
+        if (k_scale is None) != (v_scale is None):
+            raise ValueError("k_scale and v_scale go together")
+        self.kv_dtype = torch.int8 if k_scale is not None else torch.bfloat16
+        self.k_scale = self.v_scale = None
+        if k_scale is not None:
+            self.k_scale = torch.as_tensor(k_scale, dtype=torch.float32).to(self.device).contiguous()
+            self.v_scale = torch.as_tensor(v_scale, dtype=torch.float32).to(self.device).contiguous()
+            for t, name in ((self.k_scale, "k_scale"), (self.v_scale, "v_scale")):
+                _need(t, name, torch.float32, self.device, (self.cache_tokens, H))
+            self.c.kv_dtype = MSA_KV_INT8
+            self.c.k_scale = self.k_scale.data_ptr()
+            self.c.v_scale = self.v_scale.data_ptr()
 
     @property
     def max_cache_len(self):
@@ -202,7 +218,8 @@ class Problem:
         _need(iq, "iq", torch.bfloat16, self.device, (self.total_rows, self.H, self.Di))
 
     def _check_cache(self, t, name, width, heads=None):
-        _need(t, name, torch.bfloat16, self.device, (self.cache_tokens, self.H if heads is None else heads, width))
+        dtype = self.kv_dtype if name in ("k", "v") else torch.bfloat16
+        _need(t, name, dtype, self.device, (self.cache_tokens, self.H if heads is None else heads, width))
 
     def _check_sel(self, sel, nsel):
         _need(sel, "sel", torch.int32, self.device, (self.total_rows, self.H, self.top_k))

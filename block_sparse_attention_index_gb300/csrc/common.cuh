@@ -45,6 +45,47 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// Four signed int8 values (bytes of w, lowest first) as four bf16 values,
+// packed two per word (lowest index in the low half).  Each byte b is biased
+// to b + 128, placed in the low mantissa bits of 2^23 (the float 2^23 + b +
+// 128, exact) and 2^23 + 128 is subtracted, which leaves b exactly; an
+// integer of at most 8 significant bits has zero low 16 bits as a float, so
+// its bf16 is the float's upper half.
+__device__ __forceinline__ void i8x4_to_bf16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
+    const uint32_t u = w ^ 0x80808080u;
+    const float f0 = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7540)) - 8388736.f;
+    const float f1 = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7541)) - 8388736.f;
+    const float f2 = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7542)) - 8388736.f;
+    const float f3 = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7543)) - 8388736.f;
+    lo = __byte_perm(__float_as_uint(f0), __float_as_uint(f1), 0x7632);
+    hi = __byte_perm(__float_as_uint(f2), __float_as_uint(f3), 0x7632);
+}
+
+// One 64-key x 128-dim int8 tile, as TMA lands it with 128-byte swizzle in
+// the second 8 KB of a 16 KB area, rewritten in place as the bf16 layout the
+// MMAs read: dims 0-63 in the first 8 KB, dims 64-127 in the second, each a
+// [key][64 dims] tile with the same swizzle.  Row `key` is read whole into
+// registers before any of its bytes is overwritten, and no other row shares
+// those bytes, so threads may convert different rows concurrently.
+__device__ __forceinline__ void convert_i8_row(uint8_t* area, int key) {
+    const uint8_t* src = area + 8192 + key * 128;
+    uint4 c[8];
+#pragma unroll
+    for (int ch = 0; ch < 8; ++ch) c[ch] = *reinterpret_cast<const uint4*>(src + ((ch ^ (key & 7)) << 4));
+#pragma unroll
+    for (int ch = 0; ch < 8; ++ch) {  // int8 chunk ch = dims 16 ch .. 16 ch + 15
+        uint4 a, b;
+        i8x4_to_bf16x4(c[ch].x, a.x, a.y);
+        i8x4_to_bf16x4(c[ch].y, a.z, a.w);
+        i8x4_to_bf16x4(c[ch].z, b.x, b.y);
+        i8x4_to_bf16x4(c[ch].w, b.z, b.w);
+        uint8_t* dst = area + (ch >> 2) * 8192 + key * 128;
+        const int j = (ch & 3) * 2;  // bf16 chunk (8 dims) within the 64-dim half
+        *reinterpret_cast<uint4*>(dst + ((j ^ (key & 7)) << 4)) = a;
+        *reinterpret_cast<uint4*>(dst + (((j + 1) ^ (key & 7)) << 4)) = b;
+    }
+}
+
 // Monotonic map of a float to uint32 (larger float -> larger code).
 __device__ __forceinline__ uint32_t ordered_bits(float f) {
     uint32_t u = __float_as_uint(f);

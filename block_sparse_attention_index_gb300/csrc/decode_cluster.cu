@@ -15,7 +15,13 @@
 //     combines its two heads from its own shared memory:
 //         M = max m_c,  L = sum l_c 2^(m_c - M),  out = sum O_c 2^(m_c - M) / L
 //   - the kept blocks come from the pooled index scores (every CTA runs the
-//     same deterministic selection) or from a given list.
+//     same deterministic selection) or from a given list;
+//   - an int8 key/value cache (PR #1388, native Metal family commit: int8
+//     values with a scale per position and head) lands by TMA as int8 tiles
+//     that every thread rewrites row by row, in place, as bf16 (exact: the
+//     integers have at most 8 significant bits); the key scale multiplies the
+//     row's scores and the value scale its softmax weights before P V, so the
+//     MMAs are the same as for a bf16 cache.
 // Launched after the index scan as a programmatic dependent launch: q and
 // the sequence metadata are read before waiting for the scan to finish.
 #include "common.cuh"
@@ -36,6 +42,7 @@ struct __align__(1024) ClusterSmem {
     float recv_ml[kCluster][2][2];   // their (max in the log2 domain, sum)
     float wmax[4][16];
     float wsum[4][16];
+    float kvscale[2][2][64];         // int8 cache: [key/value][block][key] scales of this CTA's blocks
     uint64_t bar;
     int32_t sel[kMaxTopK];
     int32_t nsel;
@@ -96,7 +103,7 @@ __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;"
 
 // grid (kCluster, H, B), cluster (kCluster, 1, 1): CTA `rank` of the cluster of
 // (sequence b, KV head h) takes kept blocks rank and rank + kCluster.
-template <bool kSelGiven>
+template <bool kSelGiven, bool kInt8>
 __global__ void __launch_bounds__(kClThreads) decode_cluster_kernel(const __grid_constant__ CUtensorMap k_map,
                                                                     const __grid_constant__ CUtensorMap v_map,
                                                                     const DecodeAttendArgs a) {
@@ -186,7 +193,8 @@ __global__ void __launch_bounds__(kClThreads) decode_cluster_kernel(const __grid
             blk[i] = J;
         }
     }
-    if (tid == 0 && nmy > 0) mbar_arrive_expect_tx(&sm.bar, nmy * 4 * 64 * 64 * 2);
+    // bytes per kept block: K and V, bf16 (four 64-dim boxes) or int8 (two 128-dim boxes)
+    if (tid == 0 && nmy > 0) mbar_arrive_expect_tx(&sm.bar, nmy * (kInt8 ? 2 : 4) * 64 * 64 * 2);
     __syncthreads();  // the expected bytes are registered before any copy lands; q visible to every warp
     // Warp w issues the copies of block w / 2, K (w even) or V (w odd): one thread issues TMA boxes
     // at a bounded rate, so four issuers land the 64 KB sooner than one.
@@ -199,7 +207,10 @@ __global__ void __launch_bounds__(kClThreads) decode_cluster_kernel(const __grid
             row = 0;
         }
         const int tok = static_cast<int>(row);
-        if ((warp & 1) == 0) {
+        if constexpr (kInt8) {  // one int8 tile per block into the upper 8 KB, widened in place below
+            if ((warp & 1) == 0) tma_load_3d(sm.k[i][1], &k_map, &sm.bar, 0, h, tok);
+            else tma_load_3d(sm.v[i][1], &v_map, &sm.bar, 0, h, tok);
+        } else if ((warp & 1) == 0) {
             tma_load_3d(sm.k[i][0], &k_map, &sm.bar, 0, h, tok);
             tma_load_3d(sm.k[i][1], &k_map, &sm.bar, 64, h, tok);
         } else {
@@ -207,10 +218,39 @@ __global__ void __launch_bounds__(kClThreads) decode_cluster_kernel(const __grid
             tma_load_3d(sm.v[i][1], &v_map, &sm.bar, 64, h, tok);
         }
     }
+    if constexpr (kInt8) {
+        // scales of this CTA's keys (thread = block tid / 64, key tid % 64); keys past p are
+        // masked and may lie past the sequence's cache rows, so they are not read (scale 0,
+        // as for a block this CTA does not have)
+        {
+            const int i = tid >> 6, key = tid & 63;
+            const int bi = i == 0 ? blk[0] : blk[1];
+            float ks = 0.f, vs = 0.f;
+            if (i < nmy && bi * kBlock + key <= p) {
+                const int64_t row = block_row(a.cache, b, static_cast<int64_t>(bi) * kBlock);
+                if (row >= 0) {
+                    const int64_t si = (row + key) * H + h;
+                    ks = a.k_scale[si];
+                    vs = a.v_scale[si];
+                }
+            }
+            sm.kvscale[0][i][key] = ks;
+            sm.kvscale[1][i][key] = vs;
+        }
+    }
     bool kv_in_flight = false;  // a copy that did not land in time: waited for again before the CTA ends
     if (nmy > 0 && !__syncthreads_and(mbar_wait(&sm.bar, 0, a.err))) {
         nmy = 0;  // copy never landed: no keys
         kv_in_flight = true;
+    }
+    if constexpr (kInt8) {
+        // every thread widens whole key rows (K rows then V rows of this CTA's blocks)
+        for (int rr = tid; rr < nmy * 2 * 64; rr += kClThreads) {
+            const bool is_v = rr >= nmy * 64;
+            const int r2 = is_v ? rr - nmy * 64 : rr;
+            convert_i8_row(reinterpret_cast<uint8_t*>(is_v ? sm.v[r2 >> 6][0] : sm.k[r2 >> 6][0]), r2 & 63);
+        }
+        __syncthreads();  // bf16 tiles and scales visible to every warp
     }
 
 
@@ -241,7 +281,8 @@ __global__ void __launch_bounds__(kClThreads) decode_cluster_kernel(const __grid
             }
         }
     }
-    // scale (log2 domain), causal mask inside the local block, row maxima
+    // scale (log2 domain; times the key's scale for an int8 cache), causal mask inside the
+    // local block, row maxima
     float rmax[2] = {-INFINITY, -INFINITY};
 #pragma unroll
     for (int nt = 0; nt < 4; ++nt)
@@ -249,7 +290,8 @@ __global__ void __launch_bounds__(kClThreads) decode_cluster_kernel(const __grid
         for (int e = 0; e < 4; ++e) {
             const int key = key0 + nt * 8 + tig * 2 + (e & 1);
             const bool valid = warp_live && wblk * kBlock + key <= p;
-            s[nt][e] = valid ? s[nt][e] * a.scale_log2 : -INFINITY;
+            const float f = kInt8 ? a.scale_log2 * sm.kvscale[0][my_blk][key] : a.scale_log2;
+            s[nt][e] = valid ? s[nt][e] * f : -INFINITY;
             rmax[e >> 1] = fmaxf(rmax[e >> 1], s[nt][e]);
         }
 #pragma unroll
@@ -276,14 +318,18 @@ __global__ void __launch_bounds__(kClThreads) decode_cluster_kernel(const __grid
         lsum[0] += p0 + p1;
         lsum[1] += p2 + p3;
         const int key = warp * 32 + nt * 8 + tig * 2;  // key index among this CTA's 128
+        // int8 cache: the value scale of each key folds into its weight (the sum keeps the weight)
+        const float vs0 = kInt8 ? sm.kvscale[1][key >> 6][key & 63] : 1.f;
+        const float vs1 = kInt8 ? sm.kvscale[1][key >> 6][(key + 1) & 63] : 1.f;
+        const float w0 = p0 * vs0, w1 = p1 * vs1, w2 = p2 * vs0, w3 = p3 * vs1;
         const int chunk = key >> 3, within = (key & 7) * 2;
-        const uint32_t h01 = pack_bf16x2(p0, p1), h23 = pack_bf16x2(p2, p3);
+        const uint32_t h01 = pack_bf16x2(w0, w1), h23 = pack_bf16x2(w2, w3);
         *reinterpret_cast<uint32_t*>(phi + cl_swz(grp, chunk, 256) + within) = h01;
         *reinterpret_cast<uint32_t*>(phi + cl_swz(grp + 8, chunk, 256) + within) = h23;
         *reinterpret_cast<uint32_t*>(plo + cl_swz(grp, chunk, 256) + within) =
-            pack_bf16x2(p0 - bf16_lo(h01), p1 - bf16_hi(h01));
+            pack_bf16x2(w0 - bf16_lo(h01), w1 - bf16_hi(h01));
         *reinterpret_cast<uint32_t*>(plo + cl_swz(grp + 8, chunk, 256) + within) =
-            pack_bf16x2(p2 - bf16_lo(h23), p3 - bf16_hi(h23));
+            pack_bf16x2(w2 - bf16_lo(h23), w3 - bf16_hi(h23));
     }
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
@@ -371,8 +417,10 @@ __global__ void __launch_bounds__(kClThreads) decode_cluster_kernel(const __grid
 cudaError_t run_decode_cluster(const DecodeAttendArgs& a, bool after_scan, cudaStream_t stream) {
     const size_t smem = sizeof(ClusterSmem) + 1024;
     const bool given = a.pooled == nullptr;
-    const void* fn = given ? reinterpret_cast<const void*>(decode_cluster_kernel<true>)
-                           : reinterpret_cast<const void*>(decode_cluster_kernel<false>);
+    const void* fn = a.kv_int8 ? (given ? reinterpret_cast<const void*>(decode_cluster_kernel<true, true>)
+                                        : reinterpret_cast<const void*>(decode_cluster_kernel<false, true>))
+                               : (given ? reinterpret_cast<const void*>(decode_cluster_kernel<true, false>)
+                                        : reinterpret_cast<const void*>(decode_cluster_kernel<false, false>));
     cudaError_t e = ensure_smem_limit(fn, smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
@@ -389,10 +437,12 @@ cudaError_t run_decode_cluster(const DecodeAttendArgs& a, bool after_scan, cudaS
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = after_scan ? 2 : 1;  // overlap the prologue with the index scan's tail
-    if (given)
-        e = cudaLaunchKernelEx(&cfg, decode_cluster_kernel<true>, *a.k_map, *a.v_map, a);
+    if (a.kv_int8)
+        e = given ? cudaLaunchKernelEx(&cfg, decode_cluster_kernel<true, true>, *a.k_map, *a.v_map, a)
+                  : cudaLaunchKernelEx(&cfg, decode_cluster_kernel<false, true>, *a.k_map, *a.v_map, a);
     else
-        e = cudaLaunchKernelEx(&cfg, decode_cluster_kernel<false>, *a.k_map, *a.v_map, a);
+        e = given ? cudaLaunchKernelEx(&cfg, decode_cluster_kernel<true, false>, *a.k_map, *a.v_map, a)
+                  : cudaLaunchKernelEx(&cfg, decode_cluster_kernel<false, false>, *a.k_map, *a.v_map, a);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }

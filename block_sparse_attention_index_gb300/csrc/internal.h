@@ -82,6 +82,9 @@ struct DecodeAttendArgs {
     int num_seqs, H, G, top_k, total_rows, max_cache_len;
     int64_t cache_tokens;
     float scale_log2;          // softmax scale * log2(e)
+    int kv_int8;               // 1: k, v are int8 [T, H, D] with fp32 scales [T, H]
+    const float* k_scale;
+    const float* v_scale;
     void* out;
     int out_bf16;
     float* partials;           // [B, H, top_k, kPartialFloats]
@@ -131,6 +134,9 @@ struct PrefillAttendArgs {
     int num_seqs, H, G, top_k, total_rows, max_rows_per_seq, max_cache_len;
     int64_t cache_tokens;
     float scale_log2;
+    int kv_int8;               // 1: k, v are int8 [T, H, D] with fp32 scales [T, H]
+    const float* k_scale;
+    const float* v_scale;
     void* out;
     int out_bf16;
     int only_multi_row;  // 1: skip decode-family sequences (<= kDecodeMaxRows rows; fused path)

@@ -67,6 +67,13 @@ msa_status check_problem(const msa_problem* p) {
     if (!p->cu_rows || !p->cache_lens) return fail(MSA_ERR_INVALID_ARG, "device metadata is null");
     if ((reinterpret_cast<uintptr_t>(p->cu_rows) & 3u) || (reinterpret_cast<uintptr_t>(p->cache_lens) & 3u))
         return fail(MSA_ERR_INVALID_ARG, "cu_rows or cache_lens is not 4-byte aligned");
+    if (p->kv_dtype != MSA_KV_BF16 && p->kv_dtype != MSA_KV_INT8)
+        return fail(MSA_ERR_INVALID_ARG, "kv_dtype must be MSA_KV_BF16 or MSA_KV_INT8 (got %d)", p->kv_dtype);
+    if (p->kv_dtype == MSA_KV_INT8) {
+        if (!p->k_scale || !p->v_scale) return fail(MSA_ERR_INVALID_ARG, "an int8 cache needs k_scale and v_scale");
+        if ((reinterpret_cast<uintptr_t>(p->k_scale) & 3u) || (reinterpret_cast<uintptr_t>(p->v_scale) & 3u))
+            return fail(MSA_ERR_INVALID_ARG, "k_scale or v_scale is not 4-byte aligned");
+    }
     if (p->index_key_heads != 0 && p->index_key_heads != 1 && p->index_key_heads != H)
         return fail(MSA_ERR_INVALID_ARG, "index_key_heads must be 0, 1 or num_kv_heads (got %d)", p->index_key_heads);
     if (p->block_table == nullptr) {
@@ -164,17 +171,19 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     return fn;
 }
 
-// 3-D bf16 tensor (d0 innermost, contiguous) with a box of b0 x b1 x b2 and
-// 128-byte swizzle (b0 * 2 bytes must be 128).
+// 3-D tensor (d0 innermost, contiguous) of bf16 (elem_bytes 2) or one-byte
+// elements with a box of b0 x b1 x b2 and 128-byte swizzle (b0 * elem_bytes
+// must be 128).
 msa_status make_map(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint32_t b0,
-                    uint32_t b1, uint32_t b2, const char* name) {
+                    uint32_t b1, uint32_t b2, const char* name, int elem_bytes = 2) {
     auto enc = tensor_map_encoder();
     if (!enc) return fail(MSA_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable from the driver");
     cuuint64_t dims[3] = {d0, d1, d2};
-    cuuint64_t strides[2] = {d0 * 2, d0 * d1 * 2};
+    cuuint64_t strides[2] = {d0 * elem_bytes, d0 * d1 * elem_bytes};
     cuuint32_t box[3] = {b0, b1, b2};
     cuuint32_t es[3] = {1, 1, 1};
-    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+    const CUtensorMapDataType dt = elem_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+    CUresult r = enc(map, dt, 3, const_cast<void*>(base), dims, strides, box, es,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(MSA_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed with %d", name, int(r));
@@ -218,6 +227,14 @@ struct Marks {
         return MSA_OK;
     }
 };
+
+// Key or value cache map for the attention kernels: bf16 boxes of 64 dims x
+// 64 tokens (two per block), or int8 boxes of all 128 dims x 64 tokens.
+msa_status kv_map(CUtensorMap* map, const msa_problem* p, const void* base, const char* name) {
+    const uint64_t T = p->cache_tokens, H = p->num_kv_heads;
+    if (p->kv_dtype == MSA_KV_INT8) return make_map(map, base, 128, H, T, 128, 1, 64, name, 1);
+    return make_map(map, base, 128, H, T, 64, 1, 64, name);
+}
 
 bool decode_family(const msa_problem* p) { return p->num_decode_seqs != 0; }
 bool prefill_family(const msa_problem* p) {
@@ -356,6 +373,9 @@ static msa::DecodeAttendArgs decode_args(const msa_problem* p, const CUtensorMap
     a.max_cache_len = p->max_cache_len;
     a.cache_tokens = p->cache_tokens;
     a.scale_log2 = scale_log2(p);
+    a.kv_int8 = p->kv_dtype == MSA_KV_INT8;
+    a.k_scale = a.kv_int8 ? p->k_scale : nullptr;
+    a.v_scale = a.kv_int8 ? p->v_scale : nullptr;
     a.out = out;
     a.out_bf16 = p->out_dtype == MSA_OUT_BF16;
     a.partials = nullptr;  // the cluster kernel keeps its partials in distributed shared memory
@@ -373,10 +393,9 @@ msa_status msa_attend_decode(const msa_problem* p, const void* q, const void* k_
     if (s != MSA_OK) return s;
     if (p->max_rows_per_seq > msa::kDecodeMaxRows)
         return fail(MSA_ERR_INVALID_ARG, "msa_attend_decode needs at most 8 rows per sequence (max_rows_per_seq <= 8)");
-    const uint64_t T = p->cache_tokens, H = p->num_kv_heads;
     CUtensorMap km, vm;
-    if ((s = make_map(&km, k_cache, 128, H, T, 64, 1, 64, "k_cache")) != MSA_OK) return s;
-    if ((s = make_map(&vm, v_cache, 128, H, T, 64, 1, 64, "v_cache")) != MSA_OK) return s;
+    if ((s = kv_map(&km, p, k_cache, "k_cache")) != MSA_OK) return s;
+    if ((s = kv_map(&vm, p, v_cache, "v_cache")) != MSA_OK) return s;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     cudaError_t e = cudaMemsetAsync(ws, 0, l.header_bytes, st);
@@ -410,6 +429,9 @@ static msa::PrefillAttendArgs prefill_attend_args(const msa_problem* p, const CU
     a.max_cache_len = p->max_cache_len;
     a.cache_tokens = p->cache_tokens;
     a.scale_log2 = scale_log2(p);
+    a.kv_int8 = p->kv_dtype == MSA_KV_INT8;
+    a.k_scale = a.kv_int8 ? p->k_scale : nullptr;
+    a.v_scale = a.kv_int8 ? p->v_scale : nullptr;
     a.out = out;
     a.out_bf16 = p->out_dtype == MSA_OUT_BF16;
     a.err = reinterpret_cast<uint32_t*>(ws + l.err);
@@ -418,12 +440,12 @@ static msa::PrefillAttendArgs prefill_attend_args(const msa_problem* p, const CU
 
 static msa_status attention_maps(const msa_problem* p, const void* q, const void* k, const void* v, CUtensorMap* qm,
                                  CUtensorMap* km, CUtensorMap* vm) {
-    const uint64_t T = p->cache_tokens, H = p->num_kv_heads, R = p->total_rows;
+    const uint64_t R = p->total_rows;
     const uint64_t HQ = static_cast<uint64_t>(p->num_kv_heads) * p->group_size;
     msa_status s;
     if (qm && (s = make_map(qm, q, 128, HQ, R, 64, 16, 1, "q")) != MSA_OK) return s;
-    if ((s = make_map(km, k, 128, H, T, 64, 1, 64, "k_cache")) != MSA_OK) return s;
-    return make_map(vm, v, 128, H, T, 64, 1, 64, "v_cache");
+    if ((s = kv_map(km, p, k, "k_cache")) != MSA_OK) return s;
+    return kv_map(vm, p, v, "v_cache");
 }
 
 msa_status msa_attend_prefill(const msa_problem* p, const void* q, const void* k_cache, const void* v_cache,
@@ -433,6 +455,8 @@ msa_status msa_attend_prefill(const msa_problem* p, const void* q, const void* k
     Layout l;
     msa_status s = attend_common(p, q, k_cache, v_cache, sel, nsel, out, workspace, workspace_bytes, &l);
     if (s != MSA_OK) return s;
+    if (p->kv_dtype == MSA_KV_INT8)
+        return fail(MSA_ERR_UNSUPPORTED, "the prompt-chunk attention takes bf16 key/value caches only");
     CUtensorMap qm, km, vm;
     if ((s = attention_maps(p, q, k_cache, v_cache, &qm, &km, &vm)) != MSA_OK) return s;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -456,6 +480,8 @@ msa_status msa_attend_decode_noalloc(const msa_problem* p, const void* q, const 
         return s;
     if (p->max_rows_per_seq != 1)
         return fail(MSA_ERR_INVALID_ARG, "msa_attend_decode_noalloc needs one row per sequence (max_rows_per_seq == 1)");
+    if (p->kv_dtype != MSA_KV_BF16)
+        return fail(MSA_ERR_UNSUPPORTED, "msa_attend_decode_noalloc takes bf16 key/value caches only");
     const int64_t pairs = static_cast<int64_t>(p->num_seqs) * p->num_kv_heads;
     if (pairs > msa::kNoAllocMaxPairs)
         return fail(MSA_ERR_UNSUPPORTED,
@@ -503,6 +529,8 @@ msa_status msa_forward_marked(const msa_problem* p, const void* q, const void* i
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     Marks marks{events, n_events, st};
     const bool dec = decode_family(p), pre = prefill_family(p);
+    if (pre && p->kv_dtype == MSA_KV_INT8)
+        return fail(MSA_ERR_UNSUPPORTED, "the prompt-chunk attention takes bf16 key/value caches only");
     int32_t* sel = sel_out ? sel_out : reinterpret_cast<int32_t*>(ws + l.sel);
     int32_t* nsel = nsel_out ? nsel_out : reinterpret_cast<int32_t*>(ws + l.nsel);
     const uint64_t T = p->cache_tokens, H = p->num_kv_heads;

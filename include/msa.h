@@ -37,6 +37,8 @@
  *       q    [total_rows, H*G, D]   bf16   q head g of KV head h is h*G+g
  *       iq   [total_rows, H, Di]    bf16
  *       k, v [cache_tokens, H, D]   bf16   token t of sequence b is row
+ *                                   (int8 + fp32 scales [cache_tokens, H]
+ *                                   with kv_dtype = MSA_KV_INT8)
  *       ik   [cache_tokens, H, Di]  bf16   cache_starts[b] + t  (H -> 1: shared key)
  *       out  [total_rows, H*G, D]   fp32 or bf16 (msa_problem.out_dtype)
  *       sel  [total_rows, H, top_k] int32, kept blocks ascending, -1 padded
@@ -84,6 +86,9 @@ typedef enum msa_status {
 
 enum { MSA_OUT_F32 = 0, MSA_OUT_BF16 = 1 };
 
+/* Element type of the key and value caches (msa_problem.kv_dtype). */
+enum { MSA_KV_BF16 = 0, MSA_KV_INT8 = 1 };
+
 /* One batch: B sequences, each with n_b >= 1 query rows and a cache of L_b
  * tokens (n_b <= L_b).  Host fields size grids and workspaces; device
  * fields are read by the kernels. */
@@ -123,6 +128,19 @@ typedef struct msa_problem {
      * [cache_tokens, H, Di]); 1 = one key shared by every KV head (ik is
      * [cache_tokens, 1, Di]) and s_t = iq[r,h,:] . ik[t,0,:]. */
     int32_t index_key_heads;
+    /* Key/value cache element type.  PR #1388, native Metal family commit:
+     * keys and values cached as int8 with one scale per position and head
+     * (a later commit of that PR returns to bf16).  MSA_KV_BF16 (0): k, v are
+     * bf16 [cache_tokens, H, D].  MSA_KV_INT8 (1): k, v are int8
+     * [cache_tokens, H, D] and the attention reads
+     *     k[t, h, d] = k_scale[row * H + h] * k8[row, h, d]   (v likewise)
+     * for the cache row `row` of position t; the index keys stay bf16.  The
+     * scales are device fp32 [cache_tokens, H], read only with MSA_KV_INT8
+     * (NULL otherwise).  Supported by msa_forward, msa_attend_decode and
+     * msa_attend_prefill; msa_attend_decode_noalloc takes bf16 caches only. */
+    int32_t kv_dtype;
+    const float* k_scale;
+    const float* v_scale;
 } msa_problem;
 
 /* Human-readable name of a status code (static string).  Library mechanics:

@@ -27,13 +27,20 @@ def to_dev(a: np.ndarray, device="cuda") -> torch.Tensor:
 def device_inputs(x: dict, device="cuda") -> dict:
     d = {k: to_dev(x[k], device) for k in ("q", "iq", "ik")}
     if "k" in x:
-        d["k"] = to_dev(x["k"], device)
-        d["v"] = to_dev(x["v"], device)
+        for k in ("k", "v"):
+            # int8 caches go as they are; bf16 bit patterns as bf16
+            d[k] = torch.from_numpy(np.ascontiguousarray(x[k])).to(device) if x[k].dtype == np.int8 \
+                else to_dev(x[k], device)
+    for k in ("k_scale", "v_scale"):
+        if k in x:
+            d[k] = torch.from_numpy(np.ascontiguousarray(x[k])).to(device)
     return d
 
 
 def problem(w: synth.Workload, x: dict, out_dtype=torch.float32, device="cuda", **kw):
     m = msa()
+    if "k_scale" in x and "k_scale" not in kw:  # an int8 key/value cache
+        kw = dict(kw, k_scale=torch.from_numpy(x["k_scale"]), v_scale=torch.from_numpy(x["v_scale"]))
     return m.Problem(w.H, w.G, w.seqs, device, top_k=w.top_k, scale=w.softmax_scale, out_dtype=out_dtype,
                      cache_starts=[int(s) for s in x["cache_starts"]], cache_tokens=int(sum(L for _, L in w.seqs)),
                      ik_heads=w.ik_heads, **kw)

@@ -70,6 +70,9 @@ def _problem(**over):
     (dict(cache_starts=None, block_table=1024, block_table_stride=64, page_size=64, cache_tokens=4000), 1),
     (dict(cache_starts=None, block_table=1024, block_table_stride=63, page_size=64), 1),
     (dict(cache_starts=None, block_table=1026, block_table_stride=64, page_size=64), 1),
+    # int8 key/value cache: a known element type, both scale arrays, 4-byte aligned
+    (dict(kv_dtype=2), 1), (dict(kv_dtype=1), 1), (dict(kv_dtype=1, k_scale=2048), 1),
+    (dict(kv_dtype=1, k_scale=2048, v_scale=2050), 1),
 ])
 def test_invalid_problem_rejected_on_host(over, status):
     import block_sparse_attention_index_gb300 as m
@@ -77,6 +80,13 @@ def test_invalid_problem_rejected_on_host(over, status):
     pb = _problem(**over)
     assert m.lib().msa_workspace_size(C.byref(pb), C.byref(n)) == status
     assert m.lib().msa_last_error()
+
+
+def test_int8_problem_accepted_on_host():
+    import block_sparse_attention_index_gb300 as m
+    n = C.c_size_t(0)
+    pb = _problem(kv_dtype=1, k_scale=2048, v_scale=4096)
+    assert m.lib().msa_workspace_size(C.byref(pb), C.byref(n)) == 0, m.lib().msa_last_error()
 
 
 def test_workspace_size_and_pointer_checks():
