@@ -67,13 +67,16 @@ def work_counts(w: synth.Workload):
     """Algorithmic bytes and FLOPs of one step, by stage."""
     H, G, D, Di = w.H, w.G, w.D, w.Di
     dec = [(n, L) for n, L in w.seqs if n <= DECODE_MAX_ROWS]  # decode family: 1 to 8 rows per sequence
+    kv_key_bytes_bf16 = D * 2 * 2
     pre = [(n, L) for n, L in w.seqs if n > DECODE_MAX_ROWS]
     # decode scan: every cached index key once (shared by the sequence's rows), the
     # index queries, the pooled scores out
     kh = 1 if w.ik_heads == 1 else H  # index-key heads per position
     scan_bytes = sum(L * kh * Di * 2 + n * H * Di * 2 + n * ((L + 63) // 64) * H * 4 for n, L in dec)
-    # decode attention: kept K/V blocks, q in, out (fp32) out, per row
-    att_bytes = sum(H * (_kept_keys(L - n + i, w.top_k) * D * 2 * 2) + H * G * D * (2 + 4)
+    # decode attention: kept K/V blocks (bf16, or int8 + a 4-byte scale per key for each of
+    # K and V), q in, out (fp32) out, per row
+    kv_key_bytes = (D * 1 + 4) * 2 if w.kv_dtype == "int8" else D * 2 * 2
+    att_bytes = sum(H * (_kept_keys(L - n + i, w.top_k) * kv_key_bytes) + H * G * D * (2 + 4)
                     for n, L in dec for i in range(n))
     # prompt chunks: causal index-score FLOPs and kept-block attention FLOPs
     idx_flops = 0
@@ -85,7 +88,7 @@ def work_counts(w: synth.Workload):
             att_flops += 4 * D * _kept_keys(p, w.top_k) * H * G
     return dict(scan_bytes=scan_bytes, dec_att_bytes=att_bytes, idx_flops=idx_flops, att_flops=att_flops,
                 att_exec_flops=prefill_executed_flops(w), dec_rows=sum(n for n, _ in dec),
-                pre_rows=sum(n for n, _ in pre))
+                pre_rows=sum(n for n, _ in pre), kv_bytes_frac=kv_key_bytes / kv_key_bytes_bf16)
 
 
 # Tensor-core FLOPs the prompt-chunk attention issues for one pair of kept
@@ -241,7 +244,10 @@ def _dist():
 
 
 def _to_dev(a, dev):
+    """A seeded input on the device: int8 as it is, bf16 bit patterns as bf16."""
     import torch
+    if a.dtype == np.int8:
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
     return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
 
 
@@ -258,17 +264,23 @@ def measure_gpu(w, steps, warmup, dev, dist_on, flush_bytes=512 << 20, e2e_steps
     import block_sparse_attention_index_gb300 as msa
 
     x = synth.make_inputs(w)
+    scales = {}
+    if w.kv_dtype == "int8":  # an int8 key/value cache: its scales go with the problem
+        scales = dict(k_scale=torch.from_numpy(x["k_scale"]), v_scale=torch.from_numpy(x["v_scale"]))
     if page_size:  # the same caches as a shuffled page pool with a block table
         pl = synth.paged_layout(w, x, page_size, seed=page_size)
         dx = {k: _to_dev(x[k], dev) for k in ("q", "iq")}
         dx.update({k: _to_dev(pl[k], dev) for k in ("k", "v", "ik")})
+        if scales:
+            scales = dict(k_scale=torch.from_numpy(pl["k_scale"]), v_scale=torch.from_numpy(pl["v_scale"]))
         pb = msa.Problem(w.H, w.G, w.seqs, dev, top_k=w.top_k, scale=w.softmax_scale,
                          block_table=torch.from_numpy(pl["table"]), page_size=page_size,
-                         cache_tokens=pl["num_pages"] * page_size, ik_heads=w.ik_heads)
+                         cache_tokens=pl["num_pages"] * page_size, ik_heads=w.ik_heads, **scales)
         with_e2e = False
     else:
         dx = {k: _to_dev(x[k], dev) for k in ("q", "iq", "k", "v", "ik")}
-        pb = msa.Problem(w.H, w.G, w.seqs, dev, top_k=w.top_k, scale=w.softmax_scale, ik_heads=w.ik_heads)
+        pb = msa.Problem(w.H, w.G, w.seqs, dev, top_k=w.top_k, scale=w.softmax_scale, ik_heads=w.ik_heads,
+                         **scales)
     ws = pb.workspace()
     out = pb.new_out()
     sel, nsel = pb.new_sel()
@@ -687,6 +699,8 @@ def main():
                     help="skip the short timings of the remaining configurations")
     ap.add_argument("--shared-key", default="decode_4x65536_shared_ik",
                     help="decode workload with one index key shared by all KV heads ('none' to skip)")
+    ap.add_argument("--int8", default="decode_4x65536_int8",
+                    help="decode workload with an int8 key/value cache measured in the same run ('none' to skip)")
     ap.add_argument("--paged-page-size", type=int, default=64,
                     help="also time the primary workload from a paged cache with this page size (0: skip)")
     args = ap.parse_args()
@@ -788,7 +802,7 @@ def main():
                          "latency_flushed": flushed_latency(resp, rows, ws),
                          "note": "same inputs from a shuffled page pool addressed through a block table"}
         line["gpu_launches"] += resp["launches"]
-    for key, name in (("shared_key", args.shared_key),):
+    for key, name in (("shared_key", args.shared_key), ("int8", args.int8)):
         if name == "none" or name == args.workload:
             continue
         w4 = synth.workload(name)
@@ -800,7 +814,8 @@ def main():
                      "latency_flushed": flushed_latency(res4, w4.total_rows, ws),
                      "stage_us": {"decode_scan": round(res4["stage_ms"][0] * 1e3, 2),
                                   "decode_attend": round(res4["stage_ms"][1] * 1e3, 2)},
-                     "roofline": roofline_for(w4, res4, hbm, bf16, bf16_sus, peak_kind), "note": w4.note}
+                     "roofline": roofline_for(w4, res4, hbm, bf16, bf16_sus, peak_kind), "note": w4.note,
+                     "kv_bytes_frac_of_bf16": round(work_counts(w4)["kv_bytes_frac"], 4)}
         line["gpu_launches"] += res4["launches"]
     if args.multirow != "none" and args.multirow != args.workload:
         w3 = synth.workload(args.multirow)
