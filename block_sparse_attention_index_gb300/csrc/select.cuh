@@ -10,17 +10,20 @@
 //
 // Each candidate j is a distinct 64-bit key (ordered score, ~j), so the
 // result does not depend on thread order:
-//   1. every thread takes the largest key among its strided candidates; up
+//   1. every thread takes the largest score among its strided candidates; up
 //      to kRegRounds x kChunk scores per thread are loaded at once and kept
 //      in registers (longer lists are read in rounds of kChunk, and read
 //      again for the gather);
-//   2. every warp sorts its 32 per-thread maxima (bitonic, shuffles) and
-//      takes the k-th largest: that is a lower bound of the k-th largest key
-//      overall (k distinct candidates reach it); tau = the largest bound;
-//   3. candidates >= tau are gathered (a handful for typical data) and
-//      ranked exactly by counting; the k best are placed by rank;
-//   4. if more than kCandCap candidates pass the threshold (adversarial
-//      inputs), k rounds of CTA-wide arg-max give the same answer.
+//   2. every warp sorts its 32 per-thread maxima (bitonic, shuffles, on the
+//      32-bit ordered score) and takes the k-th largest: a lower bound of the
+//      k-th largest score overall (k distinct blocks reach it); tau = the
+//      largest bound over the warps;
+//   3. the blocks scoring >= tau (a few dozen for typical data) are written
+//      to shared memory at offsets from warp prefix sums (no atomics), then
+//      ranked exactly by counting on their 64-bit keys; the k best are placed
+//      by rank;
+//   4. if more than kCandCap blocks reach tau (adversarial ties), k rounds of
+//      CTA-wide arg-max give the same answer.
 #pragma once
 
 #include "common.cuh"
@@ -33,12 +36,12 @@ constexpr int kRegRounds = 4;  // rounds kept in registers (J <= 4 x 8 x NT): ev
 
 template <int NT>
 struct SelectSmem {
-    uint64_t warp_tau[NT / 32];
+    uint32_t warp_tau[NT / 32];
+    int32_t warp_cnt[NT / 32];
     uint64_t cand[kCandCap];
     uint64_t red[NT / 32];
     uint64_t tau;
     int32_t picked[kMaxTopK];
-    int32_t count;
 };
 
 // Largest key among candidates j < J with key < below (0 if none).
@@ -76,9 +79,9 @@ __device__ int cta_select(const float* pooled, int J, int top_k, int* sel, Selec
         __syncthreads();
         return J + 1;
     }
-    // 1. per-thread maxima
+    // 1. per-thread maxima of the ordered scores (0 below every real score's code)
     const bool in_regs = J <= kRegRounds * kChunk * NT;
-    uint64_t mine = 0;
+    uint32_t mine = 0;
     float v0[kRegRounds][kChunk];
     const int rounds = (J + kChunk * NT - 1) / (kChunk * NT);  // used rounds (uniform branches below)
     if (in_regs) {
@@ -97,10 +100,7 @@ __device__ int cta_select(const float* pooled, int J, int top_k, int* sel, Selec
 #pragma unroll
                 for (int i = 0; i < kChunk; ++i) {
                     const int j = (rr * kChunk + i) * NT + tid;
-                    if (j < J) {
-                        const uint64_t key = block_key(v0[rr][i], j);
-                        mine = key > mine ? key : mine;
-                    }
+                    if (j < J) mine = max(mine, ordered_bits(v0[rr][i]));
                 }
             }
     } else {
@@ -114,35 +114,34 @@ __device__ int cta_select(const float* pooled, int J, int top_k, int* sel, Selec
 #pragma unroll
             for (int i = 0; i < kChunk; ++i) {
                 const int j = base + i * NT + tid;
-                if (j < J) {
-                    const uint64_t key = block_key(v[i], j);
-                    mine = key > mine ? key : mine;
-                }
+                if (j < J) mine = max(mine, ordered_bits(v[i]));
             }
         }
     }
     // 2. per-warp bound: sort the 32 maxima descending, take the others-th;
     // warp 0 always holds min(J, 32) >= others candidates, so tau > 0
+    const int lane = tid & 31, warp = tid >> 5;
     {
-        const int lane = tid & 31;
-        uint64_t key = mine;
+        uint32_t key = mine;
 #pragma unroll
         for (int k = 2; k <= 32; k <<= 1)
 #pragma unroll
             for (int jj = k >> 1; jj > 0; jj >>= 1) {
-                const uint64_t other = __shfl_xor_sync(0xffffffffu, key, jj);
+                const uint32_t other = __shfl_xor_sync(0xffffffffu, key, jj);
                 const bool keep_max = ((lane & k) == 0) == ((lane & jj) == 0);
-                key = keep_max ? (other > key ? other : key) : (other < key ? other : key);
+                key = keep_max ? max(other, key) : min(other, key);
             }
-        const uint64_t bound = __shfl_sync(0xffffffffu, key, others - 1);
-        if (lane == 0) sm.warp_tau[tid >> 5] = bound;
+        const uint32_t bound = __shfl_sync(0xffffffffu, key, others - 1);
+        if (lane == 0) sm.warp_tau[warp] = bound;
     }
-    if (tid == 0) sm.count = 0;
     __syncthreads();
-    uint64_t tau = 0;
+    uint32_t tau = 0;
 #pragma unroll
-    for (int w = 0; w < NT / 32; ++w) tau = sm.warp_tau[w] > tau ? sm.warp_tau[w] : tau;
-    // 3. gather candidates >= tau
+    for (int w = 0; w < NT / 32; ++w) tau = max(tau, sm.warp_tau[w]);
+    // 3. candidates: blocks with ordered score >= tau, written at offsets from
+    // an inclusive scan of the per-thread counts within each warp and the warp
+    // totals across warps (deterministic, no atomics)
+    int cnt = 0;
     if (in_regs) {
 #pragma unroll
         for (int rr = 0; rr < kRegRounds; ++rr)
@@ -150,29 +149,58 @@ __device__ int cta_select(const float* pooled, int J, int top_k, int* sel, Selec
 #pragma unroll
                 for (int i = 0; i < kChunk; ++i) {
                     const int j = (rr * kChunk + i) * NT + tid;
-                    const uint64_t key = j < J ? block_key(v0[rr][i], j) : 0;
-                    if (key >= tau) {
-                        const int slot = atomicAdd(&sm.count, 1);
-                        if (slot < kCandCap) sm.cand[slot] = key;
-                    }
+                    cnt += (j < J && ordered_bits(v0[rr][i]) >= tau) ? 1 : 0;
                 }
             }
     } else {
-        for (int j = tid; j < J; j += NT) {
-            const uint64_t key = block_key(pooled[j], j);
-            if (key >= tau) {
-                const int slot = atomicAdd(&sm.count, 1);
-                if (slot < kCandCap) sm.cand[slot] = key;
+        for (int j = tid; j < J; j += NT) cnt += ordered_bits(pooled[j]) >= tau ? 1 : 0;
+    }
+    int incl = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+    }
+    if (lane == 31) sm.warp_cnt[warp] = incl;
+    __syncthreads();
+    int n = 0, off = incl - cnt;
+#pragma unroll
+    for (int w = 0; w < NT / 32; ++w) {
+        off += w < warp ? sm.warp_cnt[w] : 0;
+        n += sm.warp_cnt[w];
+    }
+    if (n <= kCandCap && cnt > 0) {
+        if (in_regs) {
+#pragma unroll
+            for (int rr = 0; rr < kRegRounds; ++rr)
+                if (rr < rounds) {
+#pragma unroll
+                    for (int i = 0; i < kChunk; ++i) {
+                        const int j = (rr * kChunk + i) * NT + tid;
+                        if (j < J && ordered_bits(v0[rr][i]) >= tau) sm.cand[off++] = block_key(v0[rr][i], j);
+                    }
+                }
+        } else {
+            for (int j = tid; j < J; j += NT) {
+                const float m = pooled[j];
+                if (ordered_bits(m) >= tau) sm.cand[off++] = block_key(m, j);
             }
         }
     }
     __syncthreads();
-    const int n = sm.count;
     if (n <= kCandCap) {
         for (int c = tid; c < n; c += NT) {
-            uint64_t key = sm.cand[c];
-            int rank = 0;
-            for (int u = 0; u < n; ++u) rank += sm.cand[u] > key;
+            const uint64_t key = sm.cand[c];
+            int r0 = 0, r1 = 0, r2 = 0, r3 = 0;  // four independent counts per pass
+            int u = 0;
+            for (; u + 4 <= n; u += 4) {
+                r0 += sm.cand[u] > key;
+                r1 += sm.cand[u + 1] > key;
+                r2 += sm.cand[u + 2] > key;
+                r3 += sm.cand[u + 3] > key;
+            }
+            for (; u < n; ++u) r0 += sm.cand[u] > key;
+            const int rank = r0 + r1 + r2 + r3;
             if (rank < others) sm.picked[rank] = key_block(key);
         }
         __syncthreads();
@@ -197,5 +225,6 @@ __device__ int cta_select(const float* pooled, int J, int top_k, int* sel, Selec
     __syncthreads();
     return others + 1;
 }
+
 
 }  // namespace msa
