@@ -61,14 +61,14 @@ __device__ __forceinline__ void i8x4_to_bf16x4(uint32_t w, uint32_t& lo, uint32_
     hi = __byte_perm(__float_as_uint(f2), __float_as_uint(f3), 0x7632);
 }
 
-// One 64-key x 128-dim int8 tile, as TMA lands it with 128-byte swizzle in
-// the second 8 KB of a 16 KB area, rewritten in place as the bf16 layout the
-// MMAs read: dims 0-63 in the first 8 KB, dims 64-127 in the second, each a
-// [key][64 dims] tile with the same swizzle.  Row `key` is read whole into
-// registers before any of its bytes is overwritten, and no other row shares
-// those bytes, so threads may convert different rows concurrently.
-__device__ __forceinline__ void convert_i8_row(uint8_t* area, int key) {
-    const uint8_t* src = area + 8192 + key * 128;
+// One 64-key x 128-dim int8 tile, as TMA lands it with 128-byte swizzle at
+// area + upper, rewritten in place as the bf16 layout the MMAs read: dims
+// 0-63 at area, dims 64-127 at area + upper, each a [key][64 dims] tile with
+// the same swizzle (upper >= 8192, a multiple of 1024).  Row `key` is read
+// whole into registers before any of its bytes is overwritten, and no other
+// row shares those bytes, so threads may convert different rows concurrently.
+__device__ __forceinline__ void convert_i8_row(uint8_t* area, int key, int upper = 8192) {
+    const uint8_t* src = area + upper + key * 128;
     uint4 c[8];
 #pragma unroll
     for (int ch = 0; ch < 8; ++ch) c[ch] = *reinterpret_cast<const uint4*>(src + ((ch ^ (key & 7)) << 4));
@@ -79,7 +79,7 @@ __device__ __forceinline__ void convert_i8_row(uint8_t* area, int key) {
         i8x4_to_bf16x4(c[ch].y, a.z, a.w);
         i8x4_to_bf16x4(c[ch].z, b.x, b.y);
         i8x4_to_bf16x4(c[ch].w, b.z, b.w);
-        uint8_t* dst = area + (ch >> 2) * 8192 + key * 128;
+        uint8_t* dst = area + (ch >> 2) * upper + key * 128;
         const int j = (ch & 3) * 2;  // bf16 chunk (8 dims) within the 64-dim half
         *reinterpret_cast<uint4*>(dst + ((j ^ (key & 7)) << 4)) = a;
         *reinterpret_cast<uint4*>(dst + (((j + 1) ^ (key & 7)) << 4)) = b;

@@ -455,8 +455,6 @@ msa_status msa_attend_prefill(const msa_problem* p, const void* q, const void* k
     Layout l;
     msa_status s = attend_common(p, q, k_cache, v_cache, sel, nsel, out, workspace, workspace_bytes, &l);
     if (s != MSA_OK) return s;
-    if (p->kv_dtype == MSA_KV_INT8)
-        return fail(MSA_ERR_UNSUPPORTED, "the prompt-chunk attention takes bf16 key/value caches only");
     CUtensorMap qm, km, vm;
     if ((s = attention_maps(p, q, k_cache, v_cache, &qm, &km, &vm)) != MSA_OK) return s;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -529,8 +527,6 @@ msa_status msa_forward_marked(const msa_problem* p, const void* q, const void* i
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     Marks marks{events, n_events, st};
     const bool dec = decode_family(p), pre = prefill_family(p);
-    if (pre && p->kv_dtype == MSA_KV_INT8)
-        return fail(MSA_ERR_UNSUPPORTED, "the prompt-chunk attention takes bf16 key/value caches only");
     int32_t* sel = sel_out ? sel_out : reinterpret_cast<int32_t*>(ws + l.sel);
     int32_t* nsel = nsel_out ? nsel_out : reinterpret_cast<int32_t*>(ws + l.nsel);
     const uint64_t T = p->cache_tokens, H = p->num_kv_heads;

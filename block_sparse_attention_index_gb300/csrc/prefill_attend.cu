@@ -41,14 +41,32 @@
 // whole warp reads a row's selection and resolves its cache rows, up to six
 // items ahead, so the producers never wait on metadata loads).  Items are
 // strided over a grid of one CTA per SM.
+//
+// int8 key/value cache (PR #1388, native Metal family commit: keys and values
+// cached as int8 with a scale per position and head): the producers land each
+// block as one int8 tile in the upper half of its ring slot, and four more
+// warps widen the tiles in place to the same bf16 layout (17-18: K pairs and
+// the item's key and value scales, 19-20: V pairs), so the MMAs are those of
+// a bf16 cache.  The softmax multiplies each key's scores by its key scale
+// and its weights by its value scale before P enters the PV MMAs (the row
+// sum keeps the plain weights).  The K ring has two slots here, which leaves
+// room for the scales of two items.
 #include "common.cuh"
 #include "internal.h"
 
 namespace msa {
 
-constexpr int kPaThreads = 544;
-constexpr int kKStages = 3;                       // K pairs ring (its own producer warp)
-constexpr int kPvStages = 3;                      // V pairs + P pairs ring: slot i holds both operands of one PV pair
+// Block shape and ring depths: bf16 caches, or int8 caches with four converter
+// warps and a shorter K ring.
+template <bool kInt8>
+struct PaCfg {
+    static constexpr int kThreads = kInt8 ? 672 : 544;
+    static constexpr int kKStages = kInt8 ? 2 : 3;   // K pairs ring (its own producer warp)
+    static constexpr int kPvStages = 3;              // V pairs + P pairs ring: slot i holds both operands of one PV pair
+    // info ring readers: K and V producers, S and PV issuers, softmax warps, epilogue warps, converters
+    static constexpr int kInfoReaders = 2 + 2 + 8 + 4 + (kInt8 ? 4 : 0);
+    static constexpr int kScaleFloats = kInt8 ? 2 * 2 * kMaxTopK * 64 : 1;  // [item parity][key/value][block][key]
+};
 constexpr int kPairBytes = 2 * 2 * 64 * 64 * 2;  // [dim half][2 blocks x 64 keys][64 dims] bf16 = 32 KB
 constexpr int kQBytes = 2 * 16 * 64 * 2;         // [dim half][16 heads][64 dims] = 4 KB
 constexpr int kPSlotBytes = 128 * 32 * 2;        // one pair: [128 keys][32 = 16 hi + 16 lo heads] bf16 = 8 KB
@@ -56,7 +74,6 @@ constexpr int kTmemCols = 512;
 constexpr int kSCol = 0;                         // S^T buffers: columns [0,128) and [128,256)
 constexpr int kOCol = 256;                       // O^T buffers: columns [256,288) and [288,320)
 constexpr int kInfoSlots = 6;                    // decoded items published by the K producer
-constexpr int kInfoReaders = 2 + 2 + 8 + 4;      // K and V producers, S and PV issuers, softmax warps, epilogue warps
 
 // One decoded work item, shared through shared memory so that only the
 // decoder warp walks the sequence metadata and reads the selection.
@@ -67,14 +84,21 @@ struct ItemInfo {
     int32_t row[kMaxTopK];    // their first cache rows
 };
 
+template <bool kInt8>
 struct __align__(1024) AttendSmem {
+    static constexpr int kKStages = PaCfg<kInt8>::kKStages, kPvStages = PaCfg<kInt8>::kPvStages;
     uint8_t kst[kKStages][kPairBytes];
     uint8_t vst[kPvStages][kPairBytes];
     uint8_t p[kPvStages][kPSlotBytes];
     uint8_t q[2][kQBytes];
+    float sc[PaCfg<kInt8>::kScaleFloats];  // int8 cache: key and value scales of two items
     uint64_t kfull[kKStages];
     uint64_t kempty[kKStages];
-    uint64_t pv_full[kPvStages];   // V pair landed and the 8 softmax warps wrote P
+    uint64_t kraw[kKStages];       // int8 cache: the K pair's int8 tiles landed
+    uint64_t vraw[kPvStages];      // int8 cache: the V pair's int8 tiles landed
+    uint64_t sc_full[2];           // int8 cache: an item's scales written
+    uint64_t sc_empty[2];          // int8 cache: the softmax is done with them
+    uint64_t pv_full[kPvStages];   // V pair ready (bf16) and the 8 softmax warps wrote P
     uint64_t pv_empty[kPvStages];  // PV pair done: V and P slot free
     uint64_t q_full[2];
     uint64_t q_empty[2];
@@ -93,7 +117,8 @@ struct __align__(1024) AttendSmem {
     uint32_t tmem_base;
 };
 
-static_assert(sizeof(AttendSmem) + 1024 <= 227 * 1024, "prompt-chunk attention exceeds 227 KB of shared memory");
+static_assert(sizeof(AttendSmem<false>) + 1024 <= 227 * 1024, "prompt-chunk attention exceeds 227 KB of shared memory");
+static_assert(sizeof(AttendSmem<true>) + 1024 <= 227 * 1024, "prompt-chunk attention (int8) exceeds 227 KB of shared memory");
 
 // One work item as decoded by a warp: the row, KV head, position, number of
 // kept blocks and sequence (the same in every lane), and kept block `lane`
@@ -159,23 +184,34 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 }
 
 
-__global__ void __launch_bounds__(kPaThreads, 1) prefill_attend_kernel(const __grid_constant__ CUtensorMap q_map,
+template <bool kInt8>
+__global__ void __launch_bounds__(PaCfg<kInt8>::kThreads, 1) prefill_attend_kernel(const __grid_constant__ CUtensorMap q_map,
                                                                        const __grid_constant__ CUtensorMap k_map,
                                                                        const __grid_constant__ CUtensorMap v_map,
                                                                        const PrefillAttendArgs a) {
+    using Cfg = PaCfg<kInt8>;
+    constexpr int kKStages = Cfg::kKStages, kPvStages = Cfg::kPvStages;
     extern __shared__ uint8_t smem_raw[];
-    AttendSmem& sm = *reinterpret_cast<AttendSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    AttendSmem<kInt8>& sm =
+        *reinterpret_cast<AttendSmem<kInt8>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int n_items = a.total_rows * a.H;
 
     if (tid == 0) {
         for (int s = 0; s < kKStages; ++s) {
-            mbar_init(&sm.kfull[s], 1);
+            mbar_init(&sm.kfull[s], kInt8 ? 2 : 1);  // the K producer's bytes, or the two K converter warps
             mbar_init(&sm.kempty[s], 1);
+            mbar_init(&sm.kraw[s], 1);
         }
         for (int s = 0; s < kPvStages; ++s) {
-            mbar_init(&sm.pv_full[s], 1 + 8);  // V producer (with the pair's bytes) + one arrival per softmax warp
+            // V bytes (producer) or the two V converter warps, + one arrival per softmax warp
+            mbar_init(&sm.pv_full[s], (kInt8 ? 2 : 1) + 8);
             mbar_init(&sm.pv_empty[s], 1);
+            mbar_init(&sm.vraw[s], 1);
+        }
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&sm.sc_full[s], 2);
+            mbar_init(&sm.sc_empty[s], 8);
         }
         for (int s = 0; s < 2; ++s) {
             mbar_init(&sm.q_full[s], 1);
@@ -190,7 +226,7 @@ __global__ void __launch_bounds__(kPaThreads, 1) prefill_attend_kernel(const __g
         for (int s = 0; s < 2; ++s) mbar_init(&sm.drain[s], 1);
         for (int s = 0; s < kInfoSlots; ++s) {
             mbar_init(&sm.info_full[s], 32);  // every lane of the decoder warp (each releases its own writes)
-            mbar_init(&sm.info_empty[s], kInfoReaders);
+            mbar_init(&sm.info_empty[s], Cfg::kInfoReaders);
         }
         fence_mbar_init();
     }
@@ -271,11 +307,16 @@ __global__ void __launch_bounds__(kPaThreads, 1) prefill_attend_kernel(const __g
                         alive = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(&sm.kfull[s], kPairBytes);
+                    uint64_t* kbar = kInt8 ? &sm.kraw[s] : &sm.kfull[s];
+                    mbar_arrive_expect_tx(kbar, kInt8 ? kPairBytes / 2 : kPairBytes);
                     for (int half = 0; half < 2; ++half) {
                         const int tok = inf.row[min(2 * q + half, nsel - 1)];
-                        tma_load_3d(sm.kst[s] + half * 8192, &k_map, &sm.kfull[s], 0, inf.h, tok);
-                        tma_load_3d(sm.kst[s] + half * 8192 + 16384, &k_map, &sm.kfull[s], 64, inf.h, tok);
+                        if constexpr (kInt8) {  // one int8 tile per block, in the slot's upper half
+                            tma_load_3d(sm.kst[s] + 16384 + half * 8192, &k_map, kbar, 0, inf.h, tok);
+                        } else {
+                            tma_load_3d(sm.kst[s] + half * 8192, &k_map, kbar, 0, inf.h, tok);
+                            tma_load_3d(sm.kst[s] + half * 8192 + 16384, &k_map, kbar, 64, inf.h, tok);
+                        }
                     }
                 }
                 mbar_arrive(&sm.info_empty[slot]);
@@ -284,7 +325,9 @@ __global__ void __launch_bounds__(kPaThreads, 1) prefill_attend_kernel(const __g
             // timed-out wait elsewhere, too): wait, bounded, for the last phase armed on
             // every slot
             for (uint32_t s = 0; s < kKStages; ++s)
-                if (g > s) mbar_wait(&sm.kfull[s], ((s + kKStages * ((g - 1 - s) / kKStages)) / kKStages) & 1, a.err);
+                if (g > s)
+                    mbar_wait(kInt8 ? &sm.kraw[s] : &sm.kfull[s], ((s + kKStages * ((g - 1 - s) / kKStages)) / kKStages) & 1,
+                              a.err);
             for (uint32_t b = 0; b < 2; ++b)
                 if (q_armed > b) mbar_wait(&sm.q_full[b], ((b + 2 * ((q_armed - 1 - b) / 2)) >> 1) & 1, a.err);
         }
@@ -307,18 +350,25 @@ __global__ void __launch_bounds__(kPaThreads, 1) prefill_attend_kernel(const __g
                         alive = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(&sm.pv_full[s], kPairBytes);
+                    uint64_t* vbar = kInt8 ? &sm.vraw[s] : &sm.pv_full[s];
+                    mbar_arrive_expect_tx(vbar, kInt8 ? kPairBytes / 2 : kPairBytes);
                     for (int half = 0; half < 2; ++half) {
                         const int tok = inf.row[min(2 * q + half, inf.nsel - 1)];
-                        tma_load_3d(sm.vst[s] + half * 8192, &v_map, &sm.pv_full[s], 0, inf.h, tok);
-                        tma_load_3d(sm.vst[s] + half * 8192 + 16384, &v_map, &sm.pv_full[s], 64, inf.h, tok);
+                        if constexpr (kInt8) {
+                            tma_load_3d(sm.vst[s] + 16384 + half * 8192, &v_map, vbar, 0, inf.h, tok);
+                        } else {
+                            tma_load_3d(sm.vst[s] + half * 8192, &v_map, vbar, 0, inf.h, tok);
+                            tma_load_3d(sm.vst[s] + half * 8192 + 16384, &v_map, vbar, 64, inf.h, tok);
+                        }
                     }
                 }
                 mbar_arrive(&sm.info_empty[slot]);
                 if (!alive) break;
             }
             for (uint32_t s = 0; s < kPvStages; ++s)  // as for K: no copy left in flight
-                if (g > s) mbar_wait(&sm.pv_full[s], ((s + kPvStages * ((g - 1 - s) / kPvStages)) / kPvStages) & 1, a.err);
+                if (g > s)
+                    mbar_wait(kInt8 ? &sm.vraw[s] : &sm.pv_full[s],
+                              ((s + kPvStages * ((g - 1 - s) / kPvStages)) / kPvStages) & 1, a.err);
         }
     } else if (warp == 14) {
         // ---------------- S issuer (tensor-memory owner): S^T(i) = K_pair . Q^T per pair
@@ -435,6 +485,11 @@ __global__ void __launch_bounds__(kPaThreads, 1) prefill_attend_kernel(const __g
                 if (idx < nsel && inf.blk[idx] * kBlock + key_in_blk <= pos) valid_mask |= 1u << q;
             }
             const int sb = n & 1;
+            // int8 cache: this item's key and value scales ([block][key], pair q's half-`half`
+            // block is block 2q + half), written by the K converter warps
+            const float* sck = sm.sc + (kInt8 ? sb * 2 * kMaxTopK * 64 : 0);
+            const float* scv = sck + (kInt8 ? kMaxTopK * 64 : 0);
+            if (kInt8 && !mbar_wait(&sm.sc_full[sb], (n >> 1) & 1, a.err)) break;
             if (!mbar_wait(&sm.s_full[sb], (n >> 1) & 1, a.err)) break;
             tc_fence_after();
             const uint32_t s_addr = lane_addr + kSCol + sb * 128 + hh * 8;
@@ -450,8 +505,9 @@ __global__ void __launch_bounds__(kPaThreads, 1) prefill_attend_kernel(const __g
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
                     if (valid_mask & (1u << (q0 + k))) {
+                        const float ks = kInt8 ? sck[(2 * (q0 + k) + half) * 64 + key_in_blk] : 1.f;
 #pragma unroll
-                        for (int g = 0; g < 8; ++g) mx[g] = fmaxf(mx[g], __uint_as_float(v[k][g]));
+                        for (int g = 0; g < 8; ++g) mx[g] = fmaxf(mx[g], __uint_as_float(v[k][g]) * ks);
                     }
                 }
             }
@@ -494,17 +550,22 @@ __global__ void __launch_bounds__(kPaThreads, 1) prefill_attend_kernel(const __g
                         break;
                     }
                     const bool valid = (valid_mask >> q) & 1u;
+                    // int8 cache: scores times the key's scale; weights times the value's scale
+                    const float ks = kInt8 && valid ? sck[(2 * q + half) * 64 + key_in_blk] : 1.f;
+                    const float vs = kInt8 && valid ? scv[(2 * q + half) * 64 + key_in_blk] : 1.f;
                     uint32_t hi[4], lo[4];
 #pragma unroll
                     for (int g2 = 0; g2 < 4; ++g2) {
                         const float p0 =
-                            valid ? exp2f(fmaf(__uint_as_float(vv[k][2 * g2]), a.scale_log2, -ms[2 * g2])) : 0.f;
+                            valid ? exp2f(fmaf(__uint_as_float(vv[k][2 * g2]) * ks, a.scale_log2, -ms[2 * g2])) : 0.f;
                         const float p1 =
-                            valid ? exp2f(fmaf(__uint_as_float(vv[k][2 * g2 + 1]), a.scale_log2, -ms[2 * g2 + 1])) : 0.f;
+                            valid ? exp2f(fmaf(__uint_as_float(vv[k][2 * g2 + 1]) * ks, a.scale_log2, -ms[2 * g2 + 1]))
+                                  : 0.f;
                         sum[2 * g2] += p0;
                         sum[2 * g2 + 1] += p1;
-                        hi[g2] = pack_bf16x2(p0, p1);
-                        lo[g2] = pack_bf16x2(p0 - bf16_lo(hi[g2]), p1 - bf16_hi(hi[g2]));
+                        const float w0 = p0 * vs, w1 = p1 * vs;
+                        hi[g2] = pack_bf16x2(w0, w1);
+                        lo[g2] = pack_bf16x2(w0 - bf16_lo(hi[g2]), w1 - bf16_hi(hi[g2]));
                     }
                     // row `row` of the slot: 4 chunks of 16 bytes (hi 0-7, hi 8-15, lo 0-7,
                     // lo 8-15), chunk c at position c ^ ((row >> 1) & 3); this warp writes
@@ -522,6 +583,7 @@ __global__ void __launch_bounds__(kPaThreads, 1) prefill_attend_kernel(const __g
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&sm.s_empty[sb]);  // S(n) fully read
+            if (kInt8 && lane == 0) mbar_arrive(&sm.sc_empty[sb]);  // the item's scales are no longer read
 #pragma unroll
             for (int g = 0; g < 8; ++g) {
 #pragma unroll
@@ -542,6 +604,65 @@ __global__ void __launch_bounds__(kPaThreads, 1) prefill_attend_kernel(const __g
                 mbar_arrive(&sm.info_empty[slot]);
             }
             if (!alive2) break;
+        }
+    } else if (kInt8 && warp >= 17) {
+        // ---------------- int8 converters: warps 17-18 widen the K pairs (warp 17 + j takes
+        // block j of every pair) and write the item's key and value scales, warps 19-20 the V
+        // pairs; each lane widens two key rows in place
+        const int cw = warp - 17;
+        const bool is_k = cw < 2;
+        const int blk_half = cw & 1;
+        uint32_t g = 0;
+        bool alive = true;
+        for (uint32_t n = 0; alive; ++n) {
+            const int slot = n % kInfoSlots;
+            if (!mbar_wait(&sm.info_full[slot], (n / kInfoSlots) & 1, a.err)) break;
+            const ItemInfo& inf = sm.info[slot];
+            if (inf.end) break;
+            const int nsel = inf.nsel, npairs = (nsel + 1) >> 1;
+            if (is_k) {
+                // scales of the item's keys (block bi of the pair list, keys past p read as 0);
+                // warp 17 + j takes blocks j, j + 2, ...
+                const int sb = n & 1;
+                if (n >= 2 && !mbar_wait(&sm.sc_empty[sb], ((n >> 1) - 1) & 1, a.err)) break;
+                float* sck = sm.sc + sb * 2 * kMaxTopK * 64;
+                float* scv = sck + kMaxTopK * 64;
+                for (int bi = blk_half; bi < 2 * npairs; bi += 2) {
+                    const int idx = min(bi, nsel - 1);
+                    const int64_t row0 = inf.row[idx];
+                    const int t0 = inf.blk[idx] * kBlock;
+#pragma unroll
+                    for (int kk = 0; kk < 2; ++kk) {
+                        const int key = lane + 32 * kk;
+                        float ks = 0.f, vs = 0.f;
+                        if (t0 + key <= inf.p) {
+                            const int64_t si = (row0 + key) * a.H + inf.h;
+                            ks = a.k_scale[si];
+                            vs = a.v_scale[si];
+                        }
+                        sck[bi * 64 + key] = ks;
+                        scv[bi * 64 + key] = vs;
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sm.sc_full[sb]);
+            }
+            for (int q = 0; q < npairs; ++q, ++g) {
+                const int s = is_k ? static_cast<int>(g % kKStages) : static_cast<int>(g % kPvStages);
+                const uint32_t ph = is_k ? (g / kKStages) & 1 : (g / kPvStages) & 1;
+                if (!mbar_wait(is_k ? &sm.kraw[s] : &sm.vraw[s], ph, a.err)) {
+                    alive = false;
+                    break;
+                }
+                uint8_t* area = (is_k ? sm.kst[s] : sm.vst[s]) + blk_half * 8192;
+                convert_i8_row(area, lane, 16384);
+                convert_i8_row(area, lane + 32, 16384);
+                fence_proxy_async_smem();  // the tensor cores read the bf16 tile
+                __syncwarp();
+                if (lane == 0) mbar_arrive(is_k ? &sm.kfull[s] : &sm.pv_full[s]);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.info_empty[slot]);
         }
     } else {
         // ---------------- epilogue (warps 4-7; thread = TMEM lane = output dim)
@@ -594,14 +715,19 @@ __global__ void __launch_bounds__(kPaThreads, 1) prefill_attend_kernel(const __g
     }
 }
 
-cudaError_t run_prefill_attend(const PrefillAttendArgs& a, cudaStream_t stream) {
-    const size_t smem = sizeof(AttendSmem) + 1024;
-    cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(prefill_attend_kernel), smem);
+template <bool kInt8>
+static cudaError_t launch_prefill_attend(const PrefillAttendArgs& a, cudaStream_t stream) {
+    const size_t smem = sizeof(AttendSmem<kInt8>) + 1024;
+    cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(prefill_attend_kernel<kInt8>), smem);
     if (e != cudaSuccess) return e;
     const int64_t items = static_cast<int64_t>(a.total_rows) * a.H;
     const int grid = static_cast<int>(items < device_sm_count() ? items : device_sm_count());
-    prefill_attend_kernel<<<grid, kPaThreads, smem, stream>>>(*a.q_map, *a.k_map, *a.v_map, a);
+    prefill_attend_kernel<kInt8><<<grid, PaCfg<kInt8>::kThreads, smem, stream>>>(*a.q_map, *a.k_map, *a.v_map, a);
     return cudaGetLastError();
+}
+
+cudaError_t run_prefill_attend(const PrefillAttendArgs& a, cudaStream_t stream) {
+    return a.kv_int8 ? launch_prefill_attend<true>(a, stream) : launch_prefill_attend<false>(a, stream);
 }
 
 }  // namespace msa

@@ -114,3 +114,61 @@ def test_int8_not_taken_by_allocation_free_entry_point():
     with pytest.raises(m.MsaError) as e:
         m.attend_decode_noalloc(pb, dx["q"], dx["k"], dx["v"], sel, nsel)
     assert e.value.status == 2  # MSA_ERR_UNSUPPORTED
+
+
+PROMPT_SEQS = [(200, 1300), (65, 65), (130, 5000), (9, 3000), (1, 2000)]
+
+
+@pytest.mark.parametrize("H,G", [(1, 16), (4, 16), (2, 13), (8, 8)])
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
+def test_int8_prompt_chunks(H, G, out_dtype):
+    """Prompt chunks (and a decode row beside them) from an int8 cache: the
+    tcgen05 attention widens the int8 tiles to bf16 in shared memory."""
+    w = _w("int8_prompt", PROMPT_SEQS, H=H, G=G, seed=90 + H + G)
+    x = synth.make_inputs(w)
+    out, sel, nsel = run_forward(w, x, out_dtype)
+    ref = oracle_forward(w, x)
+    assert_selection_equal(sel, nsel, ref)
+    assert_out_close(out, ref["out"], out_dtype)
+
+
+def test_int8_attend_prefill_given_selection():
+    m = msa()
+    w = _w("int8_prefill_given", [(300, 2500), (17, 700)], seed=91)
+    x = synth.make_inputs(w)
+    dx = device_inputs(x)
+    pb = problem(w, x)
+    ref = oracle_forward(w, x)
+    out = m.attend_prefill(pb, dx["q"], dx["k"], dx["v"], torch.from_numpy(ref["sel"]).cuda(),
+                           torch.from_numpy(ref["nsel"]).cuda())
+    torch.cuda.synchronize()
+    assert_out_close(out, ref["out"], torch.float32)
+
+
+def test_int8_paged_prompt_chunk():
+    m = msa()
+    w = _w("int8_paged_prompt", [(256, 3000), (1, 900), (40, 200)], seed=92)
+    x = synth.make_inputs(w)
+    pl = synth.paged_layout(w, x, 256, seed=12)
+    pb = m.Problem(w.H, w.G, w.seqs, "cuda", top_k=w.top_k, scale=w.softmax_scale,
+                   block_table=torch.from_numpy(pl["table"]), page_size=256, cache_tokens=pl["num_pages"] * 256,
+                   k_scale=torch.from_numpy(pl["k_scale"]), v_scale=torch.from_numpy(pl["v_scale"]))
+    dev = {k: torch.from_numpy(np.ascontiguousarray(pl[k])).cuda() for k in ("k", "v")}
+    dq = device_inputs({k: x[k] for k in ("q", "iq")} | {"ik": pl["ik"]})
+    ws = pb.workspace()
+    out, sel, nsel = m.forward(pb, dq["q"], dq["iq"], dev["k"], dev["v"], dq["ik"], workspace=ws)
+    torch.cuda.synchronize()
+    assert m.error_word(ws) == 0
+    ref = oracle_forward(w, x)
+    assert_selection_equal(sel, nsel, ref)
+    assert_out_close(out, ref["out"], torch.float32)
+
+
+def test_int8_prefill_4096_at_8192_full_size():
+    """The 4,096-row prompt chunk at an 8,192-token prefix from an int8 cache."""
+    w = synth.workload("prefill_4096_at_8192_int8")
+    x = synth.make_inputs(w)
+    out, sel, nsel = run_forward(w, x)
+    ref = oracle_forward(w, x)
+    assert_selection_equal(sel, nsel, ref)
+    assert_out_close(out, ref["out"], torch.float32)
