@@ -701,6 +701,8 @@ def main():
                     help="decode workload with one index key shared by all KV heads ('none' to skip)")
     ap.add_argument("--int8", default="decode_4x65536_int8",
                     help="decode workload with an int8 key/value cache measured in the same run ('none' to skip)")
+    ap.add_argument("--int8-prefill", default="prefill_4096_at_8192_int8",
+                    help="prompt-chunk workload with an int8 key/value cache measured in the same run ('none' to skip)")
     ap.add_argument("--paged-page-size", type=int, default=64,
                     help="also time the primary workload from a paged cache with this page size (0: skip)")
     args = ap.parse_args()
@@ -802,7 +804,7 @@ def main():
                          "latency_flushed": flushed_latency(resp, rows, ws),
                          "note": "same inputs from a shuffled page pool addressed through a block table"}
         line["gpu_launches"] += resp["launches"]
-    for key, name in (("shared_key", args.shared_key), ("int8", args.int8)):
+    for key, name in (("shared_key", args.shared_key), ("int8", args.int8), ("int8_prefill", args.int8_prefill)):
         if name == "none" or name == args.workload:
             continue
         w4 = synth.workload(name)
@@ -812,8 +814,8 @@ def main():
                      "value": round(whole_job_rate(w4.total_rows, ws, step_ms(res4)), 1),
                      "unit": "rows/s", "ms_per_step": round(step_ms(res4), 5), "l2": timing_note(res4),
                      "latency_flushed": flushed_latency(res4, w4.total_rows, ws),
-                     "stage_us": {"decode_scan": round(res4["stage_ms"][0] * 1e3, 2),
-                                  "decode_attend": round(res4["stage_ms"][1] * 1e3, 2)},
+                     "stage_us": {k: round(v * 1e3, 2) for k, v in zip(
+                         ("decode_scan", "decode_attend", "prefill_index", "prefill_attend"), res4["stage_ms"])},
                      "roofline": roofline_for(w4, res4, hbm, bf16, bf16_sus, peak_kind), "note": w4.note,
                      "kv_bytes_frac_of_bf16": round(work_counts(w4)["kv_bytes_frac"], 4)}
         line["gpu_launches"] += res4["launches"]
