@@ -41,7 +41,7 @@ class MsaProblem(C.Structure):
         ("num_decode_seqs", C.c_int32), ("cu_rows", C.c_void_p), ("cache_lens", C.c_void_p),
         ("cache_starts", C.c_void_p), ("block_table", C.c_void_p), ("block_table_stride", C.c_int32),
         ("page_size", C.c_int32), ("index_key_heads", C.c_int32), ("kv_dtype", C.c_int32),
-        ("k_scale", C.c_void_p), ("v_scale", C.c_void_p),
+        ("k_scale", C.c_void_p), ("v_scale", C.c_void_p), ("num_decode_rows", C.c_int32),
     ]
 
 
@@ -127,11 +127,14 @@ class Problem:
     index key per position shared by every KV head (ik is [T, 1, Di]).
     k_scale, v_scale (float32 [cache_tokens, H] device tensors): the key and
     value caches are int8 with these per-(cache row, head) scales.
+    num_decode_rows: host count of decode-family rows ("auto": from seqs_host;
+    0: unknown, the decode attention then covers every row slot).
     """
 
     def __init__(self, H, G, seqs_host, device, top_k=16, scale=None, out_dtype=torch.float32,
                  cache_starts=None, cache_tokens=None, D=128, Di=64, S=64, num_decode_seqs="auto",
-                 block_table=None, page_size=0, ik_heads=0, k_scale=None, v_scale=None):
+                 block_table=None, page_size=0, ik_heads=0, k_scale=None, v_scale=None,
+                 num_decode_rows="auto"):
         self.H, self.G, self.D, self.Di, self.S, self.top_k = H, G, D, Di, S, top_k
         self.device = torch.device(device)
         if self.device.type == "cuda" and self.device.index is None:
@@ -173,6 +176,9 @@ class Problem:
             self.cache_starts.data_ptr() if self.block_table is None else None,
             None if self.block_table is None else self.block_table.data_ptr(),
             0 if self.block_table is None else int(self.block_table.shape[1]), int(page_size), int(ik_heads))
+        if num_decode_rows == "auto":  # rows of the decode-family sequences (1 to 8 rows each)
+            num_decode_rows = sum(n for n in rows if n <= DECODE_MAX_ROWS)
+        self.c.num_decode_rows = int(num_decode_rows)
         self.KH = 1 if (ik_heads == 1 or H == 1) else H  # index-key heads per position
         if (k_scale is None) != (v_scale is None):
             raise ValueError("k_scale and v_scale go together")

@@ -110,10 +110,31 @@ __global__ void __launch_bounds__(kClThreads) decode_cluster_kernel(const __grid
     extern __shared__ uint8_t smem_raw[];
     ClusterSmem& sm = *reinterpret_cast<ClusterSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int rank = static_cast<int>(cluster_rank());
-    const int h = blockIdx.y, row_slot = blockIdx.z;  // b * RS + i: row i of sequence b
-    const int b = row_slot / a.rows_per_seq, row_in_seq = row_slot - b * a.rows_per_seq;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int H = a.H, G = a.G;
+    const int h = blockIdx.y;
+    int b, row_in_seq;
+    if (a.drow_prefix != nullptr) {
+        // compact grid (fused path): blockIdx.z is a decode-family row; its sequence comes from
+        // the prefix of rows the index scan wrote, so this wait comes first
+        pdl_wait();
+        const int z = blockIdx.z, B = a.num_seqs;
+        const int total = a.drow_prefix[B];
+        if (z == 0 && h == 0 && rank == 0 && tid == 0 && total > static_cast<int>(gridDim.z))
+            atomicOr(a.err, kErrBadMetadata);  // the host's row count is below the device metadata's
+        if (z >= total) return;  // a host count above the device's: nothing to do
+        int lo = 0, hi = B;  // largest b with drow_prefix[b] <= z
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (a.drow_prefix[mid] <= z) lo = mid; else hi = mid;
+        }
+        b = lo;
+        row_in_seq = z - a.drow_prefix[b];
+    } else {  // one entry per row slot: b * RS + i is row i of sequence b
+        b = blockIdx.z / a.rows_per_seq;
+        row_in_seq = blockIdx.z - b * a.rows_per_seq;
+    }
+    const int row_slot = b * a.rows_per_seq + row_in_seq;  // the row's pooled-score slot
 
     // ---- prologue: only inputs that no earlier kernel of the step writes
     const int nrows = a.cu_rows[b + 1] - a.cu_rows[b];
@@ -424,7 +445,7 @@ cudaError_t run_decode_cluster(const DecodeAttendArgs& a, bool after_scan, cudaS
     cudaError_t e = ensure_smem_limit(fn, smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(kCluster, a.H, a.num_seqs * a.rows_per_seq);
+    cfg.gridDim = dim3(kCluster, a.H, a.drow_prefix != nullptr ? a.decode_rows : a.num_seqs * a.rows_per_seq);
     cfg.blockDim = dim3(kClThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;

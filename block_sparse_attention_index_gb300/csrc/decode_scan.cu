@@ -137,6 +137,33 @@ __global__ void __launch_bounds__(ScanCfg<H, kShared>::kThreads, 1) decode_scan_
     }
     if (tid == 0) prefix[a.num_seqs] = carry;
     __syncthreads();
+    if (blockIdx.x == 0 && a.drow_prefix != nullptr) {
+        // exclusive prefix of decode-family rows per sequence: the decode attention's grid has
+        // one entry per such row and finds the row's sequence here (same chunked block scan)
+        int carry2 = 0;
+        for (int base = 0; base < a.num_seqs; base += Cfg::kThreads) {
+            const int b = base + tid;
+            const int nr = b < a.num_seqs ? a.cu_rows[b + 1] - a.cu_rows[b] : 0;
+            const int rows = nr >= 1 && nr <= kDecodeMaxRows ? nr : 0;
+            int incl = rows;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int v = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += v;
+            }
+            if (lane == 31) warp_tot[warp] = incl;
+            __syncthreads();
+            int before = 0, chunk_total = 0;
+            for (int w = 0; w < Cfg::kThreads / 32; ++w) {
+                if (w < warp) before += warp_tot[w];
+                chunk_total += warp_tot[w];
+            }
+            if (b < a.num_seqs) a.drow_prefix[b] = carry2 + before + incl - rows;
+            __syncthreads();
+            carry2 += chunk_total;
+        }
+        if (tid == 0) a.drow_prefix[a.num_seqs] = carry2;
+    }
     // the attention kernel may be scheduled now; it waits for this grid to
     // finish before it reads the pooled scores
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");

@@ -64,6 +64,7 @@ struct ScanArgs {
     float* pooled;        // [B * RS, H, max_blocks]: slot b * RS + i = row i of sequence b
     int32_t* clear_words; // zeroed by the scan (tickets of the attention kernel)
     int n_clear;
+    int32_t* drow_prefix; // nullable: [B + 1] prefix of decode-family rows per sequence, written by CTA 0
     uint32_t* err;
 };
 
@@ -73,7 +74,10 @@ struct DecodeAttendArgs {
     const uint16_t* q;
     const float* pooled;       // fused path: pooled scores [B * RS, H, max_blocks] (nullptr when sel is given)
     int max_blocks;
-    int rows_per_seq;          // RS: grid z = B * RS (sequence b, row i at z = b * RS + i)
+    int rows_per_seq;          // RS: pooled slot of row i of sequence b = b * RS + i; grid z = B * RS slots
+    const int32_t* drow_prefix;  // fused path, nullable: grid z = decode-family row z, its sequence found in
+                                 // this prefix of rows per sequence (written by the scan)
+    int decode_rows;             // with drow_prefix: the grid's z extent (host count of decode-family rows)
     const int32_t* sel_in;     // staged path: given selection
     const int32_t* nsel_in;
     const int32_t* cu_rows;

@@ -74,6 +74,12 @@ msa_status check_problem(const msa_problem* p) {
         if ((reinterpret_cast<uintptr_t>(p->k_scale) & 3u) || (reinterpret_cast<uintptr_t>(p->v_scale) & 3u))
             return fail(MSA_ERR_INVALID_ARG, "k_scale or v_scale is not 4-byte aligned");
     }
+    if (p->num_decode_rows > p->total_rows)
+        return fail(MSA_ERR_INVALID_ARG, "num_decode_rows > total_rows");
+    if (p->num_decode_rows > 0 && p->num_decode_seqs >= 0 &&
+        (p->num_decode_rows < p->num_decode_seqs ||
+         static_cast<int64_t>(p->num_decode_rows) > static_cast<int64_t>(p->num_decode_seqs) * msa::kDecodeMaxRows))
+        return fail(MSA_ERR_INVALID_ARG, "num_decode_rows must lie in [num_decode_seqs, 8 x num_decode_seqs]");
     if (p->index_key_heads != 0 && p->index_key_heads != 1 && p->index_key_heads != H)
         return fail(MSA_ERR_INVALID_ARG, "index_key_heads must be 0, 1 or num_kv_heads (got %d)", p->index_key_heads);
     if (p->block_table == nullptr) {
@@ -117,7 +123,8 @@ msa::CacheRows cache_rows_of(const msa_problem* p) {
 }
 
 struct Layout {
-    size_t err = 0, tickets = 0, idx_tickets = 0, pooled = 0, partials = 0, sel = 0, nsel = 0, idx_cand = 0, total = 0;
+    size_t err = 0, tickets = 0, idx_tickets = 0, pooled = 0, partials = 0, sel = 0, nsel = 0, idx_cand = 0,
+           drow_prefix = 0, total = 0;
     size_t header_bytes = 0;  // error word + tickets, cleared at the start of a call
 };
 
@@ -153,6 +160,8 @@ Layout layout_of(const msa_problem* p) {
     l.idx_cand = off;  // prompt-chunk indexer: per-split top-15 lists
     if (p->max_rows_per_seq > msa::kDecodeMaxRows && p->num_decode_seqs != p->num_seqs)
         off = align256(off + R * H * msa::kIdxMaxSplit * 15 * sizeof(uint64_t));
+    l.drow_prefix = off;  // decode-family rows per sequence, prefix (compact decode attention grid)
+    off = align256(off + (B + 1) * sizeof(int32_t));
     l.total = off;
     return l;
 }
@@ -237,6 +246,13 @@ msa_status kv_map(CUtensorMap* map, const msa_problem* p, const void* base, cons
 }
 
 bool decode_family(const msa_problem* p) { return p->num_decode_seqs != 0; }
+
+// The decode attention's grid covers the host's count of decode-family rows
+// (when given and smaller than the row slots) instead of every row slot.
+bool compact_decode_grid(const msa_problem* p) {
+    return p->num_decode_rows > 0 &&
+           static_cast<int64_t>(p->num_decode_rows) < static_cast<int64_t>(p->num_seqs) * decode_rows_per_seq(p);
+}
 bool prefill_family(const msa_problem* p) {
     return p->max_rows_per_seq > msa::kDecodeMaxRows && p->num_decode_seqs != p->num_seqs;
 }
@@ -566,6 +582,7 @@ msa_status msa_forward_marked(const msa_problem* p, const void* q, const void* i
         sa.pooled = reinterpret_cast<float*>(ws + l.pooled);
         sa.clear_words = reinterpret_cast<int32_t*>(ws + l.err);
         sa.n_clear = static_cast<int>(l.header_bytes / sizeof(int32_t));
+        sa.drow_prefix = compact_decode_grid(p) ? reinterpret_cast<int32_t*>(ws + l.drow_prefix) : nullptr;
         sa.err = reinterpret_cast<uint32_t*>(ws + l.err);
         if ((e = msa::run_decode_scan(sa, st)) != cudaSuccess) return cuda_fail(e, "decode scan launch");
         if ((s = marks.mark(1)) != MSA_OK) return s;
@@ -574,6 +591,8 @@ msa_status msa_forward_marked(const msa_problem* p, const void* q, const void* i
         da.max_blocks = max_blocks;
         da.sel_out = sel;
         da.nsel_out = nsel;
+        da.drow_prefix = sa.drow_prefix;
+        da.decode_rows = p->num_decode_rows;
         const bool pdl = events == nullptr || n_events < 2 || events[1] == nullptr;  // a mark in between breaks it
         if ((e = msa::run_decode_cluster(da, pdl, st)) != cudaSuccess) return cuda_fail(e, "decode attention launch");
         if ((s = marks.mark(2)) != MSA_OK) return s;

@@ -141,6 +141,15 @@ typedef struct msa_problem {
     int32_t kv_dtype;
     const float* k_scale;
     const float* v_scale;
+    /* Host count of the rows of decode-family sequences (1 to 8 rows each),
+     * or <= 0 if unknown.  msa_forward sizes the decode attention's grid by
+     * it instead of num_seqs x min(max_rows_per_seq, 8) row slots, which in a
+     * batch that mixes decode rows with prompt chunks launches mostly empty
+     * work; a count below the device metadata's sets the bad-metadata bit of
+     * the error word (the rows past it get no output), one above it only
+     * launches work that exits at once.  Library mechanics: the pages have
+     * no counterpart. */
+    int32_t num_decode_rows;
 } msa_problem;
 
 /* Human-readable name of a status code (static string).  Library mechanics:

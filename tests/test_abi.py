@@ -73,6 +73,9 @@ def _problem(**over):
     # int8 key/value cache: a known element type, both scale arrays, 4-byte aligned
     (dict(kv_dtype=2), 1), (dict(kv_dtype=1), 1), (dict(kv_dtype=1, k_scale=2048), 1),
     (dict(kv_dtype=1, k_scale=2048, v_scale=2050), 1),
+    # host count of decode-family rows: within the rows and 1..8 per decode sequence
+    (dict(num_decode_rows=2), 1), (dict(num_seqs=2, total_rows=20, max_rows_per_seq=16, num_decode_seqs=1,
+                                        num_decode_rows=9), 1),
 ])
 def test_invalid_problem_rejected_on_host(over, status):
     import block_sparse_attention_index_gb300 as m

@@ -78,3 +78,29 @@ def test_multirow_4x4_at_65536():
     assert_selection_equal(sel, nsel, ref)
     err = assert_out_close(out, ref["out"], torch.float32)
     assert np.isfinite(err)
+
+
+@pytest.mark.parametrize("count", ["auto", 0, "over", "under"])
+def test_mixed_batch_decode_row_count(count):
+    """The host's count of decode-family rows sizes the decode attention's grid
+    in a mixed batch: exact ('auto'), unknown (0: one entry per row slot) or
+    above the device metadata's count give the oracle's outputs; a count below
+    it sets the bad-metadata bit."""
+    m = msa()
+    w = synth.Workload("mixed_rows", H=4, G=16, seqs=[(3, 3000), (200, 1300), (1, 2000), (8, 900), (64, 700)],
+                       seed=64)
+    x = synth.make_inputs(w)
+    exact = 3 + 1 + 8
+    n = {"auto": "auto", 0: 0, "over": exact + 5, "under": exact - 2}[count]
+    dx = device_inputs(x)
+    pb = problem(w, x, num_decode_rows=n)
+    ws = pb.workspace()
+    out, sel, nsel = m.forward(pb, dx["q"], dx["iq"], dx["k"], dx["v"], dx["ik"], workspace=ws)
+    torch.cuda.synchronize()
+    if count == "under":
+        assert m.error_word(ws) & m.ERR_BAD_METADATA
+        return
+    assert m.error_word(ws) == 0
+    ref = oracle_forward(w, x)
+    assert_selection_equal(sel, nsel, ref)
+    assert_out_close(out, ref["out"], torch.float32)
