@@ -44,10 +44,10 @@
 //
 // int8 key/value cache (PR #1388, native Metal family commit: keys and values
 // cached as int8 with a scale per position and head): the producers land each
-// block as one int8 tile in the upper half of its ring slot, and four more
-// warps widen the tiles in place to the same bf16 layout (17-18: K pairs and
-// the item's key and value scales, 19-20: V pairs), so the MMAs are those of
-// a bf16 cache.  The softmax multiplies each key's scores by its key scale
+// block as one int8 tile in the upper half of its ring slot, and eight more
+// warps widen the tiles in place to the same bf16 layout (17-20: K pairs and
+// the item's key and value scales, 21-24: V pairs; a lane widens one key row
+// of each pair), so the MMAs are those of a bf16 cache.  The softmax multiplies each key's scores by its key scale
 // and its weights by its value scale before P enters the PV MMAs (the row
 // sum keeps the plain weights).  The K ring has two slots here, which leaves
 // room for the scales of two items.
@@ -60,11 +60,12 @@ namespace msa {
 // warps and a shorter K ring.
 template <bool kInt8>
 struct PaCfg {
-    static constexpr int kThreads = kInt8 ? 672 : 544;
+    static constexpr int kConverters = kInt8 ? 8 : 0;  // warps 17 .. 24: 4 for K, 4 for V
+    static constexpr int kThreads = 544 + 32 * kConverters;
     static constexpr int kKStages = kInt8 ? 2 : 3;   // K pairs ring (its own producer warp)
     static constexpr int kPvStages = 3;              // V pairs + P pairs ring: slot i holds both operands of one PV pair
     // info ring readers: K and V producers, S and PV issuers, softmax warps, epilogue warps, converters
-    static constexpr int kInfoReaders = 2 + 2 + 8 + 4 + (kInt8 ? 4 : 0);
+    static constexpr int kInfoReaders = 2 + 2 + 8 + 4 + kConverters;
     static constexpr int kScaleFloats = kInt8 ? 2 * 2 * kMaxTopK * 64 : 1;  // [item parity][key/value][block][key]
 };
 constexpr int kPairBytes = 2 * 2 * 64 * 64 * 2;  // [dim half][2 blocks x 64 keys][64 dims] bf16 = 32 KB
@@ -199,18 +200,18 @@ __global__ void __launch_bounds__(PaCfg<kInt8>::kThreads, 1) prefill_attend_kern
 
     if (tid == 0) {
         for (int s = 0; s < kKStages; ++s) {
-            mbar_init(&sm.kfull[s], kInt8 ? 2 : 1);  // the K producer's bytes, or the two K converter warps
+            mbar_init(&sm.kfull[s], kInt8 ? 4 : 1);  // the K producer's bytes, or the four K converter warps
             mbar_init(&sm.kempty[s], 1);
             mbar_init(&sm.kraw[s], 1);
         }
         for (int s = 0; s < kPvStages; ++s) {
-            // V bytes (producer) or the two V converter warps, + one arrival per softmax warp
-            mbar_init(&sm.pv_full[s], (kInt8 ? 2 : 1) + 8);
+            // V bytes (producer) or the four V converter warps, + one arrival per softmax warp
+            mbar_init(&sm.pv_full[s], (kInt8 ? 4 : 1) + 8);
             mbar_init(&sm.pv_empty[s], 1);
             mbar_init(&sm.vraw[s], 1);
         }
         for (int s = 0; s < 2; ++s) {
-            mbar_init(&sm.sc_full[s], 2);
+            mbar_init(&sm.sc_full[s], 4);
             mbar_init(&sm.sc_empty[s], 8);
         }
         for (int s = 0; s < 2; ++s) {
@@ -606,12 +607,12 @@ __global__ void __launch_bounds__(PaCfg<kInt8>::kThreads, 1) prefill_attend_kern
             if (!alive2) break;
         }
     } else if (kInt8 && warp >= 17) {
-        // ---------------- int8 converters: warps 17-18 widen the K pairs (warp 17 + j takes
-        // block j of every pair) and write the item's key and value scales, warps 19-20 the V
-        // pairs; each lane widens two key rows in place
+        // ---------------- int8 converters: warps 17-20 widen the K pairs (warp 17 + j takes keys
+        // 32 (j & 1) .. + 31 of block j / 2 of every pair) and write the item's key and value
+        // scales, warps 21-24 the V pairs; each lane widens one key row in place
         const int cw = warp - 17;
-        const bool is_k = cw < 2;
-        const int blk_half = cw & 1;
+        const bool is_k = cw < 4;
+        const int part = cw & 3;  // block part >> 1, keys 32 (part & 1) ..
         uint32_t g = 0;
         bool alive = true;
         for (uint32_t n = 0; alive; ++n) {
@@ -622,12 +623,12 @@ __global__ void __launch_bounds__(PaCfg<kInt8>::kThreads, 1) prefill_attend_kern
             const int nsel = inf.nsel, npairs = (nsel + 1) >> 1;
             if (is_k) {
                 // scales of the item's keys (block bi of the pair list, keys past p read as 0);
-                // warp 17 + j takes blocks j, j + 2, ...
+                // warp 17 + j takes blocks j, j + 4, ...
                 const int sb = n & 1;
                 if (n >= 2 && !mbar_wait(&sm.sc_empty[sb], ((n >> 1) - 1) & 1, a.err)) break;
                 float* sck = sm.sc + sb * 2 * kMaxTopK * 64;
                 float* scv = sck + kMaxTopK * 64;
-                for (int bi = blk_half; bi < 2 * npairs; bi += 2) {
+                for (int bi = part; bi < 2 * npairs; bi += 4) {
                     const int idx = min(bi, nsel - 1);
                     const int64_t row0 = inf.row[idx];
                     const int t0 = inf.blk[idx] * kBlock;
@@ -654,9 +655,8 @@ __global__ void __launch_bounds__(PaCfg<kInt8>::kThreads, 1) prefill_attend_kern
                     alive = false;
                     break;
                 }
-                uint8_t* area = (is_k ? sm.kst[s] : sm.vst[s]) + blk_half * 8192;
-                convert_i8_row(area, lane, 16384);
-                convert_i8_row(area, lane + 32, 16384);
+                uint8_t* area = (is_k ? sm.kst[s] : sm.vst[s]) + (part >> 1) * 8192;
+                convert_i8_row(area, (part & 1) * 32 + lane, 16384);
                 fence_proxy_async_smem();  // the tensor cores read the bf16 tile
                 __syncwarp();
                 if (lane == 0) mbar_arrive(is_k ? &sm.kfull[s] : &sm.pv_full[s]);
