@@ -146,7 +146,7 @@ __global__ void __launch_bounds__(kClThreads) decode_cluster_kernel(const __grid
     const bool meta_ok = !(r < 0 || r >= a.total_rows || L < nrows || L > a.max_cache_len || nrows > a.rows_per_seq) &&
                          seq_rows_ok(a.cache, b, L, a.cache_tokens);
     if (tid == 0) {
-        mbar_init(&sm.bar, 1);
+        mbar_init(&sm.bar, 4);  // one arrival from each of warps 0-3 (with the bytes it copies)
         fence_mbar_init();
     }
     if (meta_ok) {
@@ -191,52 +191,70 @@ __global__ void __launch_bounds__(kClThreads) decode_cluster_kernel(const __grid
     cluster_arrive_relaxed();  // matched by cluster_wait() before the first remote store
     const int p = L - nrows + row_in_seq;  // this row's position
     const int J = p / kBlock;
-    if constexpr (!kSelGiven) {
+    // ---- the kept blocks: k < nsel, block kept(k); this CTA takes k = rank and rank + kCluster
+    int nsel, others = 0;
+    if constexpr (kSelGiven) {
+        __syncthreads();  // the given list (read before the wait) visible to every thread
+        nsel = sm.nsel;
+    } else {
+        // the fused selection ranks the blocks; the kept list is [best first ..., J] and
+        // the copies go out right after the ranking (the caller's ascending list is written
+        // while they are in flight)
         const float* pooled = a.pooled + (static_cast<int64_t>(row_slot) * H + h) * a.max_blocks;
-        const int n = cta_select<kClThreads>(pooled, J, a.top_k, sm.sel, sm.select);
-        if (tid == 0) sm.nsel = n;
+        others = cta_select_ranked<kClThreads>(pooled, J, a.top_k, sm.select);
+        nsel = others + 1;
     }
-    __syncthreads();
-    const int nsel = sm.nsel;
-    if constexpr (!kSelGiven) {
-        if (rank == 0 && a.sel_out != nullptr && tid < a.top_k) {
-            a.sel_out[(static_cast<int64_t>(r) * H + h) * a.top_k + tid] = sm.sel[tid];
-            if (tid == 0) a.nsel_out[static_cast<int64_t>(r) * H + h] = nsel;
-        }
-    }
-    // ---- this CTA's blocks: kept blocks rank and rank + kCluster
+    auto kept = [&](int k) { return kSelGiven ? sm.sel[k] : (k < others ? sm.select.picked[k] : J); };
     int nmy = (rank < nsel) + (rank + kCluster < nsel);
     int blk[2] = {J, J};
     for (int i = 0; i < nmy; ++i) {
-        blk[i] = sm.sel[rank + i * kCluster];
+        blk[i] = kept(rank + i * kCluster);
         if (blk[i] < 0 || blk[i] > J) {  // a given selection outside the causal range
             if (tid == 0) atomicOr(a.err, kErrBadMetadata);
             blk[i] = J;
         }
     }
-    // bytes per kept block: K and V, bf16 (four 64-dim boxes) or int8 (two 128-dim boxes)
-    if (tid == 0 && nmy > 0) mbar_arrive_expect_tx(&sm.bar, nmy * (kInt8 ? 2 : 4) * 64 * 64 * 2);
-    __syncthreads();  // the expected bytes are registered before any copy lands; q visible to every warp
-    // Warp w issues the copies of block w / 2, K (w even) or V (w odd): one thread issues TMA boxes
-    // at a bounded rate, so four issuers land the 64 KB sooner than one.
-    if (lane == 0 && warp < 2 * nmy) {
-        const int i = warp >> 1;
-        const int bi = i == 0 ? blk[0] : blk[1];  // no dynamic index into blk: it stays in registers
-        int64_t row = block_row(a.cache, b, static_cast<int64_t>(bi) * kBlock);
-        if (row < 0) {  // page outside the pool
-            atomicOr(a.err, kErrBadMetadata);
-            row = 0;
-        }
-        const int tok = static_cast<int>(row);
-        if constexpr (kInt8) {  // one int8 tile per block into the upper 8 KB, widened in place below
-            if ((warp & 1) == 0) tma_load_3d(sm.k[i][1], &k_map, &sm.bar, 0, h, tok);
-            else tma_load_3d(sm.v[i][1], &v_map, &sm.bar, 0, h, tok);
-        } else if ((warp & 1) == 0) {
-            tma_load_3d(sm.k[i][0], &k_map, &sm.bar, 0, h, tok);
-            tma_load_3d(sm.k[i][1], &k_map, &sm.bar, 64, h, tok);
+    // Warp w issues the copies of block w / 2, K (w even) or V (w odd), each arming the barrier
+    // with its own bytes first (warps without a block arrive without bytes): one thread issues TMA
+    // boxes at a bounded rate, so four issuers land the 64 KB sooner than one.
+    if (lane == 0 && warp < 4) {
+        if (warp < 2 * nmy) {
+            const int i = warp >> 1;
+            const int bi = i == 0 ? blk[0] : blk[1];  // no dynamic index into blk: it stays in registers
+            int64_t row = block_row(a.cache, b, static_cast<int64_t>(bi) * kBlock);
+            if (row < 0) {  // page outside the pool
+                atomicOr(a.err, kErrBadMetadata);
+                row = 0;
+            }
+            const int tok = static_cast<int>(row);
+            // bytes per half block: K or V, bf16 (two 64-dim boxes) or int8 (one 128-dim box)
+            mbar_arrive_expect_tx(&sm.bar, (kInt8 ? 1 : 2) * 64 * 64 * 2);
+            if constexpr (kInt8) {  // one int8 tile per block into the upper 8 KB, widened in place below
+                if ((warp & 1) == 0) tma_load_3d(sm.k[i][1], &k_map, &sm.bar, 0, h, tok);
+                else tma_load_3d(sm.v[i][1], &v_map, &sm.bar, 0, h, tok);
+            } else if ((warp & 1) == 0) {
+                tma_load_3d(sm.k[i][0], &k_map, &sm.bar, 0, h, tok);
+                tma_load_3d(sm.k[i][1], &k_map, &sm.bar, 64, h, tok);
+            } else {
+                tma_load_3d(sm.v[i][0], &v_map, &sm.bar, 0, h, tok);
+                tma_load_3d(sm.v[i][1], &v_map, &sm.bar, 64, h, tok);
+            }
         } else {
-            tma_load_3d(sm.v[i][0], &v_map, &sm.bar, 0, h, tok);
-            tma_load_3d(sm.v[i][1], &v_map, &sm.bar, 64, h, tok);
+            mbar_arrive(&sm.bar);
+        }
+    }
+    if constexpr (!kSelGiven) {
+        if (rank == 0 && a.sel_out != nullptr && tid < a.top_k) {  // ascending, for the caller
+            const int64_t o = (static_cast<int64_t>(r) * H + h) * a.top_k;
+            if (tid < nsel) {
+                const int v = kept(tid);
+                int pos = 0;
+                for (int u = 0; u < nsel; ++u) pos += kept(u) < v;
+                a.sel_out[o + pos] = v;
+            } else {
+                a.sel_out[o + tid] = -1;
+            }
+            if (tid == 0) a.nsel_out[static_cast<int64_t>(r) * H + h] = nsel;
         }
     }
     if constexpr (kInt8) {

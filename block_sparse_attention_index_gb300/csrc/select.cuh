@@ -66,18 +66,18 @@ __device__ __forceinline__ uint64_t cta_argmax_below(const float* pooled, int J,
     return r;
 }
 
-// Selects from pooled[0..J) (+ the local block J).  All NT threads call it;
-// pooled may point to global or shared memory (generic loads only).
-// Writes the kept blocks ascending to sel[0..top_k) (-1 padded; sel may be
-// shared or global memory, written by threads < top_k) and returns nsel.
+// Ranks pooled[0..J): returns others = min(top_k - 1, J), with sm.picked[k]
+// the block of rank k (k < others; every block 0..J-1 when others == J, in
+// order) visible to every thread.  All NT threads call it; pooled may point
+// to global or shared memory (generic loads only).
 template <int NT>
-__device__ int cta_select(const float* pooled, int J, int top_k, int* sel, SelectSmem<NT>& sm) {
+__device__ int cta_select_ranked(const float* pooled, int J, int top_k, SelectSmem<NT>& sm) {
     const int tid = threadIdx.x;
     const int others = min(top_k - 1, J);
     if (others == J) {  // every causal block is kept
-        if (tid < top_k) sel[tid] = tid <= J ? tid : -1;
+        if (tid < others) sm.picked[tid] = tid;
         __syncthreads();
-        return J + 1;
+        return others;
     }
     // 1. per-thread maxima of the ordered scores (0 below every real score's code)
     const bool in_regs = J <= kRegRounds * kChunk * NT;
@@ -212,7 +212,17 @@ __device__ int cta_select(const float* pooled, int J, int top_k, int* sel, Selec
         }
         __syncthreads();
     }
-    // 4. picked[0..others) + J, ascending (J is the largest)
+    return others;
+}
+
+// Selects from pooled[0..J) (+ the local block J): writes the kept blocks
+// ascending to sel[0..top_k) (-1 padded; sel may be shared or global memory,
+// written by threads < top_k) and returns nsel.
+template <int NT>
+__device__ int cta_select(const float* pooled, int J, int top_k, int* sel, SelectSmem<NT>& sm) {
+    const int tid = threadIdx.x;
+    const int others = cta_select_ranked<NT>(pooled, J, top_k, sm);
+    // picked[0..others) + J, ascending (J is the largest)
     if (tid <= others) {
         int v = tid < others ? sm.picked[tid] : J;
         int pos = 0;
