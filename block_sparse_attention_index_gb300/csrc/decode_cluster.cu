@@ -31,15 +31,15 @@
 namespace msa {
 
 constexpr int kClThreads = 128;
-constexpr int kCluster = 8;  // CTAs per (sequence, KV head); 2 kept blocks each
+constexpr int kCluster = 8;  // CTAs per (row, KV head), 2 kept blocks each; 4 when 8 leave problems waiting
 
 struct __align__(1024) ClusterSmem {
     uint16_t k[2][2][64 * 64];  // [block][dim half][key][64 dims], 128B-swizzled by TMA
     uint16_t v[2][2][64 * 64];
     uint16_t q[16 * 128];       // [head][dim], 16-byte chunks XOR-swizzled by row
     uint16_t p[2][16 * 128];    // [hi/lo][head][128 keys], same swizzle
-    float recv_o[kCluster][2][128];  // partial outputs of my two heads, one row per source CTA
-    float recv_ml[kCluster][2][2];   // their (max in the log2 domain, sum)
+    float recv_o[16][128];  // partial outputs of my heads: row c * heads-per-CTA + slot from source CTA c
+    float recv_ml[16][2];   // their (max in the log2 domain, sum)
     float wmax[4][16];
     float wsum[4][16];
     float kvscale[2][2][64];         // int8 cache: [key/value][block][key] scales of this CTA's blocks
@@ -101,12 +101,17 @@ __device__ __forceinline__ void cluster_arrive_relaxed() {
 __device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.aligned;" ::: "memory"); }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
-// grid (kCluster, H, B), cluster (kCluster, 1, 1): CTA `rank` of the cluster of
-// (sequence b, KV head h) takes kept blocks rank and rank + kCluster.
-template <bool kSelGiven, bool kInt8>
-__global__ void __launch_bounds__(kClThreads) decode_cluster_kernel(const __grid_constant__ CUtensorMap k_map,
+// grid (kCl, H, rows), cluster (kCl, 1, 1): CTA `rank` of the cluster of (row, KV head h) takes
+// kept blocks rank + kCl * i, two per round (kCl = 8: one round; kCl = 4: two rounds through the
+// same tiles, the softmax carried over with a running max), and finishes heads kHpc * rank ...
+template <bool kSelGiven, bool kInt8, int kCl>
+__global__ void __launch_bounds__(kClThreads, 2) decode_cluster_kernel(const __grid_constant__ CUtensorMap k_map,
                                                                     const __grid_constant__ CUtensorMap v_map,
                                                                     const DecodeAttendArgs a) {
+    static_assert(kCl == 8 || kCl == 4, "clusters of 8 or 4 CTAs");
+    constexpr int kBlk = kMaxTopK / kCl;  // kept blocks per CTA
+    constexpr int kRounds = kBlk / 2;     // two blocks (64 KB of K and V) per round
+    constexpr int kHpc = 16 / kCl;        // heads each CTA combines
     extern __shared__ uint8_t smem_raw[];
     ClusterSmem& sm = *reinterpret_cast<ClusterSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int rank = static_cast<int>(cluster_rank());
@@ -177,13 +182,15 @@ __global__ void __launch_bounds__(kClThreads) decode_cluster_kernel(const __grid
     if (nsel_given < 1 || nsel_given > a.top_k) {
         if (tid == 0 && rank == 0) atomicOr(a.err, kErrBadMetadata);
         if (nsel_given < 1) {  // no kept block: the softmax is empty; the outputs are zeros
-            const int g = 2 * rank + (tid >> 6), d = (tid & 63) * 2;  // CTA `rank` owns heads 2 rank, 2 rank + 1
-            if (g < G) {
-                const int64_t oi = (static_cast<int64_t>(r) * H * G + static_cast<int64_t>(h) * G + g) * kHeadDim + d;
-                if (a.out_bf16)
-                    *reinterpret_cast<uint32_t*>(reinterpret_cast<__nv_bfloat16*>(a.out) + oi) = pack_bf16x2(0.f, 0.f);
-                else
-                    *reinterpret_cast<float2*>(reinterpret_cast<float*>(a.out) + oi) = make_float2(0.f, 0.f);
+            for (int t = tid; t < kHpc * kHeadDim / 2; t += kClThreads) {  // CTA `rank` owns heads kHpc * rank ...
+                const int g = kHpc * rank + t / (kHeadDim / 2), d = (t % (kHeadDim / 2)) * 2;
+                if (g < G) {
+                    const int64_t oi = (static_cast<int64_t>(r) * H * G + static_cast<int64_t>(h) * G + g) * kHeadDim + d;
+                    if (a.out_bf16)
+                        *reinterpret_cast<uint32_t*>(reinterpret_cast<__nv_bfloat16*>(a.out) + oi) = pack_bf16x2(0.f, 0.f);
+                    else
+                        *reinterpret_cast<float2*>(reinterpret_cast<float*>(a.out) + oi) = make_float2(0.f, 0.f);
+                }
             }
             return;  // every CTA of the cluster takes this branch, before any cluster barrier
         }
@@ -191,7 +198,7 @@ __global__ void __launch_bounds__(kClThreads) decode_cluster_kernel(const __grid
     cluster_arrive_relaxed();  // matched by cluster_wait() before the first remote store
     const int p = L - nrows + row_in_seq;  // this row's position
     const int J = p / kBlock;
-    // ---- the kept blocks: k < nsel, block kept(k); this CTA takes k = rank and rank + kCluster
+    // ---- the kept blocks: k < nsel, block kept(k); this CTA takes k = rank + kCl * i, two a round
     int nsel, others = 0;
     if constexpr (kSelGiven) {
         __syncthreads();  // the given list (read before the wait) visible to every thread
@@ -205,46 +212,66 @@ __global__ void __launch_bounds__(kClThreads) decode_cluster_kernel(const __grid
         nsel = others + 1;
     }
     auto kept = [&](int k) { return kSelGiven ? sm.sel[k] : (k < others ? sm.select.picked[k] : J); };
-    int nmy = (rank < nsel) + (rank + kCluster < nsel);
-    int blk[2] = {J, J};
-    for (int i = 0; i < nmy; ++i) {
-        blk[i] = kept(rank + i * kCluster);
-        if (blk[i] < 0 || blk[i] > J) {  // a given selection outside the causal range
-            if (tid == 0) atomicOr(a.err, kErrBadMetadata);
-            blk[i] = J;
+    int nmy = 0;
+    int blk[kBlk];
+#pragma unroll
+    for (int i = 0; i < kBlk; ++i) {
+        blk[i] = J;
+        if (rank + kCl * i < nsel) {
+            ++nmy;
+            blk[i] = kept(rank + kCl * i);
+            if (blk[i] < 0 || blk[i] > J) {  // a given selection outside the causal range
+                if (tid == 0) atomicOr(a.err, kErrBadMetadata);
+                blk[i] = J;
+            }
         }
     }
-    // Warp w issues the copies of block w / 2, K (w even) or V (w odd), each arming the barrier
-    // with its own bytes first (warps without a block arrive without bytes): one thread issues TMA
-    // boxes at a bounded rate, so four issuers land the 64 KB sooner than one.
-    if (lane == 0 && warp < 4) {
-        if (warp < 2 * nmy) {
-            const int i = warp >> 1;
-            const int bi = i == 0 ? blk[0] : blk[1];  // no dynamic index into blk: it stays in registers
-            int64_t row = block_row(a.cache, b, static_cast<int64_t>(bi) * kBlock);
-            if (row < 0) {  // page outside the pool
-                atomicOr(a.err, kErrBadMetadata);
-                row = 0;
-            }
-            const int tok = static_cast<int>(row);
-            // bytes per half block: K or V, bf16 (two 64-dim boxes) or int8 (one 128-dim box)
-            mbar_arrive_expect_tx(&sm.bar, (kInt8 ? 1 : 2) * 64 * 64 * 2);
-            if constexpr (kInt8) {  // one int8 tile per block into the upper 8 KB, widened in place below
-                if ((warp & 1) == 0) tma_load_3d(sm.k[i][1], &k_map, &sm.bar, 0, h, tok);
-                else tma_load_3d(sm.v[i][1], &v_map, &sm.bar, 0, h, tok);
-            } else if ((warp & 1) == 0) {
-                tma_load_3d(sm.k[i][0], &k_map, &sm.bar, 0, h, tok);
-                tma_load_3d(sm.k[i][1], &k_map, &sm.bar, 64, h, tok);
+
+    const int grp = lane >> 2, tig = lane & 3;
+    const int my_blk = warp >> 1, key0 = (warp & 1) * 32;  // the warp's block in a round, first key in it
+    // running softmax state of heads grp and grp + 8 over this CTA's rounds (the same in every
+    // warp): max (log2 domain) and sum; O[heads, 32w .. 32w+32) in the MMA accumulators
+    float mrun[2] = {-INFINITY, -INFINITY}, lrun[2] = {0.f, 0.f};
+    float o[4][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+    int late_phase = -1;  // a copy that did not land in time: its phase, waited for again at the end
+#pragma unroll
+    for (int rd = 0; rd < kRounds; ++rd) {
+        const int nr = min(max(nmy - 2 * rd, 0), 2);  // this round's blocks (uniform over the CTA)
+        const int bA = blk[2 * rd], bB = blk[2 * rd + 1];
+        if (rd > 0) __syncthreads();  // the tiles, P and the row statistics of the last round are read
+        // Warp w issues the copies of the round's block w / 2, K (w even) or V (w odd), each arming
+        // the barrier with its own bytes first (warps without a block arrive without bytes): one
+        // thread issues TMA boxes at a bounded rate, so four issuers land the 64 KB sooner than one.
+        if (lane == 0 && warp < 4) {
+            if (warp < 2 * nr) {
+                const int i = warp >> 1;
+                const int bi = i == 0 ? bA : bB;  // no dynamic index into blk: it stays in registers
+                int64_t row = block_row(a.cache, b, static_cast<int64_t>(bi) * kBlock);
+                if (row < 0) {  // page outside the pool
+                    atomicOr(a.err, kErrBadMetadata);
+                    row = 0;
+                }
+                const int tok = static_cast<int>(row);
+                // bytes per half block: K or V, bf16 (two 64-dim boxes) or int8 (one 128-dim box)
+                mbar_arrive_expect_tx(&sm.bar, (kInt8 ? 1 : 2) * 64 * 64 * 2);
+                if constexpr (kInt8) {  // one int8 tile per block into the upper 8 KB, widened in place below
+                    if ((warp & 1) == 0) tma_load_3d(sm.k[i][1], &k_map, &sm.bar, 0, h, tok);
+                    else tma_load_3d(sm.v[i][1], &v_map, &sm.bar, 0, h, tok);
+                } else if ((warp & 1) == 0) {
+                    tma_load_3d(sm.k[i][0], &k_map, &sm.bar, 0, h, tok);
+                    tma_load_3d(sm.k[i][1], &k_map, &sm.bar, 64, h, tok);
+                } else {
+                    tma_load_3d(sm.v[i][0], &v_map, &sm.bar, 0, h, tok);
+                    tma_load_3d(sm.v[i][1], &v_map, &sm.bar, 64, h, tok);
+                }
             } else {
-                tma_load_3d(sm.v[i][0], &v_map, &sm.bar, 0, h, tok);
-                tma_load_3d(sm.v[i][1], &v_map, &sm.bar, 64, h, tok);
+                mbar_arrive(&sm.bar);
             }
-        } else {
-            mbar_arrive(&sm.bar);
         }
-    }
-    if constexpr (!kSelGiven) {
-        if (rank == 0 && a.sel_out != nullptr && tid < a.top_k) {  // ascending, for the caller
+        if (!kSelGiven && rd == 0 && rank == 0 && a.sel_out != nullptr && tid < a.top_k) {
+            // the kept blocks ascending, for the caller, while the first copies are in flight
             const int64_t o = (static_cast<int64_t>(r) * H + h) * a.top_k;
             if (tid < nsel) {
                 const int v = kept(tid);
@@ -256,16 +283,14 @@ __global__ void __launch_bounds__(kClThreads) decode_cluster_kernel(const __grid
             }
             if (tid == 0) a.nsel_out[static_cast<int64_t>(r) * H + h] = nsel;
         }
-    }
-    if constexpr (kInt8) {
-        // scales of this CTA's keys (thread = block tid / 64, key tid % 64); keys past p are
-        // masked and may lie past the sequence's cache rows, so they are not read (scale 0,
-        // as for a block this CTA does not have)
-        {
+        if constexpr (kInt8) {
+            // scales of the round's keys (thread = block tid / 64, key tid % 64); keys past p are
+            // masked and may lie past the sequence's cache rows, so they are not read (scale 0,
+            // as for a block this CTA does not have)
             const int i = tid >> 6, key = tid & 63;
-            const int bi = i == 0 ? blk[0] : blk[1];
+            const int bi = i == 0 ? bA : bB;
             float ks = 0.f, vs = 0.f;
-            if (i < nmy && bi * kBlock + key <= p) {
+            if (i < nr && bi * kBlock + key <= p) {
                 const int64_t row = block_row(a.cache, b, static_cast<int64_t>(bi) * kBlock);
                 if (row >= 0) {
                     const int64_t si = (row + key) * H + h;
@@ -276,214 +301,286 @@ __global__ void __launch_bounds__(kClThreads) decode_cluster_kernel(const __grid
             sm.kvscale[0][i][key] = ks;
             sm.kvscale[1][i][key] = vs;
         }
-    }
-    bool kv_in_flight = false;  // a copy that did not land in time: waited for again before the CTA ends
-    if (nmy > 0 && !__syncthreads_and(mbar_wait(&sm.bar, 0, a.err))) {
-        nmy = 0;  // copy never landed: no keys
-        kv_in_flight = true;
-    }
-    if constexpr (kInt8) {
-        // every thread widens whole key rows (K rows then V rows of this CTA's blocks)
-        for (int rr = tid; rr < nmy * 2 * 64; rr += kClThreads) {
-            const bool is_v = rr >= nmy * 64;
-            const int r2 = is_v ? rr - nmy * 64 : rr;
-            convert_i8_row(reinterpret_cast<uint8_t*>(is_v ? sm.v[r2 >> 6][0] : sm.k[r2 >> 6][0]), r2 & 63);
+        if (nr == 0) break;  // no block left for this CTA (uniform)
+        if (!__syncthreads_and(mbar_wait(&sm.bar, rd & 1, a.err))) {
+            late_phase = rd & 1;  // copy never landed: no more keys
+            break;
         }
-        __syncthreads();  // bf16 tiles and scales visible to every warp
-    }
+        if constexpr (kInt8) {
+            // every thread widens whole key rows (K rows then V rows of the round's blocks)
+            for (int rr = tid; rr < nr * 2 * 64; rr += kClThreads) {
+                const bool is_v = rr >= nr * 64;
+                const int r2 = is_v ? rr - nr * 64 : rr;
+                convert_i8_row(reinterpret_cast<uint8_t*>(is_v ? sm.v[r2 >> 6][0] : sm.k[r2 >> 6][0]), r2 & 63);
+            }
+            __syncthreads();  // bf16 tiles and scales visible to every warp
+        }
 
+        // ---- S = Q K^T: warp w owns keys [32w, 32w+32) of the round's 128 (block w/2)
+        const bool warp_live = my_blk < nr;
+        const int wblk = my_blk == 0 ? bA : bB;
+        float s[4][4];
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+        if (warp_live) {
+            const uint32_t q_base = smem_u32(sm.q);
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {  // 16 dims per step
+                const int mi = lane >> 3;
+                uint32_t a0, a1, a2, a3;
+                cl_ldsm_x4(q_base + cl_swz((mi & 1) * 8 + (lane & 7), kk * 2 + (mi >> 1), 256), a0, a1, a2, a3);
+                const int dim = kk * 16 + (mi & 1) * 8;
+                const uint32_t kb = smem_u32(sm.k[my_blk][dim >> 6]);
+#pragma unroll
+                for (int pp = 0; pp < 2; ++pp) {  // two 8-key tiles per ldmatrix
+                    const int key = key0 + pp * 16 + (mi >> 1) * 8 + (lane & 7);
+                    uint32_t b0, b1, b2, b3;
+                    cl_ldsm_x4(kb + cl_swz(key, (dim & 63) >> 3, 128), b0, b1, b2, b3);
+                    cl_mma(s[pp * 2 + 0], a0, a1, a2, a3, b0, b1);
+                    cl_mma(s[pp * 2 + 1], a0, a1, a2, a3, b2, b3);
+                }
+            }
+        }
+        // scale (log2 domain; times the key's scale for an int8 cache), causal mask inside the
+        // local block, row maxima
+        float rmax[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int key = key0 + nt * 8 + tig * 2 + (e & 1);
+                const bool valid = warp_live && wblk * kBlock + key <= p;
+                const float f = kInt8 ? a.scale_log2 * sm.kvscale[0][my_blk][key] : a.scale_log2;
+                s[nt][e] = valid ? s[nt][e] * f : -INFINITY;
+                rmax[e >> 1] = fmaxf(rmax[e >> 1], s[nt][e]);
+            }
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            rmax[i] = fmaxf(rmax[i], __shfl_xor_sync(0xffffffffu, rmax[i], 1));
+            rmax[i] = fmaxf(rmax[i], __shfl_xor_sync(0xffffffffu, rmax[i], 2));
+        }
+        if (tig == 0) {
+            sm.wmax[warp][grp] = rmax[0];
+            sm.wmax[warp][grp + 8] = rmax[1];
+        }
+        __syncthreads();
+        // new running maxima; the old sums and outputs are rescaled to them
+        float mnew[2], alpha[2], lsum[2] = {0.f, 0.f};
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const int hg = grp + 8 * i;
+            const float mr = fmaxf(fmaxf(sm.wmax[0][hg], sm.wmax[1][hg]), fmaxf(sm.wmax[2][hg], sm.wmax[3][hg]));
+            if constexpr (kRounds > 1) {
+                mnew[i] = fmaxf(mrun[i], mr);
+                alpha[i] = mrun[i] == -INFINITY ? 0.f : exp2f(mrun[i] - mnew[i]);
+            } else {  // one round: nothing to carry over
+                mnew[i] = mr;
+                alpha[i] = 0.f;
+            }
+        }
+        // a row with no valid key so far gets P = 0
+        const float msafe[2] = {mnew[0] == -INFINITY ? 0.f : mnew[0], mnew[1] == -INFINITY ? 0.f : mnew[1]};
+        uint8_t* phi = reinterpret_cast<uint8_t*>(sm.p[0]);
+        uint8_t* plo = reinterpret_cast<uint8_t*>(sm.p[1]);
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt) {
+            const float p0 = exp2f(s[nt][0] - msafe[0]), p1 = exp2f(s[nt][1] - msafe[0]);
+            const float p2 = exp2f(s[nt][2] - msafe[1]), p3 = exp2f(s[nt][3] - msafe[1]);
+            lsum[0] += p0 + p1;
+            lsum[1] += p2 + p3;
+            const int key = warp * 32 + nt * 8 + tig * 2;  // key index among the round's 128
+            // int8 cache: the value scale of each key folds into its weight (the sum keeps the weight)
+            const float vs0 = kInt8 ? sm.kvscale[1][key >> 6][key & 63] : 1.f;
+            const float vs1 = kInt8 ? sm.kvscale[1][key >> 6][(key + 1) & 63] : 1.f;
+            const float w0 = p0 * vs0, w1 = p1 * vs1, w2 = p2 * vs0, w3 = p3 * vs1;
+            const int chunk = key >> 3, within = (key & 7) * 2;
+            const uint32_t h01 = pack_bf16x2(w0, w1), h23 = pack_bf16x2(w2, w3);
+            *reinterpret_cast<uint32_t*>(phi + cl_swz(grp, chunk, 256) + within) = h01;
+            *reinterpret_cast<uint32_t*>(phi + cl_swz(grp + 8, chunk, 256) + within) = h23;
+            *reinterpret_cast<uint32_t*>(plo + cl_swz(grp, chunk, 256) + within) =
+                pack_bf16x2(w0 - bf16_lo(h01), w1 - bf16_hi(h01));
+            *reinterpret_cast<uint32_t*>(plo + cl_swz(grp + 8, chunk, 256) + within) =
+                pack_bf16x2(w2 - bf16_lo(h23), w3 - bf16_hi(h23));
+        }
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            lsum[i] += __shfl_xor_sync(0xffffffffu, lsum[i], 1);
+            lsum[i] += __shfl_xor_sync(0xffffffffu, lsum[i], 2);
+        }
+        if (tig == 0) {
+            sm.wsum[warp][grp] = lsum[0];
+            sm.wsum[warp][grp + 8] = lsum[1];
+        }
+        __syncthreads();
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const int hg = grp + 8 * i;
+            const float lr = sm.wsum[0][hg] + sm.wsum[1][hg] + sm.wsum[2][hg] + sm.wsum[3][hg];
+            lrun[i] = kRounds > 1 ? lrun[i] * alpha[i] + lr : lr;
+            mrun[i] = mnew[i];
+        }
+        if constexpr (kRounds > 1) {
+#pragma unroll
+            for (int nt = 0; nt < 4; ++nt) {  // accumulator rows grp (c0, c1) and grp + 8 (c2, c3)
+                o[nt][0] *= alpha[0];
+                o[nt][1] *= alpha[0];
+                o[nt][2] *= alpha[1];
+                o[nt][3] *= alpha[1];
+            }
+        }
 
-    // ---- S = Q K^T: warp w owns keys [32w, 32w+32) of this CTA's 128 (block w/2)
-    const int grp = lane >> 2, tig = lane & 3;
-    const int my_blk = warp >> 1, key0 = (warp & 1) * 32;  // key0: first key of the warp inside its block
-    const bool warp_live = my_blk < nmy;
-    const int wblk = my_blk == 0 ? blk[0] : blk[1];
-    float s[4][4];
-#pragma unroll
-    for (int nt = 0; nt < 4; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
-    if (warp_live) {
-        const uint32_t q_base = smem_u32(sm.q);
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {  // 16 dims per step
+        // ---- O[:, 32w .. 32w+32) += P V over the round's 64 * nr keys
+        for (int kk = 0; kk < 4 * nr; ++kk) {  // 16 keys per step
             const int mi = lane >> 3;
-            uint32_t a0, a1, a2, a3;
-            cl_ldsm_x4(q_base + cl_swz((mi & 1) * 8 + (lane & 7), kk * 2 + (mi >> 1), 256), a0, a1, a2, a3);
-            const int dim = kk * 16 + (mi & 1) * 8;
-            const uint32_t kb = smem_u32(sm.k[my_blk][dim >> 6]);
+            const int row = (mi & 1) * 8 + (lane & 7);
+            uint32_t a0, a1, a2, a3, l0, l1, l2, l3;
+            cl_ldsm_x4(smem_u32(sm.p[0]) + cl_swz(row, kk * 2 + (mi >> 1), 256), a0, a1, a2, a3);
+            cl_ldsm_x4(smem_u32(sm.p[1]) + cl_swz(row, kk * 2 + (mi >> 1), 256), l0, l1, l2, l3);
+            const int vb = kk >> 2;  // block of these keys
 #pragma unroll
-            for (int pp = 0; pp < 2; ++pp) {  // two 8-key tiles per ldmatrix
-                const int key = key0 + pp * 16 + (mi >> 1) * 8 + (lane & 7);
+            for (int np = 0; np < 2; ++np) {  // pairs of 8-dim tiles
+                const int key = (kk & 3) * 16 + (mi & 1) * 8 + (lane & 7);
+                const int dim = warp * 32 + np * 16 + (mi >> 1) * 8;
                 uint32_t b0, b1, b2, b3;
-                cl_ldsm_x4(kb + cl_swz(key, (dim & 63) >> 3, 128), b0, b1, b2, b3);
-                cl_mma(s[pp * 2 + 0], a0, a1, a2, a3, b0, b1);
-                cl_mma(s[pp * 2 + 1], a0, a1, a2, a3, b2, b3);
+                cl_ldsm_x4_t(smem_u32(sm.v[vb][dim >> 6]) + cl_swz(key, (dim & 63) >> 3, 128), b0, b1, b2, b3);
+                cl_mma(o[np * 2 + 0], a0, a1, a2, a3, b0, b1);
+                cl_mma(o[np * 2 + 1], a0, a1, a2, a3, b2, b3);
+                cl_mma(o[np * 2 + 0], l0, l1, l2, l3, b0, b1);
+                cl_mma(o[np * 2 + 1], l0, l1, l2, l3, b2, b3);
             }
         }
     }
-    // scale (log2 domain; times the key's scale for an int8 cache), causal mask inside the
-    // local block, row maxima
-    float rmax[2] = {-INFINITY, -INFINITY};
-#pragma unroll
-    for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const int key = key0 + nt * 8 + tig * 2 + (e & 1);
-            const bool valid = warp_live && wblk * kBlock + key <= p;
-            const float f = kInt8 ? a.scale_log2 * sm.kvscale[0][my_blk][key] : a.scale_log2;
-            s[nt][e] = valid ? s[nt][e] * f : -INFINITY;
-            rmax[e >> 1] = fmaxf(rmax[e >> 1], s[nt][e]);
-        }
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-        rmax[i] = fmaxf(rmax[i], __shfl_xor_sync(0xffffffffu, rmax[i], 1));
-        rmax[i] = fmaxf(rmax[i], __shfl_xor_sync(0xffffffffu, rmax[i], 2));
-    }
-    if (tig == 0) {
-        sm.wmax[warp][grp] = rmax[0];
-        sm.wmax[warp][grp + 8] = rmax[1];
-    }
-    __syncthreads();
-    float m[2], lsum[2] = {0.f, 0.f};
-    m[0] = fmaxf(fmaxf(sm.wmax[0][grp], sm.wmax[1][grp]), fmaxf(sm.wmax[2][grp], sm.wmax[3][grp]));
-    m[1] = fmaxf(fmaxf(sm.wmax[0][grp + 8], sm.wmax[1][grp + 8]), fmaxf(sm.wmax[2][grp + 8], sm.wmax[3][grp + 8]));
-    // a row with no valid key in this CTA (nmy == 0) gets P = 0
-    const float msafe[2] = {m[0] == -INFINITY ? 0.f : m[0], m[1] == -INFINITY ? 0.f : m[1]};
-    uint8_t* phi = reinterpret_cast<uint8_t*>(sm.p[0]);
-    uint8_t* plo = reinterpret_cast<uint8_t*>(sm.p[1]);
-#pragma unroll
-    for (int nt = 0; nt < 4; ++nt) {
-        const float p0 = exp2f(s[nt][0] - msafe[0]), p1 = exp2f(s[nt][1] - msafe[0]);
-        const float p2 = exp2f(s[nt][2] - msafe[1]), p3 = exp2f(s[nt][3] - msafe[1]);
-        lsum[0] += p0 + p1;
-        lsum[1] += p2 + p3;
-        const int key = warp * 32 + nt * 8 + tig * 2;  // key index among this CTA's 128
-        // int8 cache: the value scale of each key folds into its weight (the sum keeps the weight)
-        const float vs0 = kInt8 ? sm.kvscale[1][key >> 6][key & 63] : 1.f;
-        const float vs1 = kInt8 ? sm.kvscale[1][key >> 6][(key + 1) & 63] : 1.f;
-        const float w0 = p0 * vs0, w1 = p1 * vs1, w2 = p2 * vs0, w3 = p3 * vs1;
-        const int chunk = key >> 3, within = (key & 7) * 2;
-        const uint32_t h01 = pack_bf16x2(w0, w1), h23 = pack_bf16x2(w2, w3);
-        *reinterpret_cast<uint32_t*>(phi + cl_swz(grp, chunk, 256) + within) = h01;
-        *reinterpret_cast<uint32_t*>(phi + cl_swz(grp + 8, chunk, 256) + within) = h23;
-        *reinterpret_cast<uint32_t*>(plo + cl_swz(grp, chunk, 256) + within) =
-            pack_bf16x2(w0 - bf16_lo(h01), w1 - bf16_hi(h01));
-        *reinterpret_cast<uint32_t*>(plo + cl_swz(grp + 8, chunk, 256) + within) =
-            pack_bf16x2(w2 - bf16_lo(h23), w3 - bf16_hi(h23));
-    }
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-        lsum[i] += __shfl_xor_sync(0xffffffffu, lsum[i], 1);
-        lsum[i] += __shfl_xor_sync(0xffffffffu, lsum[i], 2);
-    }
-    if (tig == 0) {
-        sm.wsum[warp][grp] = lsum[0];
-        sm.wsum[warp][grp + 8] = lsum[1];
-    }
-    __syncthreads();
-
-    // ---- O[:, 32w .. 32w+32) = P V over this CTA's 64 * nmy keys
-    float o[4][4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-    for (int kk = 0; kk < 4 * nmy; ++kk) {  // 16 keys per step
-        const int mi = lane >> 3;
-        const int row = (mi & 1) * 8 + (lane & 7);
-        uint32_t a0, a1, a2, a3, l0, l1, l2, l3;
-        cl_ldsm_x4(smem_u32(sm.p[0]) + cl_swz(row, kk * 2 + (mi >> 1), 256), a0, a1, a2, a3);
-        cl_ldsm_x4(smem_u32(sm.p[1]) + cl_swz(row, kk * 2 + (mi >> 1), 256), l0, l1, l2, l3);
-        const int vb = kk >> 2;  // block of these keys
-#pragma unroll
-        for (int np = 0; np < 2; ++np) {  // pairs of 8-dim tiles
-            const int key = (kk & 3) * 16 + (mi & 1) * 8 + (lane & 7);
-            const int dim = warp * 32 + np * 16 + (mi >> 1) * 8;
-            uint32_t b0, b1, b2, b3;
-            cl_ldsm_x4_t(smem_u32(sm.v[vb][dim >> 6]) + cl_swz(key, (dim & 63) >> 3, 128), b0, b1, b2, b3);
-            cl_mma(o[np * 2 + 0], a0, a1, a2, a3, b0, b1);
-            cl_mma(o[np * 2 + 1], a0, a1, a2, a3, b2, b3);
-            cl_mma(o[np * 2 + 0], l0, l1, l2, l3, b0, b1);
-            cl_mma(o[np * 2 + 1], l0, l1, l2, l3, b2, b3);
-        }
-    }
-    // ---- push my partial rows to their owners: head g is finished by CTA g / 2
+    // ---- push my partial rows to their owners: head g is finished by CTA g / kHpc
     cluster_wait();
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
         const int g = grp + 8 * half;
         if (g < G) {
-            const int owner = g >> 1, slot = g & 1;
+            const int owner = g / kHpc, slot = g % kHpc;
 #pragma unroll
             for (int nt = 0; nt < 4; ++nt) {
                 const int dim = warp * 32 + nt * 8 + tig * 2;
-                st_cluster_f32x2(map_to_rank(&sm.recv_o[rank][slot][dim], owner), o[nt][2 * half], o[nt][2 * half + 1]);
+                st_cluster_f32x2(map_to_rank(&sm.recv_o[rank * kHpc + slot][dim], owner), o[nt][2 * half],
+                                 o[nt][2 * half + 1]);
             }
+            if (warp == 0 && tig == 0)  // the (max, sum) of head g, the same in every warp
+                st_cluster_f32x2(map_to_rank(&sm.recv_ml[rank * kHpc + slot][0], owner), mrun[half], lrun[half]);
         }
-    }
-    if (tid < G) {
-        const float mg = fmaxf(fmaxf(sm.wmax[0][tid], sm.wmax[1][tid]), fmaxf(sm.wmax[2][tid], sm.wmax[3][tid]));
-        const float lg = sm.wsum[0][tid] + sm.wsum[1][tid] + sm.wsum[2][tid] + sm.wsum[3][tid];
-        st_cluster_f32x2(map_to_rank(&sm.recv_ml[rank][tid & 1][0], tid >> 1), mg, lg);
     }
     cluster_sync();  // all pushes have landed; no remote access follows
 
-    // ---- combine my heads 2*rank and 2*rank + 1; thread t owns two dims of one
-    const int slot = tid >> 6;
-    const int g = 2 * rank + slot;
-    const int d = (tid & 63) * 2;
+    // ---- combine my heads kHpc * rank .. + kHpc - 1; thread t owns kHpc dims of one
+    constexpr int kTpHead = kClThreads / kHpc;  // threads per head
+    const int slot = tid / kTpHead;
+    const int g = kHpc * rank + slot;
+    const int d = (tid % kTpHead) * kHpc;
     if (g < G) {
         float M = -INFINITY;
 #pragma unroll
-        for (int c = 0; c < kCluster; ++c) M = fmaxf(M, sm.recv_ml[c][slot][0]);
-        float Ls = 0.f, ox = 0.f, oy = 0.f;
+        for (int c = 0; c < kCl; ++c) M = fmaxf(M, sm.recv_ml[c * kHpc + slot][0]);
+        float Ls = 0.f, ov[kHpc];
 #pragma unroll
-        for (int c = 0; c < kCluster; ++c) {
-            const float mc = sm.recv_ml[c][slot][0];
+        for (int j = 0; j < kHpc; ++j) ov[j] = 0.f;
+#pragma unroll
+        for (int c = 0; c < kCl; ++c) {
+            const float mc = sm.recv_ml[c * kHpc + slot][0];
             const float w = mc == -INFINITY ? 0.f : exp2f(mc - M);
-            const float2 oc = *reinterpret_cast<const float2*>(&sm.recv_o[c][slot][d]);
-            Ls = fmaf(w, sm.recv_ml[c][slot][1], Ls);
-            ox = fmaf(w, oc.x, ox);
-            oy = fmaf(w, oc.y, oy);
+            Ls = fmaf(w, sm.recv_ml[c * kHpc + slot][1], Ls);
+#pragma unroll
+            for (int j = 0; j < kHpc; j += 2) {  // two dims per load
+                const float2 oc = *reinterpret_cast<const float2*>(&sm.recv_o[c * kHpc + slot][d + j]);
+                ov[j] = fmaf(w, oc.x, ov[j]);
+                ov[j + 1] = fmaf(w, oc.y, ov[j + 1]);
+            }
         }
         const float inv = 1.f / Ls;
         const int64_t oi = (static_cast<int64_t>(r) * H * G + static_cast<int64_t>(h) * G + g) * kHeadDim + d;
-        if (a.out_bf16)
-            *reinterpret_cast<uint32_t*>(reinterpret_cast<__nv_bfloat16*>(a.out) + oi) = pack_bf16x2(ox * inv, oy * inv);
-        else
-            *reinterpret_cast<float2*>(reinterpret_cast<float*>(a.out) + oi) = make_float2(ox * inv, oy * inv);
+#pragma unroll
+        for (int j = 0; j < kHpc; j += 2) {
+            if (a.out_bf16)
+                *reinterpret_cast<uint32_t*>(reinterpret_cast<__nv_bfloat16*>(a.out) + oi + j) =
+                    pack_bf16x2(ov[j] * inv, ov[j + 1] * inv);
+            else
+                *reinterpret_cast<float2*>(reinterpret_cast<float*>(a.out) + oi + j) =
+                    make_float2(ov[j] * inv, ov[j + 1] * inv);
+        }
     }
-    if (kv_in_flight && tid == 0) mbar_wait(&sm.bar, 0, nullptr);
+    if (late_phase >= 0 && tid == 0) mbar_wait(&sm.bar, late_phase, nullptr);
 }
 
-cudaError_t run_decode_cluster(const DecodeAttendArgs& a, bool after_scan, cudaStream_t stream) {
+template <bool kSelGiven, bool kInt8, int kCl>
+static cudaError_t launch_cluster(const DecodeAttendArgs& a, int rows, bool after_scan, cudaStream_t stream) {
     const size_t smem = sizeof(ClusterSmem) + 1024;
-    const bool given = a.pooled == nullptr;
-    const void* fn = a.kv_int8 ? (given ? reinterpret_cast<const void*>(decode_cluster_kernel<true, true>)
-                                        : reinterpret_cast<const void*>(decode_cluster_kernel<false, true>))
-                               : (given ? reinterpret_cast<const void*>(decode_cluster_kernel<true, false>)
-                                        : reinterpret_cast<const void*>(decode_cluster_kernel<false, false>));
-    cudaError_t e = ensure_smem_limit(fn, smem);
+    cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(decode_cluster_kernel<kSelGiven, kInt8, kCl>), smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(kCluster, a.H, a.drow_prefix != nullptr ? a.decode_rows : a.num_seqs * a.rows_per_seq);
+    cfg.gridDim = dim3(kCl, a.H, rows);
     cfg.blockDim = dim3(kClThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = kCluster;
+    attr[0].val.clusterDim.x = kCl;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = after_scan ? 2 : 1;  // overlap the prologue with the index scan's tail
-    if (a.kv_int8)
-        e = given ? cudaLaunchKernelEx(&cfg, decode_cluster_kernel<true, true>, *a.k_map, *a.v_map, a)
-                  : cudaLaunchKernelEx(&cfg, decode_cluster_kernel<false, true>, *a.k_map, *a.v_map, a);
-    else
-        e = given ? cudaLaunchKernelEx(&cfg, decode_cluster_kernel<true, false>, *a.k_map, *a.v_map, a)
-                  : cudaLaunchKernelEx(&cfg, decode_cluster_kernel<false, false>, *a.k_map, *a.v_map, a);
+    e = cudaLaunchKernelEx(&cfg, decode_cluster_kernel<kSelGiven, kInt8, kCl>, *a.k_map, *a.v_map, a);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
+}
+
+// Clusters of 8 CTAs of this kernel that the current device runs at once (queried once per
+// device; 0 if the query fails).
+static int clusters_of_8_at_once() {
+    static int counts[64] = {0};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    int& c = counts[dev & 63];
+    if (c == 0) {
+        const size_t smem = sizeof(ClusterSmem) + 1024;
+        if (ensure_smem_limit(reinterpret_cast<const void*>(decode_cluster_kernel<false, false, 8>), smem) != cudaSuccess)
+            return 0;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(8, 1, 1);
+        cfg.blockDim = dim3(kClThreads, 1, 1);
+        cfg.dynamicSmemBytes = smem;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 8;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, decode_cluster_kernel<false, false, 8>, &cfg) != cudaSuccess) {
+            cudaGetLastError();  // clear the query's error
+            return 0;
+        }
+        c = n > 0 ? n : -1;
+    }
+    return c > 0 ? c : 0;
+}
+
+cudaError_t run_decode_cluster(const DecodeAttendArgs& a, bool after_scan, cudaStream_t stream) {
+    const bool given = a.pooled == nullptr;
+    const int rows = a.drow_prefix != nullptr ? a.decode_rows : a.num_seqs * a.rows_per_seq;
+    // Clusters of 8 finish a (row, head) soonest; when there are more problems than clusters
+    // of 8 fit at once, clusters of 4 (two rounds a CTA) run them in fewer waves.
+    const int cap = clusters_of_8_at_once();
+    const bool four = cap > 0 && static_cast<int64_t>(rows) * a.H > cap;
+    if (a.kv_int8) {
+        if (given) return four ? launch_cluster<true, true, 4>(a, rows, after_scan, stream)
+                               : launch_cluster<true, true, 8>(a, rows, after_scan, stream);
+        return four ? launch_cluster<false, true, 4>(a, rows, after_scan, stream)
+                    : launch_cluster<false, true, 8>(a, rows, after_scan, stream);
+    }
+    if (given) return four ? launch_cluster<true, false, 4>(a, rows, after_scan, stream)
+                           : launch_cluster<true, false, 8>(a, rows, after_scan, stream);
+    return four ? launch_cluster<false, false, 4>(a, rows, after_scan, stream)
+                : launch_cluster<false, false, 8>(a, rows, after_scan, stream);
 }
 
 }  // namespace msa

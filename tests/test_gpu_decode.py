@@ -75,6 +75,31 @@ def test_decode_staged_stages():
     assert_out_close(out, ref["out"], torch.float32)
 
 
+BATCH40 = [70, 300, 1000, 1100, 2000, 3000, 5000, 9000, 64, 129]
+
+
+@pytest.mark.parametrize("kv", ["bf16", "int8"])
+def test_decode_clusters_of_four(kv):
+    """40 (row, KV head) problems, more than the clusters of 8 CTAs that fit
+    on the GPU at once: the attention takes clusters of 4 CTAs, each CTA two
+    rounds of two kept blocks with the softmax carried over between them
+    (short rows leave CTAs with one block or none).  Fused path, and the
+    given selection with bf16 output, against the oracle."""
+    m = msa()
+    w = synth.Workload("dec_cl4", H=4, G=16, seqs=[(1, L) for L in BATCH40], seed=41, kv_dtype=kv)
+    x = synth.make_inputs(w)
+    out, sel, nsel = run_forward(w, x)
+    ref = oracle_forward(w, x)
+    assert_selection_equal(sel, nsel, ref)
+    assert_out_close(out, ref["out"], torch.float32)
+    dx = device_inputs(x)
+    pb = problem(w, x, torch.bfloat16)
+    out_g = m.attend_decode(pb, dx["q"], dx["k"], dx["v"], torch.from_numpy(ref["sel"]).cuda(),
+                            torch.from_numpy(ref["nsel"]).cuda())
+    torch.cuda.synchronize()
+    assert_out_close(out_g, ref["out"], torch.bfloat16)
+
+
 def test_decode_attend_given_selection_any_blocks():
     """A synthetic (not top-k) selection: attention follows the given list."""
     m = msa()
