@@ -9,10 +9,16 @@
 //     stage their K and V by TMA (128-byte swizzle) and compute S = Q K^T
 //     and O = P V for the group's 16 query heads on mma.sync (P split into
 //     bf16 hi + lo parts so the weights keep ~16 significant bits);
-//   - each CTA stores the (m, l, O) rows of heads 2c and 2c+1 straight into
-//     the shared memory of CTA c of the cluster (distributed shared memory,
-//     remote stores: no round trip); after one cluster barrier CTA c
-//     combines its two heads from its own shared memory:
+//   - when a batch has more (row, head) problems than clusters of 8 fit on
+//     the GPU at once, clusters of 4 CTAs take four blocks each, in two
+//     rounds of two through the same tiles, the softmax carried from round
+//     to round with a running max (the partial O rescaled by 2^(m - m'));
+//     one wave of clusters of 4 ends sooner than two waves of clusters of 8;
+//   - each CTA stores the (m, l, O) rows of its heads' partials straight
+//     into the shared memory of the CTA that finishes them (head g: CTA
+//     g / (16 / cluster size); distributed shared memory, remote stores: no
+//     round trip); after one cluster barrier each CTA combines its heads from
+//     its own shared memory:
 //         M = max m_c,  L = sum l_c 2^(m_c - M),  out = sum O_c 2^(m_c - M) / L
 //   - the kept blocks come from the pooled index scores (every CTA runs the
 //     same deterministic selection) or from a given list;
