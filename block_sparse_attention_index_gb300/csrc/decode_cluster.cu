@@ -160,6 +160,10 @@ __global__ void __launch_bounds__(kClThreads, 2) decode_cluster_kernel(const __g
         mbar_init(&sm.bar, 4);  // one arrival from each of warps 0-3 (with the bytes it copies)
         fence_mbar_init();
     }
+    if (tid == 32) {  // the K/V descriptors ride along with the wait, not behind the selection
+        prefetch_tmap(&k_map);
+        prefetch_tmap(&v_map);
+    }
     if (meta_ok) {
         const uint16_t* qrow = a.q + (static_cast<int64_t>(r) * H * G + static_cast<int64_t>(h) * G) * kHeadDim;
         for (int c = tid; c < 16 * 16; c += kClThreads) {  // 16 heads x 16 chunks of 8 dims
