@@ -2,12 +2,16 @@
 
 Each translation unit under csrc/ is compiled by nvcc in parallel, then the
 objects are linked into block_sparse_attention_index_gb300/_lib/libmsa_gb300.so
-(CUDA runtime linked statically).  Rebuilds only what changed.
+(CUDA runtime linked statically).  Rebuilds only what changed, and everything
+when the objects were made on another machine, by another nvcc or with other
+flags (a stamp file records those).  Prints one line saying what it did.
 """
 from __future__ import annotations
 
 import glob
 import os
+import platform
+import shutil
 import subprocess
 import sys
 from concurrent.futures import ThreadPoolExecutor
@@ -45,18 +49,35 @@ def _compile(src, hdr_mtime, extra, verbose):
     return obj, (res.stdout + res.stderr) if verbose else ""
 
 
+def _stamp() -> str:
+    ver = subprocess.run([NVCC, "--version"], capture_output=True, text=True).stdout.strip().splitlines()
+    return "\n".join([platform.machine(), ver[-1] if ver else "nvcc ?", " ".join(FLAGS)]) + "\n"
+
+
 def build(verbose: bool = False, ptxas_info: bool = False) -> str:
+    stamp, stamp_file = _stamp(), os.path.join(OBJ_DIR, "stamp.txt")
+    try:
+        same = open(stamp_file).read() == stamp
+    except OSError:
+        same = False
+    if not same:  # objects (if any) from another machine, compiler or flag set: start over
+        for d in (OBJ_DIR, LIB_DIR):
+            shutil.rmtree(d, ignore_errors=True)
     os.makedirs(OBJ_DIR, exist_ok=True)
     os.makedirs(LIB_DIR, exist_ok=True)
     hdr = _headers_mtime()
     extra = ["-Xptxas", "-v"] if ptxas_info else []
     srcs = _sources()
+    stale = [s for s in srcs if not os.path.exists(os.path.join(OBJ_DIR, os.path.basename(s)[:-3] + ".o")) or
+             os.path.getmtime(os.path.join(OBJ_DIR, os.path.basename(s)[:-3] + ".o")) <
+             max(os.path.getmtime(s), hdr)]
     with ThreadPoolExecutor(max_workers=min(8, len(srcs))) as ex:
         results = list(ex.map(lambda s: _compile(s, hdr, extra, verbose or ptxas_info), srcs))
     objs = [o for o, _ in results]
     for _, log in results:
         if log:
             print(log)
+    linked = False
     if not os.path.exists(LIB) or os.path.getmtime(LIB) < max(os.path.getmtime(o) for o in objs):
         tmp = LIB + f".{os.getpid()}.tmp"
         cmd = [NVCC] + ARCH + ["-shared", "-o", tmp] + objs
@@ -64,6 +85,12 @@ def build(verbose: bool = False, ptxas_info: bool = False) -> str:
         if res.returncode != 0:
             raise RuntimeError(f"link failed:\n{res.stdout}\n{res.stderr}")
         os.replace(tmp, LIB)
+        linked = True
+    with open(stamp_file, "w") as f:
+        f.write(stamp)
+    mode = "full" if not same else ("incremental" if stale else "up to date")
+    print(f"msa build ({platform.machine()}, sm_103a): {mode}; compiled {len(stale)} of {len(srcs)} translation "
+          f"units; library {'linked' if linked else 'unchanged'}: {LIB}")
     return LIB
 
 
