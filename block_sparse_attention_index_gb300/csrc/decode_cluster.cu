@@ -37,7 +37,6 @@
 namespace msa {
 
 constexpr int kClThreads = 128;
-constexpr int kCluster = 8;  // CTAs per (row, KV head), 2 kept blocks each; 4 when 8 leave problems waiting
 
 struct __align__(1024) ClusterSmem {
     uint16_t k[2][2][64 * 64];  // [block][dim half][key][64 dims], 128B-swizzled by TMA

@@ -132,6 +132,29 @@ def test_int8_prompt_chunks(H, G, out_dtype):
     assert_out_close(out, ref["out"], out_dtype)
 
 
+def test_int8_prompt_extreme_values_and_scales():
+    """The same extremes for prompt chunks (the tcgen05 attention): value
+    scales from 2^-20 to 2^6 in the same blocks, so P (weight x value scale)
+    needs bf16's exponent range for the keys with small scales to keep their
+    share."""
+    w = _w("int8_prompt_extreme", [(300, 2000), (70, 900)], seed=87)
+    x = synth.make_inputs(w)
+    rng = np.random.default_rng(87)
+    for k in ("k", "v"):
+        a = x[k]
+        a[::3] = -128
+        a[1::5] = 127
+    x["k_scale"] = (2.0 ** rng.integers(-8, -3, size=x["k_scale"].shape)).astype(np.float32)
+    x["v_scale"] = (2.0 ** rng.integers(-20, 7, size=x["v_scale"].shape)).astype(np.float32)
+    out, sel, nsel = run_forward(w, x)
+    ref = oracle_forward(w, x)
+    assert_selection_equal(sel, nsel, ref)
+    o = out.cpu().numpy().astype(np.float64)
+    scale = np.maximum(1.0, np.abs(ref["out"]).max(axis=2, keepdims=True))
+    assert np.isfinite(o).all()
+    assert (np.abs(o - ref["out"]) / scale).max() <= 2e-3
+
+
 def test_int8_attend_prefill_given_selection():
     m = msa()
     w = _w("int8_prefill_given", [(300, 2500), (17, 700)], seed=91)
