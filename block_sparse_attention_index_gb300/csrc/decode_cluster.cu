@@ -48,7 +48,8 @@ struct __align__(1024) ClusterSmem {
     float wmax[4][16];
     float wsum[4][16];
     float kvscale[2][2][64];         // int8 cache: [key/value][block][key] scales of this CTA's blocks
-    uint64_t bar;
+    uint64_t bar_k;  // the round's K tiles landed
+    uint64_t bar_v;  // the round's V tiles landed
     int32_t sel[kMaxTopK];
     int32_t nsel;
     int32_t meta_ok;
@@ -156,7 +157,8 @@ __global__ void __launch_bounds__(kClThreads, 2) decode_cluster_kernel(const __g
     const bool meta_ok = !(r < 0 || r >= a.total_rows || L < nrows || L > a.max_cache_len || nrows > a.rows_per_seq) &&
                          seq_rows_ok(a.cache, b, L, a.cache_tokens);
     if (tid == 0) {
-        mbar_init(&sm.bar, 4);  // one arrival from each of warps 0-3 (with the bytes it copies)
+        mbar_init(&sm.bar_k, 4);  // one arrival from each of warps 0-3 (with the bytes it copies)
+        mbar_init(&sm.bar_v, 4);
         fence_mbar_init();
     }
     if (tid == 32) {  // the K/V descriptors ride along with the wait, not behind the selection
@@ -250,12 +252,15 @@ __global__ void __launch_bounds__(kClThreads, 2) decode_cluster_kernel(const __g
         const int nr = min(max(nmy - 2 * rd, 0), 2);  // this round's blocks (uniform over the CTA)
         const int bA = blk[2 * rd], bB = blk[2 * rd + 1];
         if (rd > 0) __syncthreads();  // the tiles, P and the row statistics of the last round are read
-        // Warp w issues the copies of the round's block w / 2, K (w even) or V (w odd), each arming
-        // the barrier with its own bytes first (warps without a block arrive without bytes): one
-        // thread issues TMA boxes at a bounded rate, so four issuers land the 64 KB sooner than one.
+        // Warps 0-3 issue the round's copies, K before V, each arming the two barriers with its
+        // own bytes first (warps without a copy arrive without bytes): one thread issues TMA boxes
+        // at a bounded rate, so four issuers land the 64 KB sooner than one, and with the K boxes
+        // queued first S and the softmax overlap the V transfer.  bf16: warp w copies dims
+        // 64 (w & 1) .. of block w / 2, K then V; int8 (one 128-dim box a tile): warp w copies
+        // the K (w < 2) or V tile of block w & 1.
         if (lane == 0 && warp < 4) {
-            if (warp < 2 * nr) {
-                const int i = warp >> 1;
+            const int i = kInt8 ? (warp & 1) : (warp >> 1);
+            if (i < nr) {
                 const int bi = i == 0 ? bA : bB;  // no dynamic index into blk: it stays in registers
                 int64_t row = block_row(a.cache, b, static_cast<int64_t>(bi) * kBlock);
                 if (row < 0) {  // page outside the pool
@@ -263,20 +268,26 @@ __global__ void __launch_bounds__(kClThreads, 2) decode_cluster_kernel(const __g
                     row = 0;
                 }
                 const int tok = static_cast<int>(row);
-                // bytes per half block: K or V, bf16 (two 64-dim boxes) or int8 (one 128-dim box)
-                mbar_arrive_expect_tx(&sm.bar, (kInt8 ? 1 : 2) * 64 * 64 * 2);
                 if constexpr (kInt8) {  // one int8 tile per block into the upper 8 KB, widened in place below
-                    if ((warp & 1) == 0) tma_load_3d(sm.k[i][1], &k_map, &sm.bar, 0, h, tok);
-                    else tma_load_3d(sm.v[i][1], &v_map, &sm.bar, 0, h, tok);
-                } else if ((warp & 1) == 0) {
-                    tma_load_3d(sm.k[i][0], &k_map, &sm.bar, 0, h, tok);
-                    tma_load_3d(sm.k[i][1], &k_map, &sm.bar, 64, h, tok);
+                    if (warp < 2) {
+                        mbar_arrive_expect_tx(&sm.bar_k, 64 * 128);
+                        tma_load_3d(sm.k[i][1], &k_map, &sm.bar_k, 0, h, tok);
+                        mbar_arrive(&sm.bar_v);
+                    } else {
+                        mbar_arrive(&sm.bar_k);
+                        mbar_arrive_expect_tx(&sm.bar_v, 64 * 128);
+                        tma_load_3d(sm.v[i][1], &v_map, &sm.bar_v, 0, h, tok);
+                    }
                 } else {
-                    tma_load_3d(sm.v[i][0], &v_map, &sm.bar, 0, h, tok);
-                    tma_load_3d(sm.v[i][1], &v_map, &sm.bar, 64, h, tok);
+                    const int half = warp & 1;
+                    mbar_arrive_expect_tx(&sm.bar_k, 64 * 64 * 2);
+                    mbar_arrive_expect_tx(&sm.bar_v, 64 * 64 * 2);
+                    tma_load_3d(sm.k[i][half], &k_map, &sm.bar_k, 64 * half, h, tok);
+                    tma_load_3d(sm.v[i][half], &v_map, &sm.bar_v, 64 * half, h, tok);
                 }
             } else {
-                mbar_arrive(&sm.bar);
+                mbar_arrive(&sm.bar_k);
+                mbar_arrive(&sm.bar_v);
             }
         }
         if (!kSelGiven && rd == 0 && rank == 0 && a.sel_out != nullptr && tid < a.top_k) {
@@ -311,7 +322,9 @@ __global__ void __launch_bounds__(kClThreads, 2) decode_cluster_kernel(const __g
             sm.kvscale[1][i][key] = vs;
         }
         if (nr == 0) break;  // no block left for this CTA (uniform)
-        if (!__syncthreads_and(mbar_wait(&sm.bar, rd & 1, a.err))) {
+        // the K tiles (an int8 cache: K and V, widened together below)
+        if (!__syncthreads_and(mbar_wait(&sm.bar_k, rd & 1, a.err) &&
+                               (!kInt8 || mbar_wait(&sm.bar_v, rd & 1, a.err)))) {
             late_phase = rd & 1;  // copy never landed: no more keys
             break;
         }
@@ -420,7 +433,11 @@ __global__ void __launch_bounds__(kClThreads, 2) decode_cluster_kernel(const __g
             sm.wsum[warp][grp] = lsum[0];
             sm.wsum[warp][grp + 8] = lsum[1];
         }
-        __syncthreads();
+        // P and the row sums written; a bf16 cache's V tiles landed
+        if (!__syncthreads_and(kInt8 || mbar_wait(&sm.bar_v, rd & 1, a.err))) {
+            late_phase = rd & 1;  // copy never landed: no more keys (the output is flagged)
+            break;
+        }
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
             const int hg = grp + 8 * i;
@@ -514,12 +531,21 @@ __global__ void __launch_bounds__(kClThreads, 2) decode_cluster_kernel(const __g
                     make_float2(ov[j] * inv, ov[j + 1] * inv);
         }
     }
-    if (late_phase >= 0 && tid == 0) mbar_wait(&sm.bar, late_phase, nullptr);
+    if (late_phase >= 0 && tid == 0) {  // the copies still in flight land before the CTA exits
+        mbar_wait(&sm.bar_k, late_phase, nullptr);
+        mbar_wait(&sm.bar_v, late_phase, nullptr);
+    }
 }
 
+// Shared memory a CTA asks for: what it uses, or (one CTA per SM) more than half of an SM's
+// 228 KB, so that no two CTAs share an SM and each takes in its 64 KB of K and V alone.
+constexpr size_t kClSmem = sizeof(ClusterSmem) + 1024;
+constexpr size_t kClSmemAlone = 120 * 1024;
+static_assert(kClSmem <= kClSmemAlone && 2 * (kClSmemAlone + 1024) > 228 * 1024, "one CTA per SM");
+
 template <bool kSelGiven, bool kInt8, int kCl>
-static cudaError_t launch_cluster(const DecodeAttendArgs& a, int rows, bool after_scan, cudaStream_t stream) {
-    const size_t smem = sizeof(ClusterSmem) + 1024;
+static cudaError_t launch_cluster(const DecodeAttendArgs& a, int rows, bool after_scan, size_t smem,
+                                  cudaStream_t stream) {
     cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(decode_cluster_kernel<kSelGiven, kInt8, kCl>), smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
@@ -541,15 +567,16 @@ static cudaError_t launch_cluster(const DecodeAttendArgs& a, int rows, bool afte
     return cudaGetLastError();
 }
 
-// Clusters of 8 CTAs of this kernel that the current device runs at once (queried once per
-// device; 0 if the query fails).
-static int clusters_of_8_at_once() {
-    static int counts[64] = {0};
+// Clusters of 8 CTAs of this kernel, each CTA with `alone` ? kClSmemAlone : kClSmem bytes of
+// shared memory, that the current device runs at once (queried once per device; 0 if the
+// query fails).
+static int clusters_of_8_at_once(bool alone) {
+    static int counts[2][64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
-    int& c = counts[dev & 63];
+    int& c = counts[alone][dev & 63];
     if (c == 0) {
-        const size_t smem = sizeof(ClusterSmem) + 1024;
+        const size_t smem = alone ? kClSmemAlone : kClSmem;
         if (ensure_smem_limit(reinterpret_cast<const void*>(decode_cluster_kernel<false, false, 8>), smem) != cudaSuccess)
             return 0;
         cudaLaunchConfig_t cfg = {};
@@ -576,20 +603,25 @@ static int clusters_of_8_at_once() {
 cudaError_t run_decode_cluster(const DecodeAttendArgs& a, bool after_scan, cudaStream_t stream) {
     const bool given = a.pooled == nullptr;
     const int rows = a.drow_prefix != nullptr ? a.decode_rows : a.num_seqs * a.rows_per_seq;
-    // Clusters of 8 finish a (row, head) soonest; when there are more problems than clusters
-    // of 8 fit at once, clusters of 4 (two rounds a CTA) run them in fewer waves.
-    const int cap = clusters_of_8_at_once();
-    const bool four = cap > 0 && static_cast<int64_t>(rows) * a.H > cap;
+    // Clusters of 8 finish a (row, head) soonest, one CTA per SM when they all fit that way;
+    // when there are more problems than clusters of 8 fit at once, clusters of 4 (two rounds a
+    // CTA) run them in fewer waves.
+    const int64_t problems = static_cast<int64_t>(rows) * a.H;
+    const int cap_alone = clusters_of_8_at_once(true);
+    const int cap = clusters_of_8_at_once(false);
+    const bool alone = cap_alone > 0 && problems <= cap_alone;
+    const bool four = !alone && cap > 0 && problems > cap;
+    const size_t smem = alone ? kClSmemAlone : kClSmem;
     if (a.kv_int8) {
-        if (given) return four ? launch_cluster<true, true, 4>(a, rows, after_scan, stream)
-                               : launch_cluster<true, true, 8>(a, rows, after_scan, stream);
-        return four ? launch_cluster<false, true, 4>(a, rows, after_scan, stream)
-                    : launch_cluster<false, true, 8>(a, rows, after_scan, stream);
+        if (given) return four ? launch_cluster<true, true, 4>(a, rows, after_scan, smem, stream)
+                               : launch_cluster<true, true, 8>(a, rows, after_scan, smem, stream);
+        return four ? launch_cluster<false, true, 4>(a, rows, after_scan, smem, stream)
+                    : launch_cluster<false, true, 8>(a, rows, after_scan, smem, stream);
     }
-    if (given) return four ? launch_cluster<true, false, 4>(a, rows, after_scan, stream)
-                           : launch_cluster<true, false, 8>(a, rows, after_scan, stream);
-    return four ? launch_cluster<false, false, 4>(a, rows, after_scan, stream)
-                : launch_cluster<false, false, 8>(a, rows, after_scan, stream);
+    if (given) return four ? launch_cluster<true, false, 4>(a, rows, after_scan, smem, stream)
+                           : launch_cluster<true, false, 8>(a, rows, after_scan, smem, stream);
+    return four ? launch_cluster<false, false, 4>(a, rows, after_scan, smem, stream)
+                : launch_cluster<false, false, 8>(a, rows, after_scan, smem, stream);
 }
 
 }  // namespace msa
