@@ -86,7 +86,8 @@ struct DecodeAttendArgs {
     int num_seqs, H, G, top_k, total_rows, max_cache_len;
     int64_t cache_tokens;
     float scale_log2;          // softmax scale * log2(e)
-    int kv_int8;               // 1: k, v are int8 [T, H, D] with fp32 scales [T, H]
+    int kv_int8;               // 1: k, v are int8 [T, H, D] with fp32 scales [T, H]; 2: k, v are the
+                               // int8 values widened to bf16 [T, H, D] (run_widen_kv), scales beside
     const float* k_scale;
     const float* v_scale;
     void* out;
@@ -146,6 +147,32 @@ struct PrefillAttendArgs {
     int only_multi_row;  // 1: skip decode-family sequences (<= kDecodeMaxRows rows; fused path)
     uint32_t* err;
 };
+
+// int8 caches, prompt chunks: the positions of every sequence the prompt-chunk
+// attention reads, widened once into a contiguous bf16 copy with the scales
+// beside it (sequence b at row wide_starts[b] = slot_b * slot_rows).
+constexpr int kWidenMaxSeqs = 8192;  // the slot prefix is kept in shared memory (4 bytes a sequence)
+struct WidenArgs {
+    const uint8_t* k8;  // int8 caches [T, H, D]
+    const uint8_t* v8;
+    const float* k_scale;  // [T, H]
+    const float* v_scale;
+    const int32_t* cu_rows;
+    const int32_t* cache_lens;
+    CacheRows cache;
+    int num_seqs, H, max_cache_len;
+    int64_t cache_tokens;
+    int only_multi_row;  // 1: sequences with more than kDecodeMaxRows rows only (fused path); 0: all
+    int max_slots;       // sequences the copy has room for
+    int slot_rows;       // rows per slot: max_cache_len rounded up to a multiple of kBlock
+    uint16_t* kw;        // bf16 [max_slots * slot_rows, H, D]
+    uint16_t* vw;
+    float* ksw;          // [max_slots * slot_rows, H]
+    float* vsw;
+    int64_t* wide_starts;  // [num_seqs]
+    uint32_t* err;
+};
+cudaError_t run_widen_kv(const WidenArgs& a, cudaStream_t stream);
 
 // Allocation-free decode attention: scratch in a file-scope device array
 // sized for at most kNoAllocMaxPairs (sequence, KV head) pairs per call.

@@ -2,6 +2,7 @@
 // maps and the launch sequence.  See include/msa.h for the contract.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -124,9 +125,40 @@ msa::CacheRows cache_rows_of(const msa_problem* p) {
 
 struct Layout {
     size_t err = 0, tickets = 0, idx_tickets = 0, pooled = 0, partials = 0, sel = 0, nsel = 0, idx_cand = 0,
-           drow_prefix = 0, total = 0;
+           drow_prefix = 0, wide_starts = 0, wide_k = 0, wide_v = 0, wide_ks = 0, wide_vs = 0, total = 0;
     size_t header_bytes = 0;  // error word + tickets, cleared at the start of a call
 };
+
+// int8 caches, prompt-chunk attention: the sequences' keys and values are widened once per call
+// into the workspace (run_widen_kv) when each widened position serves at least four kept key rows
+// on average (every row may keep top_k blocks); otherwise the attention widens the int8 tiles it
+// loads.  The sequences read are those with more than 8 rows (msa_forward: at most R / 9 of them,
+// and num_seqs - num_decode_seqs when that count is given) or all of them (msa_attend_prefill).
+constexpr int64_t kWidenMaxBytes = int64_t{8} << 30;
+struct WidenPlan {
+    bool on = false;
+    int64_t slots = 0, slot_rows = 0;
+};
+int64_t widen_bytes_per_row(const msa_problem* p) {  // K and V bf16, two fp32 scales, per cache row
+    return static_cast<int64_t>(p->num_kv_heads) * (2 * msa::kHeadDim * 2 + 2 * 4);
+}
+WidenPlan widen_plan(const msa_problem* p, bool only_multi_row) {
+    WidenPlan w;
+    if (p->kv_dtype != MSA_KV_INT8 || p->num_seqs > msa::kWidenMaxSeqs) return w;
+    int64_t n = p->num_seqs;
+    if (only_multi_row) {
+        if (p->num_decode_seqs >= 0) n = std::min<int64_t>(n, p->num_seqs - p->num_decode_seqs);
+        n = std::min<int64_t>(n, p->total_rows / (msa::kDecodeMaxRows + 1));
+    } else {
+        n = std::min<int64_t>(n, p->total_rows);
+    }
+    w.slots = n;
+    w.slot_rows = (static_cast<int64_t>(p->max_cache_len) + msa::kBlock - 1) / msa::kBlock * msa::kBlock;
+    if (n < 1) return w;
+    const int64_t kept_rows = static_cast<int64_t>(p->total_rows) * p->top_k * msa::kBlock;
+    w.on = kept_rows >= 4 * n * w.slot_rows && n * w.slot_rows * widen_bytes_per_row(p) <= kWidenMaxBytes;
+    return w;
+}
 
 // Upper bound of the prompt-chunk indexer's row tiles (128 rows each).
 int64_t index_tile_bound(const msa_problem* p) { return (p->total_rows + 127) / 128 + p->num_seqs; }
@@ -162,6 +194,21 @@ Layout layout_of(const msa_problem* p) {
         off = align256(off + R * H * msa::kIdxMaxSplit * 15 * sizeof(uint64_t));
     l.drow_prefix = off;  // decode-family rows per sequence, prefix (compact decode attention grid)
     off = align256(off + (B + 1) * sizeof(int32_t));
+    // int8 caches, prompt chunks widened once per call: room for the larger of the two entry points' plans
+    const WidenPlan wf = widen_plan(p, true), wa = widen_plan(p, false);
+    const size_t wrows = static_cast<size_t>(std::max(wf.on ? wf.slots * wf.slot_rows : 0, wa.on ? wa.slots * wa.slot_rows : 0));
+    l.wide_starts = off;
+    if (wrows > 0) {
+        off = align256(off + B * sizeof(int64_t));
+        l.wide_k = off;
+        off = align256(off + wrows * H * msa::kHeadDim * 2);
+        l.wide_v = off;
+        off = align256(off + wrows * H * msa::kHeadDim * 2);
+        l.wide_ks = off;
+        off = align256(off + wrows * H * sizeof(float));
+        l.wide_vs = off;
+        off = align256(off + wrows * H * sizeof(float));
+    }
     l.total = off;
     return l;
 }
@@ -464,6 +511,50 @@ static msa_status attention_maps(const msa_problem* p, const void* q, const void
     return kv_map(vm, p, v, "v_cache");
 }
 
+// Widens the int8 keys and values of the sequences the prompt-chunk attention reads into the
+// workspace (enqueued on `st`) and points the attention's arguments at the copy: bf16 maps
+// (*km, *vm), its rows, its scales.
+static msa_status widen_for_attention(const msa_problem* p, const WidenPlan& w, bool only_multi_row,
+                                      const void* k_cache, const void* v_cache, uint8_t* ws, const Layout& l,
+                                      CUtensorMap* km, CUtensorMap* vm, msa::PrefillAttendArgs* a, cudaStream_t st) {
+    msa::WidenArgs wa{};
+    wa.k8 = static_cast<const uint8_t*>(k_cache);
+    wa.v8 = static_cast<const uint8_t*>(v_cache);
+    wa.k_scale = p->k_scale;
+    wa.v_scale = p->v_scale;
+    wa.cu_rows = p->cu_rows;
+    wa.cache_lens = p->cache_lens;
+    wa.cache = cache_rows_of(p);
+    wa.num_seqs = p->num_seqs;
+    wa.H = p->num_kv_heads;
+    wa.max_cache_len = p->max_cache_len;
+    wa.cache_tokens = p->cache_tokens;
+    wa.only_multi_row = only_multi_row ? 1 : 0;
+    wa.max_slots = static_cast<int>(w.slots);
+    wa.slot_rows = static_cast<int>(w.slot_rows);
+    wa.kw = reinterpret_cast<uint16_t*>(ws + l.wide_k);
+    wa.vw = reinterpret_cast<uint16_t*>(ws + l.wide_v);
+    wa.ksw = reinterpret_cast<float*>(ws + l.wide_ks);
+    wa.vsw = reinterpret_cast<float*>(ws + l.wide_vs);
+    wa.wide_starts = reinterpret_cast<int64_t*>(ws + l.wide_starts);
+    wa.err = reinterpret_cast<uint32_t*>(ws + l.err);
+    const uint64_t T = static_cast<uint64_t>(w.slots * w.slot_rows), H = p->num_kv_heads;
+    msa_status s;
+    if ((s = make_map(km, wa.kw, 128, H, T, 64, 1, 64, "widened k")) != MSA_OK) return s;
+    if ((s = make_map(vm, wa.vw, 128, H, T, 64, 1, 64, "widened v")) != MSA_OK) return s;
+    cudaError_t e = msa::run_widen_kv(wa, st);
+    if (e != cudaSuccess) return cuda_fail(e, "key/value widening launch");
+    a->k_map = km;
+    a->v_map = vm;
+    a->cache = msa::CacheRows{};
+    a->cache.starts = wa.wide_starts;
+    a->cache_tokens = static_cast<int64_t>(T);
+    a->kv_int8 = 2;
+    a->k_scale = wa.ksw;
+    a->v_scale = wa.vsw;
+    return MSA_OK;
+}
+
 msa_status msa_attend_prefill(const msa_problem* p, const void* q, const void* k_cache, const void* v_cache,
                               const int32_t* sel, const int32_t* nsel, void* out, void* workspace,
                               size_t workspace_bytes, void* stream) {
@@ -479,6 +570,9 @@ msa_status msa_attend_prefill(const msa_problem* p, const void* q, const void* k
     if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
     msa::PrefillAttendArgs a = prefill_attend_args(p, &qm, &km, &vm, sel, nsel, out, ws, l);
     a.only_multi_row = 0;
+    const WidenPlan w = widen_plan(p, false);
+    CUtensorMap kwm, vwm;
+    if (w.on && (s = widen_for_attention(p, w, false, k_cache, v_cache, ws, l, &kwm, &vwm, &a, st)) != MSA_OK) return s;
     e = msa::run_prefill_attend(a, st);
     return e == cudaSuccess ? MSA_OK : cuda_fail(e, "prefill attention launch");
 }
@@ -517,7 +611,7 @@ msa_status msa_attend_decode_noalloc(const msa_problem* p, const void* q, const 
 
 int32_t msa_forward_launches(const msa_problem* p) {
     if (check_problem(p) != MSA_OK) return -1;
-    return (decode_family(p) ? 2 : 0) + (prefill_family(p) ? 2 : 0);
+    return (decode_family(p) ? 2 : 0) + (prefill_family(p) ? (widen_plan(p, true).on ? 3 : 2) : 0);
 }
 
 msa_status msa_forward_marked(const msa_problem* p, const void* q, const void* iq, const void* k_cache,
@@ -634,6 +728,10 @@ msa_status msa_forward_marked(const msa_problem* p, const void* q, const void* i
         if ((s = marks.mark(3)) != MSA_OK) return s;
         msa::PrefillAttendArgs pa = prefill_attend_args(p, &qm, &km, &vm, sel, nsel, out, ws, l);
         pa.only_multi_row = 1;
+        const WidenPlan w = widen_plan(p, true);
+        CUtensorMap kwm, vwm;
+        if (w.on && (s = widen_for_attention(p, w, true, k_cache, v_cache, ws, l, &kwm, &vwm, &pa, st)) != MSA_OK)
+            return s;
         if ((e = msa::run_prefill_attend(pa, st)) != cudaSuccess) return cuda_fail(e, "prefill attention launch");
         if ((s = marks.mark(4)) != MSA_OK) return s;
     } else {

@@ -56,17 +56,21 @@
 
 namespace msa {
 
-// Block shape and ring depths: bf16 caches, or int8 caches with four converter
-// warps and a shorter K ring.
-template <bool kInt8>
+// Key/value forms: bf16 caches; int8 caches whose tiles the kernel widens
+// (eight converter warps, 17-20 for K and the scales, 21-24 for V); int8
+// caches widened beforehand (run_widen_kv: bf16 tiles of the integers, scales
+// beside them; warps 17-20 only stage the scales).  Both int8 forms have a
+// shorter K ring, which leaves room for the scales of two items.
+enum KvForm { kKvBf16 = 0, kKvInt8 = 1, kKvWidened = 2 };
+template <int kKv>
 struct PaCfg {
-    static constexpr int kConverters = kInt8 ? 8 : 0;  // warps 17 .. 24: 4 for K, 4 for V
+    static constexpr int kConverters = kKv == kKvInt8 ? 8 : (kKv == kKvWidened ? 4 : 0);
     static constexpr int kThreads = 544 + 32 * kConverters;
-    static constexpr int kKStages = kInt8 ? 2 : 3;   // K pairs ring (its own producer warp)
+    static constexpr int kKStages = kKv != kKvBf16 ? 2 : 3;  // K pairs ring (its own producer warp)
     static constexpr int kPvStages = 3;              // V pairs + P pairs ring: slot i holds both operands of one PV pair
     // info ring readers: K and V producers, S and PV issuers, softmax warps, epilogue warps, converters
     static constexpr int kInfoReaders = 2 + 2 + 8 + 4 + kConverters;
-    static constexpr int kScaleFloats = kInt8 ? 2 * 2 * kMaxTopK * 64 : 1;  // [item parity][key/value][block][key]
+    static constexpr int kScaleFloats = kKv != kKvBf16 ? 2 * 2 * kMaxTopK * 64 : 1;  // [item parity][key/value][block][key]
 };
 constexpr int kPairBytes = 2 * 2 * 64 * 64 * 2;  // [dim half][2 blocks x 64 keys][64 dims] bf16 = 32 KB
 constexpr int kQBytes = 2 * 16 * 64 * 2;         // [dim half][16 heads][64 dims] = 4 KB
@@ -85,14 +89,14 @@ struct ItemInfo {
     int32_t row[kMaxTopK];    // their first cache rows
 };
 
-template <bool kInt8>
+template <int kKv>
 struct __align__(1024) AttendSmem {
-    static constexpr int kKStages = PaCfg<kInt8>::kKStages, kPvStages = PaCfg<kInt8>::kPvStages;
+    static constexpr int kKStages = PaCfg<kKv>::kKStages, kPvStages = PaCfg<kKv>::kPvStages;
     uint8_t kst[kKStages][kPairBytes];
     uint8_t vst[kPvStages][kPairBytes];
     uint8_t p[kPvStages][kPSlotBytes];
     uint8_t q[2][kQBytes];
-    float sc[PaCfg<kInt8>::kScaleFloats];  // int8 cache: key and value scales of two items
+    float sc[PaCfg<kKv>::kScaleFloats];  // int8 cache: key and value scales of two items
     uint64_t kfull[kKStages];
     uint64_t kempty[kKStages];
     uint64_t kraw[kKStages];       // int8 cache: the K pair's int8 tiles landed
@@ -118,8 +122,9 @@ struct __align__(1024) AttendSmem {
     uint32_t tmem_base;
 };
 
-static_assert(sizeof(AttendSmem<false>) + 1024 <= 227 * 1024, "prompt-chunk attention exceeds 227 KB of shared memory");
-static_assert(sizeof(AttendSmem<true>) + 1024 <= 227 * 1024, "prompt-chunk attention (int8) exceeds 227 KB of shared memory");
+static_assert(sizeof(AttendSmem<kKvBf16>) + 1024 <= 227 * 1024, "prompt-chunk attention exceeds 227 KB of shared memory");
+static_assert(sizeof(AttendSmem<kKvInt8>) + 1024 <= 227 * 1024, "prompt-chunk attention (int8) exceeds 227 KB of shared memory");
+static_assert(sizeof(AttendSmem<kKvWidened>) + 1024 <= 227 * 1024, "prompt-chunk attention (widened) exceeds 227 KB");
 
 // One work item as decoded by a warp: the row, KV head, position, number of
 // kept blocks and sequence (the same in every lane), and kept block `lane`
@@ -185,28 +190,30 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 }
 
 
-template <bool kInt8>
-__global__ void __launch_bounds__(PaCfg<kInt8>::kThreads, 1) prefill_attend_kernel(const __grid_constant__ CUtensorMap q_map,
-                                                                       const __grid_constant__ CUtensorMap k_map,
-                                                                       const __grid_constant__ CUtensorMap v_map,
-                                                                       const PrefillAttendArgs a) {
-    using Cfg = PaCfg<kInt8>;
+template <int kKv>
+__global__ void __launch_bounds__(PaCfg<kKv>::kThreads, 1) prefill_attend_kernel(const __grid_constant__ CUtensorMap q_map,
+                                                                     const __grid_constant__ CUtensorMap k_map,
+                                                                     const __grid_constant__ CUtensorMap v_map,
+                                                                     const PrefillAttendArgs a) {
+    using Cfg = PaCfg<kKv>;
+    constexpr bool kInt8 = kKv != kKvBf16;   // scores and weights times the int8 scales
+    constexpr bool kWiden = kKv == kKvInt8;  // int8 tiles widened here
     constexpr int kKStages = Cfg::kKStages, kPvStages = Cfg::kPvStages;
     extern __shared__ uint8_t smem_raw[];
-    AttendSmem<kInt8>& sm =
-        *reinterpret_cast<AttendSmem<kInt8>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    AttendSmem<kKv>& sm =
+        *reinterpret_cast<AttendSmem<kKv>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int n_items = a.total_rows * a.H;
 
     if (tid == 0) {
         for (int s = 0; s < kKStages; ++s) {
-            mbar_init(&sm.kfull[s], kInt8 ? 4 : 1);  // the K producer's bytes, or the four K converter warps
+            mbar_init(&sm.kfull[s], kWiden ? 4 : 1);  // the K producer's bytes, or the four K converter warps
             mbar_init(&sm.kempty[s], 1);
             mbar_init(&sm.kraw[s], 1);
         }
         for (int s = 0; s < kPvStages; ++s) {
             // V bytes (producer) or the four V converter warps, + one arrival per softmax warp
-            mbar_init(&sm.pv_full[s], (kInt8 ? 4 : 1) + 8);
+            mbar_init(&sm.pv_full[s], (kWiden ? 4 : 1) + 8);
             mbar_init(&sm.pv_empty[s], 1);
             mbar_init(&sm.vraw[s], 1);
         }
@@ -308,11 +315,11 @@ __global__ void __launch_bounds__(PaCfg<kInt8>::kThreads, 1) prefill_attend_kern
                         alive = false;
                         break;
                     }
-                    uint64_t* kbar = kInt8 ? &sm.kraw[s] : &sm.kfull[s];
-                    mbar_arrive_expect_tx(kbar, kInt8 ? kPairBytes / 2 : kPairBytes);
+                    uint64_t* kbar = kWiden ? &sm.kraw[s] : &sm.kfull[s];
+                    mbar_arrive_expect_tx(kbar, kWiden ? kPairBytes / 2 : kPairBytes);
                     for (int half = 0; half < 2; ++half) {
                         const int tok = inf.row[min(2 * q + half, nsel - 1)];
-                        if constexpr (kInt8) {  // one int8 tile per block, in the slot's upper half
+                        if constexpr (kWiden) {  // one int8 tile per block, in the slot's upper half
                             tma_load_3d(sm.kst[s] + 16384 + half * 8192, &k_map, kbar, 0, inf.h, tok);
                         } else {
                             tma_load_3d(sm.kst[s] + half * 8192, &k_map, kbar, 0, inf.h, tok);
@@ -327,7 +334,7 @@ __global__ void __launch_bounds__(PaCfg<kInt8>::kThreads, 1) prefill_attend_kern
             // every slot
             for (uint32_t s = 0; s < kKStages; ++s)
                 if (g > s)
-                    mbar_wait(kInt8 ? &sm.kraw[s] : &sm.kfull[s], ((s + kKStages * ((g - 1 - s) / kKStages)) / kKStages) & 1,
+                    mbar_wait(kWiden ? &sm.kraw[s] : &sm.kfull[s], ((s + kKStages * ((g - 1 - s) / kKStages)) / kKStages) & 1,
                               a.err);
             for (uint32_t b = 0; b < 2; ++b)
                 if (q_armed > b) mbar_wait(&sm.q_full[b], ((b + 2 * ((q_armed - 1 - b) / 2)) >> 1) & 1, a.err);
@@ -351,11 +358,11 @@ __global__ void __launch_bounds__(PaCfg<kInt8>::kThreads, 1) prefill_attend_kern
                         alive = false;
                         break;
                     }
-                    uint64_t* vbar = kInt8 ? &sm.vraw[s] : &sm.pv_full[s];
-                    mbar_arrive_expect_tx(vbar, kInt8 ? kPairBytes / 2 : kPairBytes);
+                    uint64_t* vbar = kWiden ? &sm.vraw[s] : &sm.pv_full[s];
+                    mbar_arrive_expect_tx(vbar, kWiden ? kPairBytes / 2 : kPairBytes);
                     for (int half = 0; half < 2; ++half) {
                         const int tok = inf.row[min(2 * q + half, inf.nsel - 1)];
-                        if constexpr (kInt8) {
+                        if constexpr (kWiden) {
                             tma_load_3d(sm.vst[s] + 16384 + half * 8192, &v_map, vbar, 0, inf.h, tok);
                         } else {
                             tma_load_3d(sm.vst[s] + half * 8192, &v_map, vbar, 0, inf.h, tok);
@@ -368,7 +375,7 @@ __global__ void __launch_bounds__(PaCfg<kInt8>::kThreads, 1) prefill_attend_kern
             }
             for (uint32_t s = 0; s < kPvStages; ++s)  // as for K: no copy left in flight
                 if (g > s)
-                    mbar_wait(kInt8 ? &sm.vraw[s] : &sm.pv_full[s],
+                    mbar_wait(kWiden ? &sm.vraw[s] : &sm.pv_full[s],
                               ((s + kPvStages * ((g - 1 - s) / kPvStages)) / kPvStages) & 1, a.err);
         }
     } else if (warp == 14) {
@@ -609,7 +616,8 @@ __global__ void __launch_bounds__(PaCfg<kInt8>::kThreads, 1) prefill_attend_kern
     } else if (kInt8 && warp >= 17) {
         // ---------------- int8 converters: warps 17-20 widen the K pairs (warp 17 + j takes keys
         // 32 (j & 1) .. + 31 of block j / 2 of every pair) and write the item's key and value
-        // scales, warps 21-24 the V pairs; each lane widens one key row in place
+        // scales, warps 21-24 the V pairs; each lane widens one key row in place.  Tiles widened
+        // beforehand: warps 17-20 write the scales only.
         const int cw = warp - 17;
         const bool is_k = cw < 4;
         const int part = cw & 3;  // block part >> 1, keys 32 (part & 1) ..
@@ -648,7 +656,7 @@ __global__ void __launch_bounds__(PaCfg<kInt8>::kThreads, 1) prefill_attend_kern
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&sm.sc_full[sb]);
             }
-            for (int q = 0; q < npairs; ++q, ++g) {
+            for (int q = 0; kWiden && q < npairs; ++q, ++g) {
                 const int s = is_k ? static_cast<int>(g % kKStages) : static_cast<int>(g % kPvStages);
                 const uint32_t ph = is_k ? (g / kKStages) & 1 : (g / kPvStages) & 1;
                 if (!mbar_wait(is_k ? &sm.kraw[s] : &sm.vraw[s], ph, a.err)) {
@@ -715,19 +723,20 @@ __global__ void __launch_bounds__(PaCfg<kInt8>::kThreads, 1) prefill_attend_kern
     }
 }
 
-template <bool kInt8>
+template <int kKv>
 static cudaError_t launch_prefill_attend(const PrefillAttendArgs& a, cudaStream_t stream) {
-    const size_t smem = sizeof(AttendSmem<kInt8>) + 1024;
-    cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(prefill_attend_kernel<kInt8>), smem);
+    const size_t smem = sizeof(AttendSmem<kKv>) + 1024;
+    cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(prefill_attend_kernel<kKv>), smem);
     if (e != cudaSuccess) return e;
     const int64_t items = static_cast<int64_t>(a.total_rows) * a.H;
     const int grid = static_cast<int>(items < device_sm_count() ? items : device_sm_count());
-    prefill_attend_kernel<kInt8><<<grid, PaCfg<kInt8>::kThreads, smem, stream>>>(*a.q_map, *a.k_map, *a.v_map, a);
+    prefill_attend_kernel<kKv><<<grid, PaCfg<kKv>::kThreads, smem, stream>>>(*a.q_map, *a.k_map, *a.v_map, a);
     return cudaGetLastError();
 }
 
 cudaError_t run_prefill_attend(const PrefillAttendArgs& a, cudaStream_t stream) {
-    return a.kv_int8 ? launch_prefill_attend<true>(a, stream) : launch_prefill_attend<false>(a, stream);
+    if (a.kv_int8 == 2) return launch_prefill_attend<kKvWidened>(a, stream);
+    return a.kv_int8 ? launch_prefill_attend<kKvInt8>(a, stream) : launch_prefill_attend<kKvBf16>(a, stream);
 }
 
 }  // namespace msa

@@ -169,7 +169,15 @@ const char* msa_last_error(void);
  * outside the host-side bounds, e.g. a sequence with more rows than
  * max_rows_per_seq; such a sequence is skipped, nothing is written outside
  * the buffers), 4 (tensor memory could not be allocated); valid once that
- * call has completed on the stream. */
+ * call has completed on the stream.
+ * With an int8 key/value cache (kv_dtype MSA_KV_INT8) and prompt chunks whose
+ * rows keep at least four times as many key rows (rows x top_k x 64) as the
+ * attended sequences have positions (their count x max_cache_len, rounded up
+ * to 64), the workspace also holds a bf16 copy of those sequences' keys and
+ * values with their scales (520 x H bytes a position, at most 8 GiB): each
+ * position is widened once per call (exactly: int8 values are bf16 integers)
+ * instead of once per kept block of every row, and msa_forward launches one
+ * more kernel (msa_forward_launches counts it). */
 msa_status msa_workspace_size(const msa_problem* p, size_t* bytes);
 
 /* Stage 1 alone: the lightning-indexer scores.  PR #1388, native Metal family

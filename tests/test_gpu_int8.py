@@ -155,6 +155,74 @@ def test_int8_prompt_extreme_values_and_scales():
     assert (np.abs(o - ref["out"]) / scale).max() <= 2e-3
 
 
+def _widen_plan(seqs, only_multi_row, top_k=16, S=64):
+    """The library's choice for an int8 prompt-chunk attention: widen the read
+    sequences once into the workspace when each widened position serves at
+    least four kept key rows on average (host counts exact, as the binding
+    fills them)."""
+    R = sum(n for n, _ in seqs)
+    n = sum(1 for r, _ in seqs if r > 8) if only_multi_row else len(seqs)
+    slot_rows = -(-max(L for _, L in seqs) // S) * S
+    return n >= 1 and R * top_k * S >= 4 * n * slot_rows
+
+
+@pytest.mark.parametrize("seqs,widened", [
+    ([(200, 1300), (9, 3000), (128, 4096), (1, 2000)], True),  # ragged, whole-block and decode beside
+    ([(9, 20000), (1, 3000)], False),                           # few rows over a long prefix
+    ([(40, 4000), (3, 700), (12, 129)], True),
+])
+def test_int8_prompt_widened_once_or_per_item(seqs, widened):
+    """Both int8 prompt-chunk forms: the sequences widened once per call into
+    the workspace (one more kernel), or the tiles widened by the attention."""
+    assert _widen_plan(seqs, True) == widened
+    w = _w("int8_prompt_forms", seqs, seed=95 + len(seqs))
+    x = synth.make_inputs(w)
+    pb = problem(w, x)
+    dec = any(n <= 8 for n, _ in seqs)
+    assert pb.forward_launches() == (2 if dec else 0) + (3 if widened else 2)
+    out, sel, nsel = run_forward(w, x)
+    ref = oracle_forward(w, x)
+    assert_selection_equal(sel, nsel, ref)
+    assert_out_close(out, ref["out"], torch.float32)
+
+
+def test_int8_prompt_widened_decode_count_unknown():
+    """num_decode_seqs = -1: the copy has room for every sequence that could
+    have more than 8 rows, and the slots go to those that do."""
+    seqs = [(1, 3000), (30, 2100), (2, 500), (17, 64)]
+    w = _w("int8_prompt_unknown_count", seqs, seed=97)
+    x = synth.make_inputs(w)
+    dx = device_inputs(x)
+    pb = problem(w, x, num_decode_seqs=-1)
+    # widened: 50 rows x 16 x 64 kept key rows >= 4 x min(4 sequences, 50 // 9) x 3,008 positions
+    assert pb.forward_launches() == 5
+    ws = pb.workspace()
+    out, sel, nsel = msa().forward(pb, dx["q"], dx["iq"], dx["k"], dx["v"], dx["ik"], workspace=ws)
+    torch.cuda.synchronize()
+    assert msa().error_word(ws) == 0
+    ref = oracle_forward(w, x)
+    assert_selection_equal(sel, nsel, ref)
+    assert_out_close(out, ref["out"], torch.float32)
+
+
+@pytest.mark.parametrize("seqs", [[(300, 2500), (17, 700)], [(1, 3000), (4, 700), (1, 9000)]])
+def test_int8_attend_prefill_both_forms(seqs):
+    """msa_attend_prefill on every sequence of the batch: widened once (many
+    rows) or tile by tile (a few rows over long prefixes)."""
+    m = msa()
+    w = _w("int8_prefill_forms", seqs, seed=93)
+    x = synth.make_inputs(w)
+    dx = device_inputs(x)
+    pb = problem(w, x)
+    ref = oracle_forward(w, x)
+    ws = pb.workspace()
+    out = m.attend_prefill(pb, dx["q"], dx["k"], dx["v"], torch.from_numpy(ref["sel"]).cuda(),
+                           torch.from_numpy(ref["nsel"]).cuda(), workspace=ws)
+    torch.cuda.synchronize()
+    assert m.error_word(ws) == 0
+    assert_out_close(out, ref["out"], torch.float32)
+
+
 def test_int8_attend_prefill_given_selection():
     m = msa()
     w = _w("int8_prefill_given", [(300, 2500), (17, 700)], seed=91)
