@@ -25,6 +25,8 @@
 namespace msa {
 
 constexpr int kWidenThreads = 256;
+constexpr int kWidenPos = 16;    // positions per work unit (a quarter block)
+constexpr int kWidenBatch = 4;   // 16-byte chunks of K and of V a thread loads before it stores
 
 // Byte i of w as a signed integer, then 4 bytes as 4 bf16 (two words; exact: at most 8 significant bits)
 __device__ __forceinline__ float i8_at(uint32_t w, int i) {
@@ -71,49 +73,55 @@ __global__ void __launch_bounds__(kWidenThreads) widen_kv_kernel(const WidenArgs
         }
     }
 
-    // ---- units: (sequence, 64-position block), all heads, K and V
+    // ---- units: (sequence, 16 positions), all heads, K and V; a block's positions past L_b are
+    // written as zeros, so the units run to the end of the last block
     const int H = a.H;
-    const int tiles = a.slot_rows / kBlock;
-    const int64_t units = static_cast<int64_t>(B) * tiles;
+    const int groups = a.slot_rows / kWidenPos;
+    const int64_t units = static_cast<int64_t>(B) * groups;
     const int row_chunks = H * (kHeadDim / 16);  // 16-byte int8 chunks per position
+    const int unit_chunks = kWidenPos * row_chunks;
     for (int64_t u = blockIdx.x; u < units; u += gridDim.x) {
-        const int b = static_cast<int>(u / tiles), tile = static_cast<int>(u - static_cast<int64_t>(b) * tiles);
+        const int b = static_cast<int>(u / groups), grp = static_cast<int>(u - static_cast<int64_t>(b) * groups);
         const int slot = slot_of[b];
         if (slot < 0 || slot >= a.max_slots) continue;
         const int L = a.cache_lens[b];
-        const int t0 = tile * kBlock;
-        if (L < 1 || L > a.max_cache_len || t0 >= L) continue;  // the attention rejects such a sequence
-        const int64_t row = seq_rows_ok(a.cache, b, L, a.cache_tokens) ? block_row(a.cache, b, t0) : -1;
-        if (row < 0 && tid == 0) atomicOr(a.err, kErrBadMetadata);  // the block is written as zeros
-        const int64_t src = row < 0 ? 0 : row;
+        const int t0 = grp * kWidenPos, tb = t0 & ~(kBlock - 1);  // first position, its block's
+        if (L < 1 || L > a.max_cache_len || tb >= L) continue;  // the attention rejects such a sequence
+        const int64_t brow = seq_rows_ok(a.cache, b, L, a.cache_tokens) ? block_row(a.cache, b, tb) : -1;
+        if (brow < 0 && tid == 0 && t0 == tb) atomicOr(a.err, kErrBadMetadata);  // the block is written as zeros
+        const int64_t src = brow < 0 ? 0 : brow + (t0 - tb);  // a block's rows are contiguous (a page holds whole blocks)
         const int64_t dst = static_cast<int64_t>(slot) * a.slot_rows + t0;
-        const int live_rows = row < 0 ? 0 : min(kBlock, L - t0);
-        // 64 rows of H x 128 int8 each are contiguous in the cache (a page holds whole blocks)
+        const int live_rows = brow < 0 ? 0 : max(0, min(kWidenPos, L - t0));
         const uint8_t* k8 = a.k8 + src * H * kHeadDim;
         const uint8_t* v8 = a.v8 + src * H * kHeadDim;
         uint16_t* kw = a.kw + dst * H * kHeadDim;
         uint16_t* vw = a.vw + dst * H * kHeadDim;
-        for (int c = tid; c < kBlock * row_chunks; c += kWidenThreads) {
-            const bool live = c < live_rows * row_chunks;
-            const uint4 kx = live ? ld_stream_v4(k8 + c * 16) : make_uint4(0, 0, 0, 0);
-            const uint4 vx = live ? ld_stream_v4(v8 + c * 16) : make_uint4(0, 0, 0, 0);
-            const uint32_t kw4[4] = {kx.x, kx.y, kx.z, kx.w}, vw4[4] = {vx.x, vx.y, vx.z, vx.w};
-            uint4 ko[2], vo[2];
+        for (int c0 = tid; c0 < unit_chunks; c0 += kWidenBatch * kWidenThreads) {
+            uint4 kx[kWidenBatch], vx[kWidenBatch];  // every load of the batch in flight before a store
 #pragma unroll
-            for (int i = 0; i < 2; ++i) {
-                const uint2 k0 = widen_i8x4(kw4[2 * i]), k1 = widen_i8x4(kw4[2 * i + 1]);
-                const uint2 v0 = widen_i8x4(vw4[2 * i]), v1 = widen_i8x4(vw4[2 * i + 1]);
-                ko[i] = make_uint4(k0.x, k0.y, k1.x, k1.y);
-                vo[i] = make_uint4(v0.x, v0.y, v1.x, v1.y);
+            for (int j = 0; j < kWidenBatch; ++j) {
+                const int c = c0 + j * kWidenThreads;
+                const bool live = c < live_rows * row_chunks;
+                kx[j] = live ? ld_stream_v4(k8 + c * 16) : make_uint4(0, 0, 0, 0);
+                vx[j] = live ? ld_stream_v4(v8 + c * 16) : make_uint4(0, 0, 0, 0);
             }
-            uint4* kd = reinterpret_cast<uint4*>(kw + static_cast<int64_t>(c) * 16);
-            uint4* vd = reinterpret_cast<uint4*>(vw + static_cast<int64_t>(c) * 16);
-            kd[0] = ko[0];
-            kd[1] = ko[1];
-            vd[0] = vo[0];
-            vd[1] = vo[1];
+#pragma unroll
+            for (int j = 0; j < kWidenBatch; ++j) {
+                const int c = c0 + j * kWidenThreads;
+                if (c >= unit_chunks) break;
+                const uint2 k0 = widen_i8x4(kx[j].x), k1 = widen_i8x4(kx[j].y), k2 = widen_i8x4(kx[j].z),
+                            k3 = widen_i8x4(kx[j].w);
+                const uint2 v0 = widen_i8x4(vx[j].x), v1 = widen_i8x4(vx[j].y), v2 = widen_i8x4(vx[j].z),
+                            v3 = widen_i8x4(vx[j].w);
+                uint4* kd = reinterpret_cast<uint4*>(kw + static_cast<int64_t>(c) * 16);
+                uint4* vd = reinterpret_cast<uint4*>(vw + static_cast<int64_t>(c) * 16);
+                kd[0] = make_uint4(k0.x, k0.y, k1.x, k1.y);
+                kd[1] = make_uint4(k2.x, k2.y, k3.x, k3.y);
+                vd[0] = make_uint4(v0.x, v0.y, v1.x, v1.y);
+                vd[1] = make_uint4(v2.x, v2.y, v3.x, v3.y);
+            }
         }
-        for (int c = tid; c < kBlock * H; c += kWidenThreads) {
+        for (int c = tid; c < kWidenPos * H; c += kWidenThreads) {
             const bool live = c < live_rows * H;
             a.ksw[dst * H + c] = live ? a.k_scale[src * H + c] : 0.f;
             a.vsw[dst * H + c] = live ? a.v_scale[src * H + c] : 0.f;
@@ -122,8 +130,8 @@ __global__ void __launch_bounds__(kWidenThreads) widen_kv_kernel(const WidenArgs
 }
 
 cudaError_t run_widen_kv(const WidenArgs& a, cudaStream_t stream) {
-    const int64_t units = static_cast<int64_t>(a.num_seqs) * (a.slot_rows / kBlock);
-    const int64_t cap = 2 * static_cast<int64_t>(device_sm_count());
+    const int64_t units = static_cast<int64_t>(a.num_seqs) * (a.slot_rows / kWidenPos);
+    const int64_t cap = 4 * static_cast<int64_t>(device_sm_count());
     const int grid = static_cast<int>(units < cap ? (units > 0 ? units : 1) : cap);
     const size_t smem = static_cast<size_t>(a.num_seqs) * sizeof(int32_t);
     widen_kv_kernel<<<grid, kWidenThreads, smem, stream>>>(a);
