@@ -87,7 +87,7 @@ struct DecodeAttendArgs {
     int64_t cache_tokens;
     float scale_log2;          // softmax scale * log2(e)
     int kv_int8;               // 1: k, v are int8 [T, H, D] with fp32 scales [T, H]; 2: k, v are the
-                               // int8 values widened to bf16 [T, H, D] (run_widen_kv), scales beside
+                               // int8 values widened to bf16 [T, H, D] (run_widen_kv), scales [H, T]
     const float* k_scale;
     const float* v_scale;
     void* out;
@@ -167,7 +167,7 @@ struct WidenArgs {
     int slot_rows;       // rows per slot: max_cache_len rounded up to a multiple of kBlock
     uint16_t* kw;        // bf16 [max_slots * slot_rows, H, D]
     uint16_t* vw;
-    float* ksw;          // [max_slots * slot_rows, H]
+    float* ksw;          // [H, max_slots * slot_rows] (head-major)
     float* vsw;
     int64_t* wide_starts;  // [num_seqs]
     uint32_t* err;

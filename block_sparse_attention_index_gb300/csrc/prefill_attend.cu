@@ -644,8 +644,9 @@ __global__ void __launch_bounds__(PaCfg<kKv>::kThreads, 1) prefill_attend_kernel
                     for (int kk = 0; kk < 2; ++kk) {
                         const int key = lane + 32 * kk;
                         float ks = 0.f, vs = 0.f;
-                        if (t0 + key <= inf.p) {
-                            const int64_t si = (row0 + key) * a.H + inf.h;
+                        if (t0 + key <= inf.p) {  // the widened copy keeps its scales head-major
+                            const int64_t si = kKv == kKvWidened ? inf.h * a.cache_tokens + row0 + key
+                                                                 : (row0 + key) * a.H + inf.h;
                             ks = a.k_scale[si];
                             vs = a.v_scale[si];
                         }

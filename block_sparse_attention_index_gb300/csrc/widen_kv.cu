@@ -13,8 +13,9 @@
 //
 // Layout: sequence b's copy starts at row  slot_b * slot_rows  (slot_b counts
 // the widened sequences before b; slot_rows = max_cache_len rounded up to a
-// whole block), rows [T', H, 128] bf16 for K and V and [T', H] fp32 for the
-// scales.  Positions from L_b to the end of their 64-position block are
+// whole block), rows [T', H, 128] bf16 for K and V and [H, T'] fp32 for the
+// scales (head-major, so that a warp staging one head's scales for 32
+// consecutive keys reads one 128-byte line).  Positions from L_b to the end of their 64-position block are
 // written as zeros: keys past a row's position are masked, and a zero value
 // keeps 0 x value out of the P V products.  Row starts per sequence go to
 // `wide_starts` (0 for a sequence that is not widened, -1 for one past the
@@ -76,6 +77,7 @@ __global__ void __launch_bounds__(kWidenThreads) widen_kv_kernel(const WidenArgs
     // ---- units: (sequence, 16 positions), all heads, K and V; a block's positions past L_b are
     // written as zeros, so the units run to the end of the last block
     const int H = a.H;
+    const int64_t wide_rows = static_cast<int64_t>(a.max_slots) * a.slot_rows;
     const int groups = a.slot_rows / kWidenPos;
     const int64_t units = static_cast<int64_t>(B) * groups;
     const int row_chunks = H * (kHeadDim / 16);  // 16-byte int8 chunks per position
@@ -121,10 +123,12 @@ __global__ void __launch_bounds__(kWidenThreads) widen_kv_kernel(const WidenArgs
                 vd[1] = make_uint4(v2.x, v2.y, v3.x, v3.y);
             }
         }
-        for (int c = tid; c < kWidenPos * H; c += kWidenThreads) {
+        for (int c = tid; c < kWidenPos * H; c += kWidenThreads) {  // scales head-major: [H][rows]
             const bool live = c < live_rows * H;
-            a.ksw[dst * H + c] = live ? a.k_scale[src * H + c] : 0.f;
-            a.vsw[dst * H + c] = live ? a.v_scale[src * H + c] : 0.f;
+            const int pos = c / H, h = c - pos * H;
+            const int64_t o = static_cast<int64_t>(h) * wide_rows + dst + pos;
+            a.ksw[o] = live ? a.k_scale[src * H + c] : 0.f;
+            a.vsw[o] = live ? a.v_scale[src * H + c] : 0.f;
         }
     }
 }
