@@ -247,49 +247,64 @@ __global__ void __launch_bounds__(kClThreads, 2) decode_cluster_kernel(const __g
 #pragma unroll
     for (int i = 0; i < 4; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
     int late_phase = -1;  // a copy that did not land in time: its phase, waited for again at the end
+    int k_armed = -1;     // last phase of the K barrier with copies armed (round r arms phase r)
+    // Warps 0-3 issue a round's copies, each arming the barrier with its own bytes first (warps
+    // without a copy arrive without bytes): one thread issues TMA boxes at a bounded rate, so
+    // four issuers land the 64 KB sooner than one.  K goes first, so that S and the softmax
+    // overlap the V transfer, and a later round's K leaves as soon as the last round's S has read
+    // the K tiles.  bf16: warp w copies dims 64 (w & 1) .. of block w / 2; int8 (one 128-dim box
+    // a tile): warp w copies the K (w < 2) or V tile of block w & 1.  Called by lane 0 of warps
+    // 0-3; every call arrives once on its barrier.
+    auto copy_row = [&](int bi) {
+        int64_t row = block_row(a.cache, b, static_cast<int64_t>(bi) * kBlock);
+        if (row < 0) {  // page outside the pool
+            atomicOr(a.err, kErrBadMetadata);
+            row = 0;
+        }
+        return static_cast<int>(row);
+    };
+    auto issue_k = [&](int nr, int bA, int bB) {
+        const int i = kInt8 ? (warp & 1) : (warp >> 1);
+        if (i < nr && (!kInt8 || warp < 2)) {
+            const int tok = copy_row(i == 0 ? bA : bB);
+            if constexpr (kInt8) {  // one int8 tile per block into the upper 8 KB, widened in place below
+                mbar_arrive_expect_tx(&sm.bar_k, 64 * 128);
+                tma_load_3d(sm.k[i][1], &k_map, &sm.bar_k, 0, h, tok);
+            } else {
+                const int half = warp & 1;
+                mbar_arrive_expect_tx(&sm.bar_k, 64 * 64 * 2);
+                tma_load_3d(sm.k[i][half], &k_map, &sm.bar_k, 64 * half, h, tok);
+            }
+        } else {
+            mbar_arrive(&sm.bar_k);
+        }
+    };
+    auto issue_v = [&](int nr, int bA, int bB) {
+        const int i = kInt8 ? (warp & 1) : (warp >> 1);
+        if (i < nr && (!kInt8 || warp >= 2)) {
+            const int tok = copy_row(i == 0 ? bA : bB);
+            if constexpr (kInt8) {
+                mbar_arrive_expect_tx(&sm.bar_v, 64 * 128);
+                tma_load_3d(sm.v[i][1], &v_map, &sm.bar_v, 0, h, tok);
+            } else {
+                const int half = warp & 1;
+                mbar_arrive_expect_tx(&sm.bar_v, 64 * 64 * 2);
+                tma_load_3d(sm.v[i][half], &v_map, &sm.bar_v, 64 * half, h, tok);
+            }
+        } else {
+            mbar_arrive(&sm.bar_v);
+        }
+    };
 #pragma unroll
     for (int rd = 0; rd < kRounds; ++rd) {
         const int nr = min(max(nmy - 2 * rd, 0), 2);  // this round's blocks (uniform over the CTA)
         const int bA = blk[2 * rd], bB = blk[2 * rd + 1];
-        if (rd > 0) __syncthreads();  // the tiles, P and the row statistics of the last round are read
-        // Warps 0-3 issue the round's copies, K before V, each arming the two barriers with its
-        // own bytes first (warps without a copy arrive without bytes): one thread issues TMA boxes
-        // at a bounded rate, so four issuers land the 64 KB sooner than one, and with the K boxes
-        // queued first S and the softmax overlap the V transfer.  bf16: warp w copies dims
-        // 64 (w & 1) .. of block w / 2, K then V; int8 (one 128-dim box a tile): warp w copies
-        // the K (w < 2) or V tile of block w & 1.
+        if (rd > 0) __syncthreads();  // the V tiles, P and the row statistics of the last round are read
         if (lane == 0 && warp < 4) {
-            const int i = kInt8 ? (warp & 1) : (warp >> 1);
-            if (i < nr) {
-                const int bi = i == 0 ? bA : bB;  // no dynamic index into blk: it stays in registers
-                int64_t row = block_row(a.cache, b, static_cast<int64_t>(bi) * kBlock);
-                if (row < 0) {  // page outside the pool
-                    atomicOr(a.err, kErrBadMetadata);
-                    row = 0;
-                }
-                const int tok = static_cast<int>(row);
-                if constexpr (kInt8) {  // one int8 tile per block into the upper 8 KB, widened in place below
-                    if (warp < 2) {
-                        mbar_arrive_expect_tx(&sm.bar_k, 64 * 128);
-                        tma_load_3d(sm.k[i][1], &k_map, &sm.bar_k, 0, h, tok);
-                        mbar_arrive(&sm.bar_v);
-                    } else {
-                        mbar_arrive(&sm.bar_k);
-                        mbar_arrive_expect_tx(&sm.bar_v, 64 * 128);
-                        tma_load_3d(sm.v[i][1], &v_map, &sm.bar_v, 0, h, tok);
-                    }
-                } else {
-                    const int half = warp & 1;
-                    mbar_arrive_expect_tx(&sm.bar_k, 64 * 64 * 2);
-                    mbar_arrive_expect_tx(&sm.bar_v, 64 * 64 * 2);
-                    tma_load_3d(sm.k[i][half], &k_map, &sm.bar_k, 64 * half, h, tok);
-                    tma_load_3d(sm.v[i][half], &v_map, &sm.bar_v, 64 * half, h, tok);
-                }
-            } else {
-                mbar_arrive(&sm.bar_k);
-                mbar_arrive(&sm.bar_v);
-            }
+            if (rd == 0) issue_k(nr, bA, bB);  // a later round's K left after the last round's S
+            issue_v(nr, bA, bB);
         }
+        if (rd == 0) k_armed = 0;
         if (!kSelGiven && rd == 0 && rank == 0 && a.sel_out != nullptr && tid < a.top_k) {
             // the kept blocks ascending, for the caller, while the first copies are in flight
             const int64_t o = (static_cast<int64_t>(r) * H + h) * a.top_k;
@@ -386,6 +401,13 @@ __global__ void __launch_bounds__(kClThreads, 2) decode_cluster_kernel(const __g
             sm.wmax[warp][grp + 8] = rmax[1];
         }
         __syncthreads();
+        if constexpr (kRounds > 1) {
+            if (rd + 1 < kRounds) {  // every warp has read the K tiles: the next round's K leaves now
+                if (lane == 0 && warp < 4)
+                    issue_k(min(max(nmy - 2 * (rd + 1), 0), 2), blk[2 * rd + 2], blk[2 * rd + 3]);
+                k_armed = rd + 1;
+            }
+        }
         // new running maxima; the old sums and outputs are rescaled to them
         float mnew[2], alpha[2], lsum[2] = {0.f, 0.f};
 #pragma unroll
@@ -532,7 +554,7 @@ __global__ void __launch_bounds__(kClThreads, 2) decode_cluster_kernel(const __g
         }
     }
     if (late_phase >= 0 && tid == 0) {  // the copies still in flight land before the CTA exits
-        mbar_wait(&sm.bar_k, late_phase, nullptr);
+        mbar_wait(&sm.bar_k, k_armed & 1, nullptr);  // the last K phase armed (the earlier ones completed)
         mbar_wait(&sm.bar_v, late_phase, nullptr);
     }
 }
