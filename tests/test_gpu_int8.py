@@ -205,6 +205,27 @@ def test_int8_prompt_widened_decode_count_unknown():
     assert_out_close(out, ref["out"], torch.float32)
 
 
+def test_int8_prompt_widened_many_sequences():
+    """More than 256 sequences (the widening pass's slot prefix gives each
+    thread several), prompt chunks of 9 to 12 rows interleaved with decode
+    rows that are not widened, ragged lengths."""
+    rng = np.random.default_rng(96)
+    seqs = []
+    for i in range(330):
+        if i % 5 == 4:
+            seqs.append((1, int(rng.integers(1, 300))))
+        else:
+            L = int(rng.integers(12, 260))
+            seqs.append((int(rng.integers(9, 13)), L))
+    assert _widen_plan(seqs, True)
+    w = _w("int8_prompt_many", seqs, H=2, G=4, seed=96)
+    x = synth.make_inputs(w)
+    out, sel, nsel = run_forward(w, x)
+    ref = oracle_forward(w, x)
+    assert_selection_equal(sel, nsel, ref)
+    assert_out_close(out, ref["out"], torch.float32)
+
+
 @pytest.mark.parametrize("seqs", [[(300, 2500), (17, 700)], [(1, 3000), (4, 700), (1, 9000)]])
 def test_int8_attend_prefill_both_forms(seqs):
     """msa_attend_prefill on every sequence of the batch: widened once (many
@@ -236,13 +257,14 @@ def test_int8_attend_prefill_given_selection():
     assert_out_close(out, ref["out"], torch.float32)
 
 
-def test_int8_paged_prompt_chunk():
+@pytest.mark.parametrize("page", [64, 256, 1024])
+def test_int8_paged_prompt_chunk(page):
     m = msa()
     w = _w("int8_paged_prompt", [(256, 3000), (1, 900), (40, 200)], seed=92)
     x = synth.make_inputs(w)
-    pl = synth.paged_layout(w, x, 256, seed=12)
+    pl = synth.paged_layout(w, x, page, seed=12)
     pb = m.Problem(w.H, w.G, w.seqs, "cuda", top_k=w.top_k, scale=w.softmax_scale,
-                   block_table=torch.from_numpy(pl["table"]), page_size=256, cache_tokens=pl["num_pages"] * 256,
+                   block_table=torch.from_numpy(pl["table"]), page_size=page, cache_tokens=pl["num_pages"] * page,
                    k_scale=torch.from_numpy(pl["k_scale"]), v_scale=torch.from_numpy(pl["v_scale"]))
     dev = {k: torch.from_numpy(np.ascontiguousarray(pl[k])).cuda() for k in ("k", "v")}
     dq = device_inputs({k: x[k] for k in ("q", "iq")} | {"ik": pl["ik"]})
