@@ -185,6 +185,14 @@ __device__ bool decode_item_warp(const PrefillAttendArgs& a, int it, int lane, W
 
 __device__ __forceinline__ void named_sync_softmax() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 
+// Maximum of v over the 32 lanes of the warp, in every lane (one warp reduction instruction of the
+// sm_100 family; NaN inputs are ignored as by fmaxf, -inf stays -inf).
+__device__ __forceinline__ float warp_max_f32(float v) {
+    float r;
+    asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+    return r;
+}
+
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -520,10 +528,7 @@ __global__ void __launch_bounds__(PaCfg<kKv>::kThreads, 1) prefill_attend_kernel
                 }
             }
 #pragma unroll
-            for (int g = 0; g < 8; ++g) {
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) mx[g] = fmaxf(mx[g], __shfl_xor_sync(0xffffffffu, mx[g], o));
-            }
+            for (int g = 0; g < 8; ++g) mx[g] = warp_max_f32(mx[g]);  // over the warp's 32 keys
             if (lane < 8) {
                 float m = mx[0];
 #pragma unroll
