@@ -185,6 +185,22 @@ __device__ bool decode_item_warp(const PrefillAttendArgs& a, int it, int lane, W
 
 __device__ __forceinline__ void named_sync_softmax() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 
+// Sums of v[0..7] over the warp's 32 lanes by halving exchanges (a reduce-scatter: 9 shuffles
+// instead of 8 x 5): lane l returns the sum of v[(l >> 2) & 7].
+__device__ __forceinline__ float warp_sum8_scatter(const float (&v)[8], int lane) {
+    const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4;
+    float a[4];  // after the exchange over lane bit 4: value (b4 ? 4 : 0) + i
+#pragma unroll
+    for (int i = 0; i < 4; ++i) a[i] = (b4 ? v[i + 4] : v[i]) + __shfl_xor_sync(0xffffffffu, b4 ? v[i] : v[i + 4], 16);
+    float c[2];  // over bit 3: value (b4 ? 4 : 0) + (b3 ? 2 : 0) + i
+#pragma unroll
+    for (int i = 0; i < 2; ++i) c[i] = (b3 ? a[i + 2] : a[i]) + __shfl_xor_sync(0xffffffffu, b3 ? a[i] : a[i + 2], 8);
+    float d = (b2 ? c[1] : c[0]) + __shfl_xor_sync(0xffffffffu, b2 ? c[0] : c[1], 4);  // over bit 2
+    d += __shfl_xor_sync(0xffffffffu, d, 2);
+    d += __shfl_xor_sync(0xffffffffu, d, 1);
+    return d;
+}
+
 // Maximum of v over the 32 lanes of the warp, in every lane (one warp reduction instruction of the
 // sm_100 family; NaN inputs are ignored as by fmaxf, -inf stays -inf).
 __device__ __forceinline__ float warp_max_f32(float v) {
@@ -597,16 +613,21 @@ __global__ void __launch_bounds__(PaCfg<kKv>::kThreads, 1) prefill_attend_kernel
             __syncwarp();
             if (lane == 0) mbar_arrive(&sm.s_empty[sb]);  // S(n) fully read
             if (kInt8 && lane == 0) mbar_arrive(&sm.sc_empty[sb]);  // the item's scales are no longer read
+            if constexpr (!kInt8) {  // (measured: the int8 forms, at 80 registers, ran slower with it)
+                const float hs = warp_sum8_scatter(sum, lane);  // lanes 4g .. 4g + 3: head g's sum
+                if ((lane & 3) == 0) sm.red[quarter][hh * 8 + (lane >> 2)] = hs;
+            } else {
 #pragma unroll
-            for (int g = 0; g < 8; ++g) {
+                for (int g = 0; g < 8; ++g) {
 #pragma unroll
-                for (int o = 16; o > 0; o >>= 1) sum[g] += __shfl_xor_sync(0xffffffffu, sum[g], o);
-            }
-            if (lane < 8) {
-                float m = sum[0];
+                    for (int o = 16; o > 0; o >>= 1) sum[g] += __shfl_xor_sync(0xffffffffu, sum[g], o);
+                }
+                if (lane < 8) {
+                    float m = sum[0];
 #pragma unroll
-                for (int g = 1; g < 8; ++g) m = lane == g ? sum[g] : m;
-                sm.red[quarter][hh * 8 + lane] = m;
+                    for (int g = 1; g < 8; ++g) m = lane == g ? sum[g] : m;
+                    sm.red[quarter][hh * 8 + lane] = m;
+                }
             }
             named_sync_softmax();
             if (n >= 2) mbar_wait(&sm.rs_empty[sb], ((n >> 1) - 1) & 1, a.err);
