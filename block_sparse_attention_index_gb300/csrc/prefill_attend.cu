@@ -117,7 +117,8 @@ struct __align__(1024) AttendSmem {
     uint64_t info_full[kInfoSlots];
     uint64_t info_empty[kInfoSlots];
     ItemInfo info[kInfoSlots];
-    float red[4][16];
+    float red_max[4][16];  // per lane quarter: the heads' maxima, then (a separate array, so that no
+    float red_sum[4][16];  // barrier guards the reuse) their sums
     float rowsum[2][16];
     uint32_t tmem_base;
 };
@@ -549,16 +550,17 @@ __global__ void __launch_bounds__(PaCfg<kKv>::kThreads, 1) prefill_attend_kernel
                 float m = mx[0];
 #pragma unroll
                 for (int g = 1; g < 8; ++g) m = lane == g ? mx[g] : m;
-                sm.red[quarter][hh * 8 + lane] = m;
+                sm.red_max[quarter][hh * 8 + lane] = m;
             }
             named_sync_softmax();
             float ms[8];
 #pragma unroll
             for (int g = 0; g < 8; ++g) {
                 const int hg = hh * 8 + g;
-                ms[g] = fmaxf(fmaxf(sm.red[0][hg], sm.red[1][hg]), fmaxf(sm.red[2][hg], sm.red[3][hg])) * a.scale_log2;
+                ms[g] = fmaxf(fmaxf(sm.red_max[0][hg], sm.red_max[1][hg]), fmaxf(sm.red_max[2][hg], sm.red_max[3][hg])) *
+                        a.scale_log2;
             }
-            named_sync_softmax();  // everyone has its maxima before red is reused
+            // (red_max is written again only in the next item, after the barrier that closes this one)
             // pass 2: P = 2^(s*scale*log2e - max) as bf16 hi + lo, pair by pair
             float sum[8];
 #pragma unroll
@@ -615,7 +617,7 @@ __global__ void __launch_bounds__(PaCfg<kKv>::kThreads, 1) prefill_attend_kernel
             if (kInt8 && lane == 0) mbar_arrive(&sm.sc_empty[sb]);  // the item's scales are no longer read
             if constexpr (!kInt8) {  // (measured: the int8 forms, at 80 registers, ran slower with it)
                 const float hs = warp_sum8_scatter(sum, lane);  // lanes 4g .. 4g + 3: head g's sum
-                if ((lane & 3) == 0) sm.red[quarter][hh * 8 + (lane >> 2)] = hs;
+                if ((lane & 3) == 0) sm.red_sum[quarter][hh * 8 + (lane >> 2)] = hs;
             } else {
 #pragma unroll
                 for (int g = 0; g < 8; ++g) {
@@ -626,13 +628,16 @@ __global__ void __launch_bounds__(PaCfg<kKv>::kThreads, 1) prefill_attend_kernel
                     float m = sum[0];
 #pragma unroll
                     for (int g = 1; g < 8; ++g) m = lane == g ? sum[g] : m;
-                    sm.red[quarter][hh * 8 + lane] = m;
+                    sm.red_sum[quarter][hh * 8 + lane] = m;
                 }
             }
             named_sync_softmax();
             if (n >= 2) mbar_wait(&sm.rs_empty[sb], ((n >> 1) - 1) & 1, a.err);
-            if (tid < 16) sm.rowsum[sb][tid] = sm.red[0][tid] + sm.red[1][tid] + sm.red[2][tid] + sm.red[3][tid];
-            named_sync_softmax();  // red is free again; rowsum written
+            if (tid < 16)
+                sm.rowsum[sb][tid] = sm.red_sum[0][tid] + sm.red_sum[1][tid] + sm.red_sum[2][tid] + sm.red_sum[3][tid];
+            // red_sum is written again only after the next item's first barrier; warp 0's row sums
+            // are ordered before its lane 0's arrival below
+            __syncwarp();
             if (lane == 0) {
                 mbar_arrive(&sm.rs_full[sb]);
                 mbar_arrive(&sm.info_empty[slot]);
