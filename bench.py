@@ -655,11 +655,17 @@ def roofline_for(w, res, hbm, bf16, bf16_sus, peak_kind):
         traffic = (ncu_traffic("prefill_attend_4096_at_8192.md", ["prefill_attend.cu", "common.cuh"])
                    if w.name == "prefill_4096_at_8192" else None)
         executed = wc["att_exec_flops"] / (stage[3] * 1e-3) / 1e12
+        # the indexer's FLOPs counted with the attention's, over both stages (the second figure the
+        # prompt-chunk target is stated for)
+        both = ((wc["att_flops"] + wc["idx_flops"]) / ((stage[2] + stage[3]) * 1e-3) / 1e12
+                if stage[2] > 0 else None)
         return {"kernel": "prefill_attend_kernel", "bound": "tensor", "achieved": round(achieved, 1), "peak": bf16,
                 "unit": "TFLOP/s", "frac": round(achieved / bf16, 4), "traffic": traffic,
                 "traffic_source": _traffic_source("prefill_attend_4096_at_8192.md", traffic),
                 "algorithmic_flops": wc["att_flops"], "executed_flops": wc["att_exec_flops"],
                 "executed_tflops": round(executed, 1), "executed_frac": round(executed / bf16, 4),
+                "with_indexer_flops": wc["att_flops"] + wc["idx_flops"],
+                "with_indexer_frac": round(both / bf16, 4) if both is not None else None,
                 "kernel_us": round(stage[3] * 1e3, 2), "peak_source": f"{peak_kind} bf16_tflops (burst)"}
     return None
 
