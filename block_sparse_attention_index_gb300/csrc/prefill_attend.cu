@@ -185,6 +185,18 @@ __device__ bool decode_item_warp(const PrefillAttendArgs& a, int it, int lane, W
 }
 
 __device__ __forceinline__ void named_sync_softmax() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+// The same barrier, returning the AND of p over the 256 softmax threads (so that a decision to stop,
+// taken after a bounded wait gave up, is the same in every thread and none waits at a later barrier
+// for threads that left).
+__device__ __forceinline__ bool named_sync_softmax_and(bool p) {
+    uint32_t r;
+    asm volatile("{\n\t.reg .pred q, o;\n\tsetp.ne.u32 q, %1, 0;\n\tbar.red.and.pred o, 1, 256, q;\n\t"
+                 "selp.u32 %0, 1, 0, o;\n\t}"
+                 : "=r"(r)
+                 : "r"(static_cast<uint32_t>(p))
+                 : "memory");
+    return r != 0;
+}
 
 // Sums of v[0..7] over the warp's 32 lanes by halving exchanges (a reduce-scatter: 9 shuffles
 // instead of 8 x 5): lane l returns the sum of v[(l >> 2) & 7].
@@ -631,7 +643,7 @@ __global__ void __launch_bounds__(PaCfg<kKv>::kThreads, 1) prefill_attend_kernel
                     sm.red_sum[quarter][hh * 8 + lane] = m;
                 }
             }
-            named_sync_softmax();
+            alive2 = named_sync_softmax_and(alive2);  // every thread stops together
             if (n >= 2) mbar_wait(&sm.rs_empty[sb], ((n >> 1) - 1) & 1, a.err);
             if (tid < 16)
                 sm.rowsum[sb][tid] = sm.red_sum[0][tid] + sm.red_sum[1][tid] + sm.red_sum[2][tid] + sm.red_sum[3][tid];
