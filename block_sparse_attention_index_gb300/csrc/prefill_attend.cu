@@ -50,7 +50,16 @@
 // of each pair), so the MMAs are those of a bf16 cache.  The softmax multiplies each key's scores by its key scale
 // and its weights by its value scale before P enters the PV MMAs (the row
 // sum keeps the plain weights).  The K ring has two slots here, which leaves
-// room for the scales of two items.
+// room for the scales of two items.  When a chunk's rows keep many key rows
+// per position, the positions are widened once per call beforehand
+// (run_widen_kv: bf16 integers and head-major scales in the workspace) and a
+// third form loads those bf16 tiles directly; four warps (17-20) only stage
+// each item's scales.
+//
+// The softmax's cross-lane reductions use one redux.sync.max.f32 per head for
+// the maxima and (bf16 form) a reduce-scatter by halving exchanges for the
+// row sums; its per-head maxima and sums go through separate shared arrays,
+// so two 256-thread barriers an item suffice.
 #include "common.cuh"
 #include "internal.h"
 
